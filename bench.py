@@ -1,0 +1,407 @@
+"""Benchmark of the ZeRO-DP partitioned mixed-precision AdamW step on GB300.
+
+One step = the whole hot path on one batch of synthetic gradients: the reduce-scatter
+arithmetic of N simulated ranks' bf16 gradient copies (with unscale, overflow flag and
+per-tile sums of squares), the global norm / clip / scaler kernel, and the fused AdamW +
+bf16 cast into the gathered parameter layout.  Workload: the GPT-2-1.5B-shaped flat
+buffer (psi = 1,557,611,200, N = 8, ZeRO-2), inputs resident in HBM; its 65 GB working
+set is far larger than the 129 MB L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the build's own baseline) on bounded samples of the
+same workload on the host cores.  Under torchrun (N > 1) every rank runs its own replica
+of the single-GPU step (weak scaling, no collective); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "params updated/s and achieved HBM GB/s (% of ~8 TB/s) for the fused shard step"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+ADAMW_BYTES = 30   # per parameter: g, master, m, v read (16); master, m, v, bf16 written (14)
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks, power and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.t_on = self.t_off = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark(self, on: bool):
+        if on:
+            self.t_on = time.time()
+        else:
+            self.t_off = time.time()
+
+    def stop(self) -> dict:
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = [r for t, r in self.rows if self.t_on and self.t_on - 0.15 <= t <= (self.t_off or t) + 0.15]
+        if not rows:
+            rows = [r for _, r in self.rows]
+        sm = [float(r[1]) for r in rows if len(r) > 8 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if len(r) > 8 and r[2].replace(".", "").isdigit()]
+        pw = [float(r[3]) for r in rows if len(r) > 8 and r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows if len(r) > 8 for i in range(4)
+                          if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+def cpu_oracle_baseline(steps: int = 1, psi_sample: int = 1 << 24):
+    """Time the CPU oracle (as it stands, single-threaded) on a bounded sample of the
+    GPT-2 workload: the same recipe at psi_sample parameters, N = 8; params/s."""
+    import numpy as np
+
+    import oracle
+    import synth
+    from synth import workloads as W
+
+    wl = W.scaled(W.C2, psi_sample, steps=steps)
+    orc = oracle.load()
+    lay = orc.partition(wl.psi, wl.n_ranks, wl.stage)
+    P = lay.psi_padded
+    hp = oracle.hparams(**wl.hp.__dict__)
+    reps = [synth.fill_host(wl.grad_out, wl.grad_kind, wl.grad_key(1, k), 0, P, wl.psi,
+                            wl.grad_sigma) for k in range(wl.n_ranks)]
+    st = [synth.fill_host(synth.OUT_F32, kind, wl.state_key(role), 0, P, wl.psi, sig)
+          for role, kind, sig in ((synth.ROLE_MASTER, synth.NORMAL, wl.master_sigma),
+                                  (synth.ROLE_MOM, synth.NORMAL, wl.mom_sigma),
+                                  (synth.ROLE_VAR, synth.NORMAL_SQ, wl.mom_sigma))]
+    g = np.zeros(P, np.float32)
+    out = np.zeros(P, np.uint16)
+    sc = oracle.scaler(1.0, False, 1000)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        orc.step(lay, hp, oracle.BF16, reps, g, *st, out, sc)
+    dt = time.perf_counter() - t0
+    return wl.psi * steps / dt, dt, wl
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    sample = 1 << 22
+    for _ in range(args.warmup):
+        cpu_oracle_baseline(1, sample)
+    total = 0.0
+    for _ in range(args.steps):
+        _, dt, wl = cpu_oracle_baseline(1, sample)
+        total += dt
+    value = sample * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "params/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": _config(),
+        "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: the GPT-2-1.5B recipe at psi={sample} "
+                                   f"(N=8 bf16 copies, random fp32 state), one oracle step"},
+        "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config(extra=None, psi=None):
+    from synth import workloads as W
+    psi = W.C2.psi if psi is None else psi
+    name = ("GPT-2-1.5B-shaped flat buffer, psi=1,557,611,200" if psi == W.C2.psi else
+            f"GPT-2-1.5B recipe at a reduced psi={psi:,} (profiling case, not the headline)")
+    c = {"workload": name + ", N=8 simulated ranks, ZeRO-2, bf16 gradient copies ~N(0,1e-4), "
+                     "fp32 master/m/v random-init, AdamW lr 1e-3 betas 0.9/0.999 eps 1e-8 "
+                     "wd 0.01 clip 1.0",
+         "psi": psi, "n_ranks": W.C2.n_ranks, "stage": W.C2.stage, "grad_dtype": "bf16",
+         "l2": f"inputs larger than L2 ({(42 * psi) / 1e9:.1f} GB working set vs 129 MB L2); "
+               "no flush needed"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def run_ours(args):
+    import torch
+
+    import synth
+    import zero_partitioned_optimizer_shard_gb300 as z
+    from synth import workloads as W
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = W.C2 if args.psi in (None, W.C2.psi) else W.scaled(W.C2, args.psi)
+    lay = z.zero_partition(wl.psi, wl.n_ranks, wl.stage)
+    P, N = lay.psi_padded, lay.n_ranks
+    hp = z.hparams(**wl.hp.__dict__)
+    stream = torch.cuda.current_stream(dev)
+    s = stream.cuda_stream
+
+    reps = [torch.empty(P, dtype=torch.int16, device=dev) for _ in range(N)]
+    for k, r in enumerate(reps):
+        synth.fill_dev(r.data_ptr(), wl.grad_out, wl.grad_kind, wl.grad_key(1, k), 0, P, wl.psi,
+                       wl.grad_sigma, 1.0, s)
+    master = torch.empty(P, dtype=torch.float32, device=dev)
+    m = torch.empty(P, dtype=torch.float32, device=dev)
+    v = torch.empty(P, dtype=torch.float32, device=dev)
+    for t_, role, kind, sig in ((master, synth.ROLE_MASTER, synth.NORMAL, wl.master_sigma),
+                                (m, synth.ROLE_MOM, synth.NORMAL, wl.mom_sigma),
+                                (v, synth.ROLE_VAR, synth.NORMAL_SQ, wl.mom_sigma)):
+        synth.fill_dev(t_.data_ptr(), synth.OUT_F32, kind, wl.state_key(role), 0, P, wl.psi, sig,
+                       1.0, s)
+    g = torch.empty(P, dtype=torch.float32, device=dev)
+    out = torch.empty(P, dtype=torch.int16, device=dev)
+    partials = torch.empty(lay.n_tiles, dtype=torch.float64, device=dev)
+    st = torch.empty(z.STATE_BYTES, dtype=torch.uint8, device=dev)
+    z.zero_step_state_init(lay, 1.0, False, 1000, st, partials, stream)
+    rep_ptrs = [r.data_ptr() for r in reps]
+
+    def step(ev=None):
+        z.zero_reduce_shard_unscale(lay, z.ZERO_BF16, rep_ptrs, 0, P, g, partials, st, stream)
+        if ev:
+            ev[0].record(stream)
+        z.zero_grad_norm(lay, hp, partials, st, stream)
+        if ev:
+            ev[1].record(stream)
+        z.zero_adamw_cast_gather(lay, hp, g, master, m, v, out, st, stream)
+        if ev:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.mark(True)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    prev = t_start
+    reduce_ms, norm_ms, adamw_ms = [], [], []
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.mark(False)
+    elapsed_ms = t_start.elapsed_time(t_end)
+    for i in range(args.steps):
+        reduce_ms.append(prev.elapsed_time(evs[i][0]))
+        norm_ms.append(evs[i][0].elapsed_time(evs[i][1]))
+        adamw_ms.append(evs[i][1].elapsed_time(evs[i][2]))
+        prev = evs[i][2]
+    if ws > 1:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+        dist.barrier()
+    clk = clocks.stop()
+    stt = z.zero_step_state_read(st, stream)
+    assert stt.t == args.warmup + args.steps and stt.skip == 0 and stt.norm == stt.norm
+
+    # --- end to end through zero_step_host: gradients from pinned host memory -----------
+    e2e = None
+    if not args.no_e2e:
+        e2e = _e2e(args, z, torch, dev, wl, hp, reps, g, partials, master, m, v, out, st, stream)
+
+    peak, peak_kind = _peaks()
+    ms = elapsed_ms / args.steps
+    params_per_s = wl.psi * args.steps * ws / (elapsed_ms / 1e3)
+    bytes_26 = (26 + 2 * N) * P
+    bytes_mat = (34 + 2 * N) * P
+    adamw_avg = statistics.mean(adamw_ms)
+    reduce_avg = statistics.mean(reduce_ms)
+    ach = ADAMW_BYTES * P / (adamw_avg / 1e3) / 1e9
+    red_bytes = (2 * N + 4) * P
+    line = {
+        "metric": METRIC, "value": params_per_s, "unit": "params/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": _config({"parallelism": f"{ws} independent replica(s) of the simulated "
+                                          f"{N}-rank step" if ws > 1 else "1 GPU, 8 simulated ranks"},
+                          psi=wl.psi),
+        "hbm": {
+            "gbs_at_26p2n_bytes": bytes_26 / (ms / 1e3) / 1e9,
+            "pct_of_8tbs": 100 * bytes_26 / (ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+            "pct_of_measured_peak": 100 * bytes_26 / (ms / 1e3) / 1e9 / peak,
+            "gbs_at_34p2n_bytes_moved": bytes_mat / (ms / 1e3) / 1e9,
+            "note": "(26+2N) B/param is the headline roofline; an exact step must also write "
+                    "and re-read the fp32 gradient (34+2N) because clipping needs the global "
+                    "norm before any update",
+        },
+        "roofline": {
+            "kernel": "k_adamw (fused AdamW + bf16 cast + gathered write)",
+            "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+            "peak_kind": peak_kind + ", burst figure of a kernel timed alone",
+            "traffic": _traffic_from_profile(), "bytes_per_launch": ADAMW_BYTES * P,
+            "avg_launch_ms": adamw_avg,
+        },
+        "kernels": {
+            "k_reduce": {"avg_ms": reduce_avg, "bytes_per_launch": red_bytes,
+                         "gbs": red_bytes / (reduce_avg / 1e3) / 1e9},
+            "k_finalize": {"avg_ms": statistics.mean(norm_ms)},
+            "k_adamw": {"avg_ms": adamw_avg, "bytes_per_launch": ADAMW_BYTES * P, "gbs": ach},
+        },
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+        "e2e": e2e,
+        "final_state": {"t": stt.t, "norm": stt.norm, "clip_coef": stt.clip_coef},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        v, dt, swl = cpu_oracle_baseline(1, 1 << 24)
+        line["cpu_baseline"] = {"value": v, "unit": "params/s", "cores": 1, "kind": "oracle",
+                                "sample": f"one oracle step of the GPT-2-1.5B recipe at psi={swl.psi} "
+                                          f"(N=8 bf16 copies, random fp32 state), {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def _traffic_from_profile():
+    """DRAM bytes per k_adamw launch from the committed ncu summary, if current."""
+    path = os.path.join(ROOT, "profiles", "k_adamw_traffic.json")
+    try:
+        with open(path) as f:
+            return json.load(f).get("traffic_bytes_per_launch_full_size")
+    except Exception:
+        return None
+
+
+def _e2e(args, z, torch, dev, wl, hp, reps, g, partials, master, m, v, out, st, stream):
+    P, N = reps[0].numel(), len(reps)
+    need = N * P * 2
+    try:
+        avail = int([l for l in open("/proc/meminfo") if l.startswith("MemAvailable")][0].split()[1]) * 1024
+    except Exception:
+        avail = 0
+    if avail < 2 * need:
+        return {"value": None, "unit": "params/s", "h2d_bytes_per_step": need,
+                "d2h_bytes_per_step": z.STATE_BYTES, "note": f"skipped: {avail/1e9:.0f} GB host RAM free"}
+    W = 1 << 26
+    lay = z.zero_partition(wl.psi, wl.n_ranks, wl.stage, 1, W)
+    hreps = [torch.empty(P, dtype=torch.int16, pin_memory=True) for _ in range(N)]
+    for h, r in zip(hreps, reps):
+        h.copy_(r)
+    staging = torch.empty(2 * N * W, dtype=torch.int16, device=dev)
+    hstate = torch.empty(z.STATE_BYTES, dtype=torch.uint8, pin_memory=True)
+    cs = torch.cuda.Stream(dev)
+    steps = max(1, args.e2e_steps)
+    z.zero_step_host(lay, hp, z.ZERO_BF16, hreps, staging, staging.numel() * 2, g, partials,
+                     master, m, v, out, st, hstate, stream, cs)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        z.zero_step_host(lay, hp, z.ZERO_BF16, hreps, staging, staging.numel() * 2, g, partials,
+                         master, m, v, out, st, hstate, stream, cs)
+        stream.synchronize()  # the step's result (norm, flag, scale) is on the host
+    dt = time.perf_counter() - t0
+    return {"value": wl.psi * steps / dt, "unit": "params/s", "h2d_bytes_per_step": need,
+            "d2h_bytes_per_step": z.STATE_BYTES, "steps": steps, "ms_per_step": dt / steps * 1e3,
+            "path": "zero_step_host: N pinned host gradient copies -> 2 x 64M-element staging "
+                    "ring (H2D on a copy stream, overlapped with the bucket reduces) -> norm -> "
+                    "AdamW; step state copied back to pinned host memory"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--psi", type=int, default=None,
+                    help="profiling only: the same recipe at another size (default: the "
+                         "GPT-2-1.5B buffer)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    if args.impl == "reference":
+        return run_reference(args)
+    import fcntl
+
+    import __graft_entry__
+    os.makedirs(os.path.join(ROOT, "_build"), exist_ok=True)
+    with open(os.path.join(ROOT, "_build", ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)  # ranks of one node build once, in turn
+        __graft_entry__.build()
+        fcntl.flock(lock, fcntl.LOCK_UN)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,265 @@
+/*
+ * zero.h -- C ABI of the GB300 (sm_103a) ZeRO-DP partitioned mixed-precision AdamW step.
+ *
+ * One optimizer step of ZeRO-DP data parallelism with all N data-parallel ranks held as
+ * buffers on one GPU:
+ *   1. partition      Psi flat parameters into N equal, padded shards (rank r owns
+ *                     flat [r*S, (r+1)*S)), with the per-rank model-state ledger
+ *   2. reduce-scatter average the N ranks' fp16/bf16 gradient copies into fp32, remove
+ *                     the loss scale, flag inf/NaN, and sum g^2 per rank-local tile
+ *   3. grad norm      global L2 norm of the averaged gradient, clip coefficient,
+ *                     loss-scale update and the skip decision, all on the device
+ *   4. AdamW + cast   update the fp32 master / momentum / variance of every shard and
+ *                     write each shard's bf16 parameters at its own offset r*S of one
+ *                     gathered buffer (the layout the parameter all-gather produces)
+ *
+ * Sources (web pages on ZeRO):
+ *   [ZW] "【论文解读】ZeRO", wkq9411.github.io: sec. 4(1)-(3) the three partitioning stages,
+ *        sec. 6(1)-(2) reduce-scatter / all-gather and the 8-parameter, 4-GPU example
+ *   [ZM] "ZeRO 显存优化：ZeRO-1、ZeRO-2 与 ZeRO-3", xiangdong0520.pages.dev: sec. 2-3 ledger
+ *   [ZS] operatorworld.com ZeRO optimizer-sharding article: AdamW 16-byte ledger (bf16
+ *        weights and gradients), stage flows, communication accounting
+ *   [ZO] "3、ZeRO技术概述：ZeRO三个阶段原理与对比", 5688vip.com: stage-2 iteration flow,
+ *        DeepSpeed config with "fp16": enabled
+ *   [MD] gitcode.csdn.net article on Megatron's distributed optimizer: sec. 1 global
+ *        grad-norm all-reduce before clip_coeff
+ *
+ * Conventions for every function below:
+ *   - Ownership: the caller allocates and frees every buffer.  No function allocates or
+ *     frees device memory; zero_step_host creates and destroys four CUDA events.
+ *   - Device pointers must be 16-byte aligned (ZERO_EALIGN otherwise).
+ *   - Asynchrony: device work is enqueued on the caller's stream and the call returns
+ *     without waiting, except zero_step_state_read / zero_step_state_write, which wait.
+ *   - Errors: arguments are validated on the host before anything is enqueued; a
+ *     rejected call changes nothing.  A launch failure returns ZERO_ECUDA and
+ *     zero_last_cuda_error() gives the CUDA error code.  Faults inside kernels surface at
+ *     the caller's next synchronisation.  Overflow of the gradients is not an error: it
+ *     is reported in the step state and the step is skipped.
+ *   - Thread safety: calls on different streams may run concurrently if they share no
+ *     buffers.
+ */
+#ifndef ZERO_H
+#define ZERO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA runtime's cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* zero_stream_t;
+
+#define ZERO_OK 0
+#define ZERO_EINVAL (-1)   /* invalid argument */
+#define ZERO_EALIGN (-2)   /* pointer or window not aligned as required */
+#define ZERO_ENOMEM (-3)   /* caller-provided buffer too small */
+#define ZERO_ECUDA (-4)    /* CUDA launch or copy failed; see zero_last_cuda_error() */
+#define ZERO_ETIMEOUT (-5) /* reserved for bounded device waits (none wait today) */
+
+typedef enum zero_dtype { ZERO_F16 = 1, ZERO_BF16 = 2 } zero_dtype_t;
+
+#define ZERO_MAX_RANKS (1u << 20)   /* zero_partition (ledger and layout) */
+#define ZERO_MAX_KERNEL_RANKS 64u   /* device entry points: replicas summed per element */
+#define ZERO_TILE_ELEMS 8192u       /* rank-local tile of the sum-of-squares partials */
+
+/* Partition of Psi flat parameters over N ranks.  Filled by zero_partition; pass it back
+ * unchanged to the device entry points (they re-check its invariants). */
+typedef struct zero_layout {
+    uint64_t psi;                    /* Psi: parameters */
+    uint64_t shard;                  /* S = ceil(Psi/N) rounded up to align: elements per rank */
+    uint64_t psi_padded;             /* N*S: length of every flat buffer */
+    uint64_t pad;                    /* N*S - Psi: trailing padding, gradient 0, output 0 */
+    uint64_t bucket_elems;           /* W: window of one reduce launch in zero_step */
+    uint64_t n_buckets;              /* ceil(N*S / W) */
+    uint64_t tiles_per_rank;         /* ceil(S / tile_elems) */
+    uint64_t n_tiles;                /* N * tiles_per_rank: fp64 partial slots */
+    uint64_t bytes_per_rank[4];      /* model-state bytes per rank: [0] plain DP 16*Psi,
+                                        [1] 4*N*S + 12*S, [2] 2*N*S + 14*S, [3] 16*S */
+    uint64_t comm_elems_per_rank[4]; /* elements each rank sends per step on a ring:
+                                        2(N-1)S for [0..2], 3(N-1)S for stage 3 */
+    uint32_t n_ranks;                /* N */
+    uint32_t stage;                  /* 0 plain DP, 1 P_os, 2 P_os+g, 3 P_os+g+p */
+    uint32_t align;                  /* S is a multiple of align */
+    uint32_t tile_elems;             /* ZERO_TILE_ELEMS */
+} zero_layout_t;
+
+typedef struct zero_adamw_hparams {
+    float lr;
+    float beta1;            /* in [0, 1) */
+    float beta2;            /* in [0, 1) */
+    float eps;              /* > 0 */
+    float weight_decay;     /* decoupled: p *= 1 - lr*weight_decay */
+    float max_grad_norm;    /* global-norm clip threshold; <= 0 disables clipping */
+} zero_adamw_hparams_t;
+
+/* Scalar step state.  Lives in DEVICE memory (caller allocates sizeof(zero_step_state_t)
+ * bytes, 16-byte aligned); read it with zero_step_state_read. */
+typedef struct zero_step_state {
+    double sumsq;           /* sum of g^2 of the last finalised step (fp64) */
+    double norm;            /* its square root: the global L2 gradient norm */
+    float clip_coef;        /* c applied by the last finalised step (1 when skipped) */
+    float loss_scale;       /* L of the NEXT step's gradients */
+    float inv_scale;        /* f32(1 / (N*L)): the reduce's unscale factor */
+    float step_size;        /* lr / (1 - beta1^t) for the step being applied */
+    float rbc2;             /* sqrt(1 - beta2^t) */
+    float decay;            /* 1 - lr*weight_decay */
+    uint32_t overflow;      /* non-finite seen by this step's reduce windows so far */
+    uint32_t skip;          /* 1 if the last finalised step was skipped (overflow) */
+    uint32_t t;             /* applied optimizer steps */
+    uint32_t good_steps;    /* consecutive applied steps since the last scale change */
+    uint32_t growth_interval;
+    uint32_t dynamic;       /* 1: dynamic loss scale (halve on overflow, double every
+                               growth_interval good steps, floor 1, cap 2^24) */
+    uint32_t n_ranks;
+    uint32_t n_steps;       /* finalised steps, applied or skipped */
+    uint32_t n_skipped;
+    uint32_t error;         /* device error word, 0 = none (reserved) */
+    uint32_t reserved[12];
+} zero_step_state_t;        /* 128 bytes */
+
+/* -------------------------------------------------------------------------------------
+ * zero_partition -- host only, no CUDA call.
+ * [ZW] sec. 4(1)-(3): N equal partitions, rank r owns partition r; the ledger per stage
+ * ([ZW] sec. 2(1) and 8, [ZM] sec. 3): 16*Psi, (4 + 12/N)Psi, (2 + 14/N)Psi, 16*Psi/N,
+ * counted on the padded buffers; the ring traffic of [ZW] sec. 6 eq. dp-comm.
+ *   psi           >= 1, <= 2^56
+ *   n_ranks       1 .. ZERO_MAX_RANKS
+ *   stage         0 .. 3 (0 = plain data parallelism, for the ledger only)
+ *   align         S is rounded up to a multiple of align (1 .. 2^20)
+ *   bucket_elems  window of one reduce launch in zero_step; 0 = one window over the
+ *                 whole flat buffer; otherwise a multiple of 8
+ *   out           written on success
+ * Returns ZERO_OK or ZERO_EINVAL.
+ * ------------------------------------------------------------------------------------- */
+int zero_partition(uint64_t psi, uint32_t n_ranks, uint32_t stage, uint32_t align,
+                   uint64_t bucket_elems, zero_layout_t* out);
+
+/* Bytes of the fp64 partials workspace the device entry points need:
+ * layout->n_tiles * 8.  0 for an invalid layout. */
+size_t zero_workspace_bytes(const zero_layout_t* layout);
+
+/* -------------------------------------------------------------------------------------
+ * zero_step_state_init -- start a fresh optimizer (t = 0) on the device.
+ *   loss_scale       initial L (> 0, finite); 1 for bf16 training
+ *   dynamic          1: dynamic loss scaling (fp16 training, [ZO] "fp16": enabled);
+ *                    0: static scale, overflow still skips the step
+ *   growth_interval  good steps between doublings of a dynamic scale (0 = never)
+ *   st               device, sizeof(zero_step_state_t)
+ *   partials         device, zero_workspace_bytes(layout); zeroed here
+ * Enqueues one kernel on `stream`.
+ * ------------------------------------------------------------------------------------- */
+int zero_step_state_init(const zero_layout_t* layout, float loss_scale, uint32_t dynamic,
+                         uint32_t growth_interval, zero_step_state_t* st, double* partials,
+                         zero_stream_t stream);
+
+/* Copy the device state to host memory and wait for it (checkpoints, monitoring). */
+int zero_step_state_read(const zero_step_state_t* st, zero_step_state_t* host_out,
+                         zero_stream_t stream);
+
+/* Copy a host state (e.g. from a checkpoint) to the device and wait for it. */
+int zero_step_state_write(zero_step_state_t* st, const zero_step_state_t* host_in,
+                          zero_stream_t stream);
+
+/* -------------------------------------------------------------------------------------
+ * zero_reduce_shard_unscale -- the reduce-scatter arithmetic on one flat window.
+ * [ZW] sec. 6(1)-(2): the ranks' gradients are averaged; with gradient partitioning the
+ * average is reduce-scattered so rank r receives only flat [r*S, (r+1)*S).  [ZW] sec. 4(2):
+ * gradients are bucketed and each bucket reduced as it becomes ready.
+ * For every flat i in [begin, begin+count):
+ *   g[i] = (sum over k = 0..N-1, ascending, in fp32, of x_k[i]) * st->inv_scale
+ *   with g[i] = 0 for padding (i >= psi; replica values there are ignored);
+ *   st->overflow |= any non-finite g[i];
+ *   partials[tile of i] += sum of g^2 over the window's part of each rank-local tile
+ *   (tile j of rank r = flat r*S + [j*T, min((j+1)*T, S)), T = tile_elems).
+ *   dtype      ZERO_F16 or ZERO_BF16 (the replicas' element type)
+ *   replicas   HOST array of N DEVICE pointers; replicas[k] points at flat element
+ *              `begin` of rank k's gradient copy and holds at least `count` elements
+ *   begin      multiple of 8 (ZERO_EALIGN otherwise); begin + count <= psi_padded
+ *   g          DEVICE fp32 array of psi_padded elements (indexed by the flat index)
+ *   partials   DEVICE, zero_workspace_bytes(layout); zeroed by zero_step_state_init and
+ *              by every zero_grad_norm, accumulated here
+ *   st         DEVICE step state
+ * N must be <= ZERO_MAX_KERNEL_RANKS.  Windows of one step may come in any order but
+ * must not overlap; together they must cover [0, psi_padded) before zero_grad_norm.
+ * ------------------------------------------------------------------------------------- */
+int zero_reduce_shard_unscale(const zero_layout_t* layout, zero_dtype_t dtype,
+                              const void* const* replicas, uint64_t begin, uint64_t count,
+                              float* g, double* partials, zero_step_state_t* st,
+                              zero_stream_t stream);
+
+/* -------------------------------------------------------------------------------------
+ * zero_grad_norm -- global norm, clip coefficient, loss scaler and skip decision.
+ * [MD] sec. 1: inside optimizer.step(), before clipping, one all-reduce forms the global
+ * L2 gradient norm that sets clip_coeff.  Here the all-reduce is the fixed-order sum of
+ * the per-rank partial sums (each rank's tiles, then ranks in order):
+ *   norm = sqrt(sumsq);  c = min(1, max_norm / (norm + 1e-6)) (fp64, rounded to fp32)
+ *   overflow: skip = 1, c = 1, t unchanged, dynamic L = max(L/2, 1)
+ *   else:     skip = 0, t += 1, step_size = f32(lr/(1-beta1^t)), rbc2 = f32(sqrt(1-beta2^t)),
+ *             decay = f32(1 - lr*wd); dynamic L doubles after growth_interval good steps
+ *   inv_scale = f32(1/(N*L)) for the next step; overflow flag and partials reset to 0.
+ * One single-block kernel; no host synchronisation.
+ * ------------------------------------------------------------------------------------- */
+int zero_grad_norm(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,
+                   double* partials, zero_step_state_t* st, zero_stream_t stream);
+
+/* -------------------------------------------------------------------------------------
+ * zero_adamw_cast_gather -- fused AdamW on every shard plus the bf16 gathered write.
+ * [ZW] sec. 6(2): each rank updates its own parameters from its own reduced gradient and
+ * the all-gather rebuilds [p0' ... p7'] in order; [ZS]: AdamW, bf16 weights.
+ * Does nothing (on the device) when st->skip.  Otherwise, per flat i < psi, in fp32:
+ *   gc = c*g;  m = b1*m + (1-b1)*gc;  v = b2*v + (1-b2)*(gc*gc)
+ *   p  = p*decay - step_size * (m / (sqrt(v)/rbc2 + eps));  params[i] = bf16_rne(p)
+ * and params[i] = 0 for padding (master/m/v there untouched).
+ *   g, master, m, v   DEVICE fp32, psi_padded elements each (master/m/v updated in place)
+ *   params            DEVICE bf16 bit patterns (uint16), psi_padded elements
+ *   hp                must equal the hp given to zero_grad_norm for this step
+ * ------------------------------------------------------------------------------------- */
+int zero_adamw_cast_gather(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,
+                           const float* g, float* master, float* m, float* v, uint16_t* params,
+                           const zero_step_state_t* st, zero_stream_t stream);
+
+/* -------------------------------------------------------------------------------------
+ * zero_step -- one whole step: every bucket's reduce, the norm, AdamW + cast.
+ *   replicas   HOST array of n_buckets * N DEVICE pointers, bucket-major:
+ *              replicas[b*N + k] holds rank k's gradient for flat
+ *              [b*W, min((b+1)*W, psi_padded)).  With n_buckets = 1 these are simply
+ *              the N full gradient copies.
+ *   other arguments as in the three calls above.  3 + n_buckets - 1 kernel launches.
+ * ------------------------------------------------------------------------------------- */
+int zero_step(const zero_layout_t* layout, const zero_adamw_hparams_t* hp, zero_dtype_t dtype,
+              const void* const* replicas, float* g, double* partials, float* master, float* m,
+              float* v, uint16_t* params, zero_step_state_t* st, zero_stream_t stream);
+
+/* -------------------------------------------------------------------------------------
+ * zero_step_host -- zero_step with the gradients in HOST memory.
+ * The N gradient copies arrive from pinned host memory, one bucket of W elements at a
+ * time, through a two-slot device staging ring: the copy of bucket b+1 (on copy_stream,
+ * one cudaMemcpyAsync per rank) overlaps the reduce of bucket b (on stream).
+ *   host_replicas   HOST array of N HOST pointers (pinned for overlap), each psi_padded
+ *                   elements of dtype
+ *   staging         DEVICE buffer of staging_bytes >= 2 * N * W * sizeof(dtype)
+ *   host_state_out  optional HOST pointer (pinned): the step state is copied there at
+ *                   the end of the step on `stream` (the caller synchronises)
+ *   copy_stream     must differ from stream
+ * Returns ZERO_ENOMEM if staging is too small.
+ * ------------------------------------------------------------------------------------- */
+int zero_step_host(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,
+                   zero_dtype_t dtype, const void* const* host_replicas, void* staging,
+                   uint64_t staging_bytes, float* g, double* partials, float* master, float* m,
+                   float* v, uint16_t* params, zero_step_state_t* st,
+                   zero_step_state_t* host_state_out, zero_stream_t stream,
+                   zero_stream_t copy_stream);
+
+/* Text for a status code. */
+const char* zero_strerror(int status);
+
+/* cudaError_t of the last ZERO_ECUDA returned on this thread (0 if none). */
+int zero_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZERO_H */

@@ -1,0 +1,192 @@
+"""Test harness: the ZeRO step on the GPU through the C ABI, and the same step in the oracle.
+
+GpuRun keeps every device buffer between canary guard zones (4 KiB of 0xA5 before and
+after, plus the slack up to the next 256 bytes) so any out-of-bounds write by a kernel
+shows up in check_guards(), with no sanitizer.  Gradients are regenerated each step from
+the seeded generator: on the device for GpuRun, on the host for OracleRun, bit-identical.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import synth
+import zero_partitioned_optimizer_shard_gb300 as z
+
+GUARD = 4096
+CANARY = 0xA5
+_ESZ = {torch.float32: 4, torch.float64: 8, torch.int16: 2, torch.uint8: 1}
+
+
+def dtype_code(wl) -> int:
+    return z.ZERO_F16 if wl.grad_dtype == "f16" else z.ZERO_BF16
+
+
+class GpuRun:
+    def __init__(self, wl, bucket_elems: int = 0, device: str = "cuda:0", guarded: bool = True,
+                 hp=None):
+        self.wl = wl
+        self.dev = torch.device(device)
+        self.stream = torch.cuda.current_stream(self.dev)
+        self.guarded = guarded
+        self._raw = []
+        self.lay = z.zero_partition(wl.psi, wl.n_ranks, wl.stage, 1, bucket_elems)
+        P = self.lay.psi_padded
+        self.hp = hp if hp is not None else z.hparams(**wl.hp.__dict__)
+        self.reps = [self.alloc(P, torch.int16) for _ in range(wl.n_ranks)]
+        self.g = self.alloc(P, torch.float32)
+        self.master = self.alloc(P, torch.float32)
+        self.m = self.alloc(P, torch.float32)
+        self.v = self.alloc(P, torch.float32)
+        self.out = self.alloc(P, torch.int16)
+        self.partials = self.alloc(max(self.lay.n_tiles, 1), torch.float64)
+        self.st = self.alloc(z.STATE_BYTES, torch.uint8)
+        self._fill(self.master, synth.OUT_F32, synth.NORMAL, wl.state_key(synth.ROLE_MASTER),
+                   wl.master_sigma)
+        if wl.random_moments:
+            self._fill(self.m, synth.OUT_F32, synth.NORMAL, wl.state_key(synth.ROLE_MOM), wl.mom_sigma)
+            self._fill(self.v, synth.OUT_F32, synth.NORMAL_SQ, wl.state_key(synth.ROLE_VAR),
+                       wl.mom_sigma)
+        else:
+            self.m.zero_()
+            self.v.zero_()
+        self.out.zero_()
+        z.zero_step_state_init(self.lay, wl.loss_scale, wl.dynamic, wl.growth_interval, self.st,
+                               self.partials, self.stream)
+
+    def alloc(self, n: int, dtype) -> torch.Tensor:
+        nbytes = n * _ESZ[dtype]
+        if not self.guarded:
+            return torch.empty(n, dtype=dtype, device=self.dev)
+        body = (nbytes + 255) // 256 * 256
+        raw = torch.full((GUARD + body + GUARD,), CANARY, dtype=torch.uint8, device=self.dev)
+        self._raw.append((raw, nbytes))
+        return raw[GUARD:GUARD + nbytes].view(dtype)
+
+    def check_guards(self) -> None:
+        torch.cuda.synchronize(self.dev)
+        for raw, nbytes in self._raw:
+            assert bool(torch.all(raw[:GUARD] == CANARY)), "write before a buffer"
+            assert bool(torch.all(raw[GUARD + nbytes:] == CANARY)), "write past a buffer"
+
+    def _fill(self, t, out, kind, key, sigma, scale=1.0, begin=0, count=None):
+        count = t.numel() if count is None else count
+        synth.fill_dev(t.data_ptr(), out, kind, key, begin, count, self.wl.psi, sigma, scale,
+                       self.stream.cuda_stream)
+
+    def state(self) -> z.StepState:
+        return z.zero_step_state_read(self.st, self.stream)
+
+    def gen_grads(self, step: int) -> float:
+        """Fill the N gradient copies for `step` at the current loss scale; returns L."""
+        L = self.state().loss_scale
+        wl = self.wl
+        for k, r in enumerate(self.reps):
+            self._fill(r, wl.grad_out, wl.grad_kind, wl.grad_key(step, k), wl.grad_sigma, L)
+        inj = wl.injection(step)
+        if inj:
+            rank, idx, bits = inj
+            self.reps[rank][idx] = int(np.uint16(bits).view(np.int16))
+        return L
+
+    def bucket_ptrs(self):
+        W, N, P = self.lay.bucket_elems, self.lay.n_ranks, self.lay.psi_padded
+        return [self.reps[k].data_ptr() + 2 * b * W for b in range(self.lay.n_buckets) for k in range(N)]
+
+    def step(self, step: int) -> z.StepState:
+        self.gen_grads(step)
+        z.zero_step(self.lay, self.hp, dtype_code(self.wl), self.bucket_ptrs(), self.g,
+                    self.partials, self.master, self.m, self.v, self.out, self.st, self.stream)
+        return self.state()
+
+    def arrays(self) -> dict:
+        torch.cuda.synchronize(self.dev)
+        return dict(g=self.g.cpu().numpy(), master=self.master.cpu().numpy(),
+                    m=self.m.cpu().numpy(), v=self.v.cpu().numpy(),
+                    out=self.out.cpu().numpy().view(np.uint16))
+
+
+class OracleRun:
+    def __init__(self, wl, hp=None):
+        self.wl = wl
+        self.orc = oracle.load()
+        self.lay = self.orc.partition(wl.psi, wl.n_ranks, wl.stage)
+        P = self.lay.psi_padded
+        self.hp = hp if hp is not None else oracle.hparams(**wl.hp.__dict__)
+        f = lambda role, kind, sigma: synth.fill_host(synth.OUT_F32, kind, wl.state_key(role), 0, P,
+                                                      wl.psi, sigma)
+        self.master = f(synth.ROLE_MASTER, synth.NORMAL, wl.master_sigma)
+        if wl.random_moments:
+            self.m = f(synth.ROLE_MOM, synth.NORMAL, wl.mom_sigma)
+            self.v = f(synth.ROLE_VAR, synth.NORMAL_SQ, wl.mom_sigma)
+        else:
+            self.m = np.zeros(P, np.float32)
+            self.v = np.zeros(P, np.float32)
+        self.g = np.zeros(P, np.float32)
+        self.out = np.zeros(P, np.uint16)
+        self.sc = oracle.scaler(wl.loss_scale, wl.dynamic, wl.growth_interval)
+
+    def grads(self, step: int):
+        wl, P = self.wl, self.lay.psi_padded
+        reps = [synth.fill_host(wl.grad_out, wl.grad_kind, wl.grad_key(step, k), 0, P, wl.psi,
+                                wl.grad_sigma, self.sc.loss_scale) for k in range(wl.n_ranks)]
+        inj = wl.injection(step)
+        if inj:
+            reps[inj[0]][inj[1]] = inj[2]
+        return reps
+
+    def step(self, step: int):
+        dt = oracle.F16 if self.wl.grad_dtype == "f16" else oracle.BF16
+        return self.orc.step(self.lay, self.hp, dt, self.grads(step), self.g, self.master, self.m,
+                             self.v, self.out, self.sc)
+
+    def arrays(self) -> dict:
+        return dict(g=self.g, master=self.master, m=self.m, v=self.v, out=self.out)
+
+
+# tolerances: the stated ones (1e-5 relative on master/m/v and the norm, 1 bf16 ulp on the
+# gathered parameters); exact zeros use an absolute floor of 1e-30.
+REL = 1e-5
+FLOOR = 1e-30
+
+
+def assert_state_close(got: dict, want: dict, psi: int, exact_expected: bool = True) -> dict:
+    """Compare GPU and oracle arrays; returns counts of exact matches per array."""
+    stats = {}
+    ga_, gw_ = got["g"], want["g"]
+    # bit-exact, except that any NaN matches any NaN (payloads are not part of the result)
+    same = (ga_.view(np.uint32) == gw_.view(np.uint32)) | (np.isnan(ga_) & np.isnan(gw_))
+    assert same.all(), f"g differs at {np.flatnonzero(~same)[:8]}"
+    for k in ("master", "m", "v"):
+        a, b = got[k], want[k]
+        bad = ~(np.abs(a.astype(np.float64) - b) <= REL * np.abs(b.astype(np.float64)) + FLOOR)
+        assert not bad.any(), f"{k}: {bad.sum()} elements beyond tolerance, e.g. " \
+                              f"{np.flatnonzero(bad)[:5]} {a[bad][:3]} vs {b[bad][:3]}"
+        stats[k] = int(np.sum(a.view(np.uint32) == b.view(np.uint32)))
+        assert np.array_equal(a[psi:].view(np.uint32), b[psi:].view(np.uint32))  # pads untouched
+    ga, wa = got["out"], want["out"]
+    ulp = np.abs(bf16_ordinal(ga) - bf16_ordinal(wa))
+    assert ulp.max(initial=0) <= 1, f"bf16 params differ by {ulp.max()} ulp"
+    assert np.all(ga[psi:] == 0) and np.all(wa[psi:] == 0)
+    stats["out"] = int(np.sum(ga == wa))
+    if exact_expected:
+        n = ga.size
+        assert stats["master"] == stats["m"] == stats["v"] == stats["out"] == n, stats
+    return stats
+
+
+def bf16_ordinal(bits: np.ndarray) -> np.ndarray:
+    """Map bf16 bit patterns to integers that are consecutive for adjacent values."""
+    b = bits.astype(np.int64)
+    return np.where(b & 0x8000, -(b & 0x7FFF), b)
+
+
+def assert_scalars(s: z.StepState, rep, rel_norm: float = REL) -> None:
+    assert s.overflow == 0
+    assert s.skip == rep.skipped and s.t == rep.t
+    assert s.loss_scale == rep.loss_scale_next
+    if not rep.skipped:
+        assert abs(s.norm - rep.norm) <= rel_norm * rep.norm, (s.norm, rep.norm)
+        assert s.clip_coef == rep.clip_coef or \
+            abs(s.clip_coef - rep.clip_coef) <= 2 ** -23 * rep.clip_coef, (s.clip_coef, rep.clip_coef)

@@ -1,0 +1,294 @@
+"""GPU path vs the CPU oracle, element by element, through the C ABI (needs a GB300).
+
+Sizes here are ones the oracle finishes in seconds while still spanning many 8192-element
+tiles, shard boundaries in the middle of tiles and a padded ragged tail.  Expectations:
+the reduced gradient g, indices, pads, flags, the skip decision and the loss-scale
+sequence bit-exact; master/m/v within 1e-5 relative (and in practice bit-exact, since both
+sides evaluate the same fp32 operations in the same order); the gathered bf16 parameters
+within 1 ulp; the norm within 1e-5 relative.
+"""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+import zero_partitioned_optimizer_shard_gb300 as z
+from synth import workloads as W
+from tests.gpu_harness import GpuRun, OracleRun, assert_scalars, assert_state_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available()
+
+
+def _run_pair(wl, steps, bucket_elems=0, check_every=True):
+    gpu = GpuRun(wl, bucket_elems)
+    orc = OracleRun(wl)
+    for s in range(1, steps + 1):
+        st = gpu.step(s)
+        rep = orc.step(s)
+        assert_scalars(st, rep)
+        if check_every or s == steps:
+            exact = st.clip_coef == rep.clip_coef
+            assert_state_close(gpu.arrays(), orc.arrays(), wl.psi, exact_expected=exact)
+    gpu.check_guards()
+    return gpu, orc
+
+
+def test_c1_full_size():
+    """C1 exactly: psi = 1,000,003 (odd; the last shard carries one pad), N = 4, fp16."""
+    gpu, orc = _run_pair(W.C1, 1)
+    s = gpu.state()
+    assert s.t == 1 and s.skip == 0 and s.loss_scale == 1024.0 and s.n_steps == 1
+    assert 0.45 < s.norm < 0.55 and s.clip_coef == 1.0  # clipping inactive in C1
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 7, 8, 16, 17, 33, 64])
+def test_tiny_and_ragged(n):
+    """Degenerate sizes: N > psi, one-element shards, shards of < 8 elements, 64 ranks."""
+    for psi in (1, 2, 3, 7, 8, 9, 15, 16, 17, 31, 33, 63, 64, 65, 100, 257, 8195):
+        dt = "f16" if (psi + n) % 2 else "bf16"
+        wl = replace(W.scaled(W.C1, psi, steps=2), n_ranks=n, grad_dtype=dt,
+                     loss_scale=1024.0 if dt == "f16" else 1.0, dynamic=dt == "f16",
+                     random_moments=bool(psi % 3))
+        _run_pair(wl, 2)
+
+
+def test_tiles_shards_windows_bucketed_equals_whole():
+    """Bucketed windows (tile pieces reduced in several launches) give the same bits."""
+    psi = 4 * 3 * 8192 + 12345
+    wl = replace(W.scaled(W.C2, psi, steps=2), n_ranks=4)
+    ref, _ = _run_pair(wl, 2)
+    want = ref.arrays()
+    want_state = ref.state()
+    for W_ in (8, 1000, 8192, 3 * 8192 + 8, psi // 3 // 8 * 8):
+        got, _ = _run_pair(wl, 2, bucket_elems=W_, check_every=False)
+        a = got.arrays()
+        s = got.state()
+        # tile pieces add up in another fp64 order: the norm may move in its last bits
+        assert abs(s.norm - want_state.norm) <= 1e-13 * want_state.norm
+        assert np.array_equal(a["g"].view(np.uint8), want["g"].view(np.uint8))
+        if s.clip_coef == want_state.clip_coef:
+            for k in want:
+                assert np.array_equal(a[k].view(np.uint8), want[k].view(np.uint8)), (W_, k)
+
+
+def test_reduce_windows_in_any_order():
+    """The three entry points called directly, windows given out of order."""
+    psi = 2 * 8192 * 5 + 77
+    wl = replace(W.scaled(W.C2, psi, steps=1), n_ranks=5)
+    gpu = GpuRun(wl)
+    orc = OracleRun(wl)
+    gpu.gen_grads(1)
+    P = gpu.lay.psi_padded
+    cuts = [0, 8, 8192, 20000, 20480, 40000, P]
+    order = [3, 0, 5, 1, 4, 2]
+    dt = z.ZERO_BF16
+    for i in order:
+        b, e = cuts[i], cuts[i + 1]
+        reps = [r.data_ptr() + 2 * b for r in gpu.reps]
+        z.zero_reduce_shard_unscale(gpu.lay, dt, reps, b, e - b, gpu.g, gpu.partials, gpu.st)
+    z.zero_grad_norm(gpu.lay, gpu.hp, gpu.partials, gpu.st)
+    z.zero_adamw_cast_gather(gpu.lay, gpu.hp, gpu.g, gpu.master, gpu.m, gpu.v, gpu.out, gpu.st)
+    rep = orc.step(1)
+    st = gpu.state()
+    assert_scalars(st, rep)
+    assert_state_close(gpu.arrays(), orc.arrays(), psi, exact_expected=st.clip_coef == rep.clip_coef)
+    gpu.check_guards()
+
+
+@pytest.mark.parametrize("bits", [0x7C00, 0x7E00, 0xFC00])
+def test_overflow_skips_and_backs_off(bits):
+    """A non-finite value in one rank's copy: flag set, step skipped, every state byte kept,
+    L halved; the next step proceeds (fp16 dynamic scaling)."""
+    wl = W.scaled(W.C1, 50_001, steps=3)
+    gpu = GpuRun(wl)
+    orc = OracleRun(wl)
+    st = gpu.step(1)
+    orc.step(1)
+    before = gpu.arrays()
+    L = gpu.gen_grads(2)
+    gpu.reps[3][31337] = int(np.uint16(bits).view(np.int16))
+    z.zero_step(gpu.lay, gpu.hp, z.ZERO_F16, gpu.bucket_ptrs(), gpu.g, gpu.partials, gpu.master,
+                gpu.m, gpu.v, gpu.out, gpu.st)
+    st = gpu.state()
+    assert st.skip == 1 and st.t == 1 and st.loss_scale == L / 2 and st.n_skipped == 1
+    assert st.overflow == 0  # cleared for the next step
+    after = gpu.arrays()
+    for k in ("master", "m", "v", "out"):
+        assert np.array_equal(after[k].view(np.uint8), before[k].view(np.uint8)), k
+    # the oracle, fed the same fault, agrees; then both run a clean step
+    reps = orc.grads(2)
+    reps[3][31337] = bits
+    from oracle import F16
+    rep = orc.orc.step(orc.lay, orc.hp, F16, reps, orc.g, orc.master, orc.m, orc.v, orc.out, orc.sc)
+    assert rep.skipped == 1 and rep.loss_scale_next == st.loss_scale
+    st = gpu.step(3)
+    rep = orc.step(3)
+    assert_scalars(st, rep)
+    assert_state_close(gpu.arrays(), orc.arrays(), wl.psi, exact_expected=st.clip_coef == rep.clip_coef)
+    gpu.check_guards()
+
+
+def test_bf16_static_scale_overflow_skips_without_backoff():
+    wl = W.scaled(W.C2, 30_000, steps=1)
+    gpu = GpuRun(wl)
+    gpu.gen_grads(1)
+    gpu.reps[0][12] = int(np.uint16(0x7F80).view(np.int16))  # bf16 +inf
+    z.zero_step(gpu.lay, gpu.hp, z.ZERO_BF16, gpu.bucket_ptrs(), gpu.g, gpu.partials, gpu.master,
+                gpu.m, gpu.v, gpu.out, gpu.st)
+    st = gpu.state()
+    assert st.skip == 1 and st.loss_scale == 1.0 and st.t == 0
+
+
+def test_multistep_c2_recipe():
+    """The GPT-2 workload's recipe (bf16, random state, clipping active) at 2^20+3, 10 steps."""
+    _run_pair(W.scaled(W.C2, (1 << 20) + 3, steps=10), 10)
+
+
+def test_c5_recipe_dynamic_scaling():
+    """The fp16 stress recipe at psi = 2^20, N = 16, 50 steps: heavy tails, injected
+    inf/NaN every 7th step, loss-scale back-off, clipping (threshold 0.2 here: the norm of
+    this smaller buffer is about 0.45); flag and L bit-exact per step."""
+    wl = replace(W.scaled(W.C5, 1 << 20, steps=50), hp=W.HP(max_grad_norm=0.2))
+    gpu = GpuRun(wl)
+    orc = OracleRun(wl)
+    skipped = []
+    for s in range(1, 51):
+        st = gpu.step(s)
+        rep = orc.step(s)
+        assert_scalars(st, rep)
+        skipped.append(rep.skipped)
+        if s % 10 == 0 or rep.skipped:
+            assert_state_close(gpu.arrays(), orc.arrays(), wl.psi,
+                               exact_expected=st.clip_coef == rep.clip_coef)
+    assert sum(skipped) >= 7 and all(skipped[s - 1] for s in range(7, 51, 7))
+    gpu.check_guards()
+
+
+def test_determinism_bitwise():
+    wl = W.scaled(W.C2, 777_777, steps=2)
+    results = []
+    for _ in range(3):
+        g = GpuRun(wl)
+        g.step(1)
+        s = g.step(2)
+        a = g.arrays()
+        results.append((s.norm, s.sumsq, {k: a[k].tobytes() for k in a}))
+    for r in results[1:]:
+        assert r[0] == results[0][0] and r[1] == results[0][1] and r[2] == results[0][2]
+
+
+def test_checkpoint_resume_bitwise():
+    """5 steps, save state + arrays, restore into fresh buffers, 5 more == 10 straight."""
+    wl = W.scaled(W.C5, 200_000, steps=10)
+    a = GpuRun(wl)
+    for s in range(1, 11):
+        a.step(s)
+    b = GpuRun(wl)
+    for s in range(1, 6):
+        b.step(s)
+    saved = b.state()
+    arrs = {k: getattr(b, k).clone() for k in ("master", "m", "v", "out")}
+    c = GpuRun(wl)
+    for k, t in arrs.items():
+        getattr(c, k).copy_(t)
+    z.zero_step_state_write(c.st, saved)
+    for s in range(6, 11):
+        c.step(s)
+    x, y = a.arrays(), c.arrays()
+    for k in ("master", "m", "v", "out"):
+        assert np.array_equal(x[k].view(np.uint8), y[k].view(np.uint8)), k
+    sa, sc = a.state(), c.state()
+    assert (sa.t, sa.loss_scale, sa.norm, sa.n_steps) == (sc.t, sc.loss_scale, sc.norm, sc.n_steps)
+
+
+@pytest.mark.parametrize("psi,n,stage", [(1 << 20, 2, 1), ((1 << 20) + 1, 64, 3), (1 << 22, 16, 2),
+                                         ((1 << 22) + 1, 8, 1), (1 << 21, 4, 3)])
+def test_sweep_points_all_elements(psi, n, stage):
+    """Bandwidth-sweep points (bf16 ~N(0,1e-3)) small enough for the oracle, every element."""
+    _run_pair(W.sweep_point(psi, n, stage, steps=2), 2)
+
+
+def test_stages_share_arithmetic():
+    outs = []
+    for stage in (1, 2, 3):
+        g = GpuRun(W.sweep_point(100_003, 8, stage))
+        g.step(1)
+        outs.append(g.arrays())
+    for o in outs[1:]:
+        for k in o:
+            assert np.array_equal(o[k].view(np.uint8), outs[0][k].view(np.uint8))
+
+
+def test_step_host_equals_device_path():
+    """zero_step_host (gradients in pinned host memory, bucketed H2D ring) gives the same
+    bits as zero_step on device-resident gradients."""
+    wl = W.scaled(W.C2, 3 * 65536 + 40, steps=2)
+    dev = GpuRun(wl, bucket_elems=65536)
+    host = GpuRun(wl, bucket_elems=65536)
+    P = host.lay.psi_padded
+    staging = torch.empty(2 * wl.n_ranks * 65536, dtype=torch.int16, device="cuda")
+    copy_stream = torch.cuda.Stream()
+    hstate = torch.empty(z.STATE_BYTES, dtype=torch.uint8).pin_memory()
+    for s in (1, 2):
+        dev.step(s)
+        host.gen_grads(s)
+        hreps = [r.cpu().pin_memory() for r in host.reps]
+        for r in host.reps:
+            r.fill_(0x7F7F)  # the device copies must not be read
+        z.zero_step_host(host.lay, host.hp, z.ZERO_BF16, hreps, staging, staging.numel() * 2,
+                         host.g, host.partials, host.master, host.m, host.v, host.out, host.st,
+                         hstate, None, copy_stream)
+        torch.cuda.synchronize()
+        hs = z.StepState.from_buffer_copy(hstate.numpy().tobytes())
+        ds = dev.state()
+        assert hs.norm == ds.norm and hs.t == ds.t == s
+    x, y = dev.arrays(), host.arrays()
+    for k in x:
+        assert np.array_equal(x[k].view(np.uint8), y[k].view(np.uint8)), k
+    assert P == host.lay.psi_padded
+
+
+def test_device_rejects_bad_calls_without_side_effects():
+    wl = W.scaled(W.C2, 10_000, steps=1)
+    gpu = GpuRun(wl)
+    gpu.step(1)
+    before = gpu.arrays()
+    with pytest.raises(z.ZeroError) as e:
+        z.zero_reduce_shard_unscale(gpu.lay, z.ZERO_BF16, gpu.reps, 4, 8, gpu.g, gpu.partials, gpu.st)
+    assert e.value.status == z.ZERO_EALIGN
+    with pytest.raises(z.ZeroError):
+        z.zero_adamw_cast_gather(gpu.lay, z.hparams(beta1=1.0), gpu.g, gpu.master, gpu.m, gpu.v,
+                                 gpu.out, gpu.st)
+    with pytest.raises(z.ZeroError):
+        z.zero_step(gpu.lay, gpu.hp, z.ZERO_BF16, gpu.reps[:-1] + [0], gpu.g, gpu.partials,
+                    gpu.master, gpu.m, gpu.v, gpu.out, gpu.st)
+    after = gpu.arrays()
+    for k in before:
+        assert np.array_equal(after[k].view(np.uint8), before[k].view(np.uint8))
+    gpu.check_guards()
+
+
+def test_generator_twins_agree():
+    """Device and host generators: same bits for every kind and output type (inputs)."""
+    n = 1 << 20
+    for out, kind, sigma, scale in [(synth.OUT_BF16, synth.NORMAL, 1e-4, 1.0),
+                                    (synth.OUT_F16, synth.NORMAL, 1e-3, 1024.0),
+                                    (synth.OUT_F16, synth.STUDENT_T3, 1e-3, 65536.0),
+                                    (synth.OUT_F32, synth.NORMAL, 0.02, 1.0),
+                                    (synth.OUT_F32, synth.NORMAL_SQ, 1e-4, 1.0)]:
+        k = synth.key(7, 1, 3, 5)
+        dt = torch.float32 if out == synth.OUT_F32 else torch.int16
+        d = torch.empty(n, dtype=dt, device="cuda")
+        begin = (1 << 33) + 12345  # a high flat offset exercises 64-bit counters
+        synth.fill_dev(d.data_ptr(), out, kind, k, begin, n, begin + n - 100, sigma, scale)
+        h = synth.fill_host(out, kind, k, begin, n, begin + n - 100, sigma, scale)
+        assert np.array_equal(d.cpu().numpy().view(np.uint8), h.view(np.uint8))

@@ -1,0 +1,381 @@
+/*
+ * api.cu -- the C entry points of include/zero.h: argument checks, then kernel launches.
+ *
+ * Every check runs on the host before anything is enqueued, so a rejected call leaves
+ * all buffers and the stream untouched.  No entry point allocates device memory.
+ */
+#include "zero_internal.h"
+
+#include <mutex>
+#include <string.h>
+
+namespace zero {
+
+namespace {
+thread_local int g_last_cuda_error = 0;
+
+int cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess)
+        return ZERO_OK;
+    g_last_cuda_error = (int)e;
+    return ZERO_ECUDA;
+}
+
+bool aligned16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
+
+/* The invariants zero_partition establishes; the kernels' indexing relies on them. */
+bool layout_ok(const zero_layout_t* L)
+{
+    if (!L || L->n_ranks == 0 || L->n_ranks > ZERO_MAX_RANKS || L->psi == 0 || L->shard == 0)
+        return false;
+    if (L->psi_padded / L->n_ranks != L->shard || L->psi_padded % L->n_ranks != 0)
+        return false;
+    if (L->psi > L->psi_padded || L->pad != L->psi_padded - L->psi || L->psi > (1ull << 56))
+        return false;
+    if (L->tile_elems != ZERO_TILE_ELEMS)
+        return false;
+    if (L->tiles_per_rank != (L->shard + L->tile_elems - 1) / L->tile_elems ||
+        L->n_tiles != (uint64_t)L->n_ranks * L->tiles_per_rank)
+        return false;
+    const uint64_t W = L->bucket_elems;
+    if (W == 0 || W > L->psi_padded || (W != L->psi_padded && W % 8 != 0))
+        return false;
+    return L->n_buckets == (L->psi_padded + W - 1) / W;
+}
+
+bool kernel_layout_ok(const zero_layout_t* L)
+{
+    return layout_ok(L) && L->n_ranks <= ZERO_MAX_KERNEL_RANKS;
+}
+
+bool hparams_ok(const zero_adamw_hparams_t* hp)
+{
+    if (!hp)
+        return false;
+    const float vals[6] = {hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay, hp->max_grad_norm};
+    for (float x : vals)
+        if (!(x == x) || x > 3.0e38f || x < -3.0e38f)
+            return false;
+    return hp->beta1 >= 0.0f && hp->beta1 < 1.0f && hp->beta2 >= 0.0f && hp->beta2 < 1.0f &&
+           hp->eps > 0.0f && hp->lr >= 0.0f;
+}
+
+int reduce_window(const zero_layout_t* L, zero_dtype_t dtype, const void* const* replicas,
+                  uint64_t begin, uint64_t count, float* g, double* partials,
+                  zero_step_state_t* st, cudaStream_t stream)
+{
+    ReduceArgs a;
+    memset(&a, 0, sizeof a);
+    for (uint32_t k = 0; k < L->n_ranks; ++k)
+        a.rep[k] = replicas[k];
+    a.g = g;
+    a.partials = partials;
+    a.st = st;
+    a.begin = begin;
+    a.end = begin + count;
+    a.psi = L->psi;
+    a.shard = L->shard;
+    a.tiles_per_rank = L->tiles_per_rank;
+    a.n_ranks = L->n_ranks;
+    a.tile = L->tile_elems;
+    const uint64_t T = L->tile_elems, S = L->shard;
+    const uint64_t r0 = begin / S, r1 = (a.end - 1) / S;
+    const uint64_t u0 = r0 * L->tiles_per_rank + (begin - r0 * S) / T;
+    const uint64_t u1 = r1 * L->tiles_per_rank + (a.end - 1 - r1 * S) / T;
+    a.unit_first = u0;
+    a.unit_count = u1 - u0 + 1;
+    return cuda_status(launch_reduce(a, dtype, stream));
+}
+
+int check_reduce_args(const zero_layout_t* L, zero_dtype_t dtype, const void* const* replicas,
+                      uint64_t begin, uint64_t count, const float* g, const double* partials,
+                      const zero_step_state_t* st)
+{
+    if (!kernel_layout_ok(L) || (dtype != ZERO_F16 && dtype != ZERO_BF16) || !replicas)
+        return ZERO_EINVAL;
+    if (count == 0 || begin >= L->psi_padded || count > L->psi_padded - begin)
+        return ZERO_EINVAL;
+    if (!g || !partials || !st)
+        return ZERO_EINVAL;
+    for (uint32_t k = 0; k < L->n_ranks; ++k)
+        if (!replicas[k])
+            return ZERO_EINVAL;
+    if (begin % 8 != 0 || !aligned16(g) || !aligned16(partials) || !aligned16(st))
+        return ZERO_EALIGN;
+    for (uint32_t k = 0; k < L->n_ranks; ++k)
+        if (!aligned16(replicas[k]))
+            return ZERO_EALIGN;
+    return ZERO_OK;
+}
+
+int check_adamw_args(const zero_layout_t* L, const zero_adamw_hparams_t* hp, const float* g,
+                     const float* master, const float* m, const float* v, const uint16_t* params,
+                     const zero_step_state_t* st)
+{
+    if (!kernel_layout_ok(L) || !hparams_ok(hp) || !g || !master || !m || !v || !params || !st)
+        return ZERO_EINVAL;
+    if (!aligned16(g) || !aligned16(master) || !aligned16(m) || !aligned16(v) ||
+        !aligned16(params) || !aligned16(st))
+        return ZERO_EALIGN;
+    return ZERO_OK;
+}
+
+int grad_norm(const zero_layout_t* L, const zero_adamw_hparams_t* hp, double* partials,
+              zero_step_state_t* st, cudaStream_t stream)
+{
+    FinalizeArgs a;
+    a.partials = partials;
+    a.st = st;
+    a.tiles_per_rank = L->tiles_per_rank;
+    a.n_ranks = L->n_ranks;
+    a.hp = *hp;
+    return cuda_status(launch_finalize(a, stream));
+}
+
+int adamw(const zero_layout_t* L, const zero_adamw_hparams_t* hp, const float* g, float* master,
+          float* m, float* v, uint16_t* params, const zero_step_state_t* st, cudaStream_t stream)
+{
+    AdamwArgs a;
+    a.g = g;
+    a.master = master;
+    a.m = m;
+    a.v = v;
+    a.out = params;
+    a.st = st;
+    a.psi = L->psi;
+    a.psi_padded = L->psi_padded;
+    a.beta1 = hp->beta1;
+    a.beta2 = hp->beta2;
+    a.eps = hp->eps;
+    return cuda_status(launch_adamw(a, stream));
+}
+
+}  // namespace
+
+int sm_count()
+{
+    static std::mutex mu;
+    static int count[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (count[dev & 63] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        count[dev & 63] = n > 0 ? n : 1;
+    }
+    return count[dev & 63];
+}
+
+}  // namespace zero
+
+using namespace zero;
+
+extern "C" int zero_step_state_init(const zero_layout_t* layout, float loss_scale, uint32_t dynamic,
+                                    uint32_t growth_interval, zero_step_state_t* st,
+                                    double* partials, zero_stream_t stream)
+{
+    if (!kernel_layout_ok(layout) || !st || !partials || !(loss_scale > 0.0f) || loss_scale > 3.0e38f)
+        return ZERO_EINVAL;
+    if (!aligned16(st) || !aligned16(partials))
+        return ZERO_EALIGN;
+    InitArgs a;
+    a.st = st;
+    a.partials = partials;
+    a.n_tiles = layout->n_tiles;
+    a.loss_scale = loss_scale;
+    a.dynamic = dynamic ? 1u : 0u;
+    a.growth_interval = growth_interval;
+    a.n_ranks = layout->n_ranks;
+    return cuda_status(launch_state_init(a, (cudaStream_t)stream));
+}
+
+extern "C" int zero_step_state_read(const zero_step_state_t* st, zero_step_state_t* host_out,
+                                    zero_stream_t stream)
+{
+    if (!st || !host_out)
+        return ZERO_EINVAL;
+    cudaError_t e = cudaMemcpyAsync(host_out, st, sizeof *st, cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize((cudaStream_t)stream);
+    return cuda_status(e);
+}
+
+extern "C" int zero_step_state_write(zero_step_state_t* st, const zero_step_state_t* host_in,
+                                     zero_stream_t stream)
+{
+    if (!st || !host_in)
+        return ZERO_EINVAL;
+    if (!aligned16(st))
+        return ZERO_EALIGN;
+    cudaError_t e = cudaMemcpyAsync(st, host_in, sizeof *st, cudaMemcpyHostToDevice, (cudaStream_t)stream);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize((cudaStream_t)stream);
+    return cuda_status(e);
+}
+
+extern "C" int zero_reduce_shard_unscale(const zero_layout_t* layout, zero_dtype_t dtype,
+                                         const void* const* replicas, uint64_t begin, uint64_t count,
+                                         float* g, double* partials, zero_step_state_t* st,
+                                         zero_stream_t stream)
+{
+    const int rc = check_reduce_args(layout, dtype, replicas, begin, count, g, partials, st);
+    if (rc != ZERO_OK)
+        return rc;
+    return reduce_window(layout, dtype, replicas, begin, count, g, partials, st, (cudaStream_t)stream);
+}
+
+extern "C" int zero_grad_norm(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,
+                              double* partials, zero_step_state_t* st, zero_stream_t stream)
+{
+    if (!kernel_layout_ok(layout) || !hparams_ok(hp) || !partials || !st)
+        return ZERO_EINVAL;
+    if (!aligned16(partials) || !aligned16(st))
+        return ZERO_EALIGN;
+    return grad_norm(layout, hp, partials, st, (cudaStream_t)stream);
+}
+
+extern "C" int zero_adamw_cast_gather(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,
+                                      const float* g, float* master, float* m, float* v,
+                                      uint16_t* params, const zero_step_state_t* st,
+                                      zero_stream_t stream)
+{
+    const int rc = check_adamw_args(layout, hp, g, master, m, v, params, st);
+    if (rc != ZERO_OK)
+        return rc;
+    return adamw(layout, hp, g, master, m, v, params, st, (cudaStream_t)stream);
+}
+
+extern "C" int zero_step(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,
+                         zero_dtype_t dtype, const void* const* replicas, float* g, double* partials,
+                         float* master, float* m, float* v, uint16_t* params, zero_step_state_t* st,
+                         zero_stream_t stream)
+{
+    if (!kernel_layout_ok(layout) || !replicas)
+        return ZERO_EINVAL;
+    const uint64_t W = layout->bucket_elems, P = layout->psi_padded, N = layout->n_ranks;
+    for (uint64_t b = 0; b < layout->n_buckets; ++b) {
+        const uint64_t begin = b * W, count = begin + W < P ? W : P - begin;
+        int rc = check_reduce_args(layout, dtype, replicas + b * N, begin, count, g, partials, st);
+        if (rc != ZERO_OK)
+            return rc;
+    }
+    int rc = check_adamw_args(layout, hp, g, master, m, v, params, st);
+    if (rc != ZERO_OK)
+        return rc;
+    if (!aligned16(partials))
+        return ZERO_EALIGN;
+    const cudaStream_t s = (cudaStream_t)stream;
+    for (uint64_t b = 0; b < layout->n_buckets; ++b) {
+        const uint64_t begin = b * W, count = begin + W < P ? W : P - begin;
+        rc = reduce_window(layout, dtype, replicas + b * N, begin, count, g, partials, st, s);
+        if (rc != ZERO_OK)
+            return rc;
+    }
+    rc = grad_norm(layout, hp, partials, st, s);
+    if (rc != ZERO_OK)
+        return rc;
+    return adamw(layout, hp, g, master, m, v, params, st, s);
+}
+
+extern "C" int zero_step_host(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,
+                              zero_dtype_t dtype, const void* const* host_replicas, void* staging,
+                              uint64_t staging_bytes, float* g, double* partials, float* master,
+                              float* m, float* v, uint16_t* params, zero_step_state_t* st,
+                              zero_step_state_t* host_state_out, zero_stream_t stream,
+                              zero_stream_t copy_stream)
+{
+    if (!kernel_layout_ok(layout) || (dtype != ZERO_F16 && dtype != ZERO_BF16) || !host_replicas ||
+        !staging || stream == copy_stream)
+        return ZERO_EINVAL;
+    const uint64_t W = layout->bucket_elems, P = layout->psi_padded, N = layout->n_ranks;
+    for (uint64_t k = 0; k < N; ++k)
+        if (!host_replicas[k])
+            return ZERO_EINVAL;
+    if (!aligned16(staging) || (W % 8 != 0 && layout->n_buckets > 1))
+        return ZERO_EALIGN;
+    const uint64_t slot_elems = (W + 7) / 8 * 8;  // keeps every staged copy 16-byte aligned
+    if (staging_bytes / 2 / N / 2 < slot_elems)
+        return ZERO_ENOMEM;
+    int rc = check_adamw_args(layout, hp, g, master, m, v, params, st);
+    if (rc != ZERO_OK)
+        return rc;
+    if (!partials)
+        return ZERO_EINVAL;
+    if (!aligned16(partials))
+        return ZERO_EALIGN;
+
+    const cudaStream_t s = (cudaStream_t)stream, cs = (cudaStream_t)copy_stream;
+    cudaEvent_t start, filled[2], consumed[2];
+    cudaError_t e = cudaEventCreateWithFlags(&start, cudaEventDisableTiming);
+    int made = e == cudaSuccess ? 1 : 0;
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+        e = cudaEventCreateWithFlags(&filled[i], cudaEventDisableTiming);
+        made += e == cudaSuccess;
+        if (e == cudaSuccess) {
+            e = cudaEventCreateWithFlags(&consumed[i], cudaEventDisableTiming);
+            made += e == cudaSuccess;
+        }
+    }
+    // the staging ring may still be read by earlier work on `stream`
+    if (e == cudaSuccess)
+        e = cudaEventRecord(start, s);
+    if (e == cudaSuccess)
+        e = cudaStreamWaitEvent(cs, start, 0);
+    uint16_t* ring = (uint16_t*)staging;
+    const void* reps[ZERO_MAX_KERNEL_RANKS];
+    for (uint64_t b = 0; b < layout->n_buckets && e == cudaSuccess && rc == ZERO_OK; ++b) {
+        const int slot = (int)(b & 1);
+        const uint64_t begin = b * W, count = begin + W < P ? W : P - begin;
+        if (b >= 2)
+            e = cudaStreamWaitEvent(cs, consumed[slot], 0);
+        for (uint64_t k = 0; k < N && e == cudaSuccess; ++k) {
+            uint16_t* dst = ring + ((uint64_t)slot * N + k) * slot_elems;
+            const uint16_t* src = (const uint16_t*)host_replicas[k] + begin;
+            e = cudaMemcpyAsync(dst, src, count * 2, cudaMemcpyHostToDevice, cs);
+            reps[k] = dst;
+        }
+        if (e == cudaSuccess)
+            e = cudaEventRecord(filled[slot], cs);
+        if (e == cudaSuccess)
+            e = cudaStreamWaitEvent(s, filled[slot], 0);
+        if (e == cudaSuccess)
+            rc = reduce_window(layout, dtype, reps, begin, count, g, partials, st, s);
+        if (e == cudaSuccess && rc == ZERO_OK)
+            e = cudaEventRecord(consumed[slot], s);
+    }
+    if (e == cudaSuccess && rc == ZERO_OK)
+        rc = grad_norm(layout, hp, partials, st, s);
+    if (e == cudaSuccess && rc == ZERO_OK)
+        rc = adamw(layout, hp, g, master, m, v, params, st, s);
+    if (e == cudaSuccess && rc == ZERO_OK && host_state_out)
+        e = cudaMemcpyAsync(host_state_out, st, sizeof *st, cudaMemcpyDeviceToHost, s);
+    // destroying a recorded event is allowed; its resources go when the work completes
+    if (made >= 1)
+        cudaEventDestroy(start);
+    for (int i = 0; i < 2; ++i) {
+        if (made >= 2 + 2 * i)
+            cudaEventDestroy(filled[i]);
+        if (made >= 3 + 2 * i)
+            cudaEventDestroy(consumed[i]);
+    }
+    if (e != cudaSuccess)
+        return cuda_status(e);
+    return rc;
+}
+
+extern "C" const char* zero_strerror(int status)
+{
+    switch (status) {
+    case ZERO_OK: return "ok";
+    case ZERO_EINVAL: return "invalid argument";
+    case ZERO_EALIGN: return "pointer or window not aligned (16-byte pointers, window start a multiple of 8)";
+    case ZERO_ENOMEM: return "caller-provided buffer too small";
+    case ZERO_ECUDA: return "CUDA launch or copy failed";
+    case ZERO_ETIMEOUT: return "bounded device wait timed out";
+    default: return "unknown status";
+    }
+}
+
+extern "C" int zero_last_cuda_error(void) { return g_last_cuda_error; }

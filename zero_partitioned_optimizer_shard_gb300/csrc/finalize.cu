@@ -1,0 +1,159 @@
+/*
+ * finalize.cu -- global gradient norm, clip coefficient, loss scaler, skip decision.
+ *
+ * The Megatron distributed-optimizer page (gitcode.csdn.net, sec. 1, AdamW global
+ * grad_norm table): inside optimizer.step(), before gradients are clipped, one all-reduce
+ * turns the ranks' local squared norms into the global L2 norm that sets clip_coeff.  With
+ * the ranks on one GPU that all-reduce is a fixed-order sum: each rank's tile partials
+ * (written by the reduce pass) are summed per rank, then the ranks in order.
+ *
+ * The scaler follows fp16 mixed-precision training ("3、ZeRO技术概述" DeepSpeed config,
+ * "fp16": enabled): a step whose reduced gradient holds inf/NaN is skipped and a dynamic
+ * loss scale halves (floor 1); every growth_interval consecutive good steps it doubles
+ * (cap 2^24).  Everything stays on the device, so a training loop never waits for the
+ * host between steps.
+ *
+ * One block of 1024 threads: warps split the ranks' partial ranges (fixed assignment
+ * that depends only on N and the tile count), each lane sums a strided subset in fp64,
+ * a shuffle tree folds the warp, thread 0 folds warps and ranks in order.  The partials
+ * are zeroed as they are read, ready for the next step's reduce windows.
+ */
+#include "zero_internal.h"
+
+#include <math.h>
+
+namespace zero {
+namespace {
+
+constexpr int kFinalizeThreads = 1024;
+
+__global__ void __launch_bounds__(kFinalizeThreads) k_finalize(const __grid_constant__ FinalizeArgs a)
+{
+    __shared__ double warp_sum[32];
+    const int w = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t N = a.n_ranks;
+    const uint64_t tpr = a.tiles_per_rank;
+    const int warps_per_rank = N >= 32 ? 1 : 32 / (int)N;
+    const int ranks_per_pass = 32 / warps_per_rank;
+    double total = 0.0;  // meaningful in thread 0
+
+    for (uint32_t r0 = 0; r0 < N; r0 += ranks_per_pass) {
+        const int slot = w / warps_per_rank;
+        const int sub = w % warps_per_rank;
+        const uint32_t r = r0 + slot;
+        double s = 0.0;
+        if (slot < ranks_per_pass && r < N) {
+            const uint64_t chunk = (tpr + warps_per_rank - 1) / warps_per_rank;
+            const uint64_t j0 = (uint64_t)sub * chunk;
+            const uint64_t j1 = j0 + chunk < tpr ? j0 + chunk : tpr;
+            double* p = a.partials + (uint64_t)r * tpr;
+            for (uint64_t jj = j0 + lane; jj < j1; jj += 32) {
+                s += p[jj];
+                p[jj] = 0.0;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0)
+            warp_sum[w] = s;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            for (int rr = 0; rr < ranks_per_pass && r0 + rr < N; ++rr) {
+                double q = 0.0;
+                for (int k = 0; k < warps_per_rank; ++k)
+                    q += warp_sum[rr * warps_per_rank + k];
+                total += q;
+            }
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x != 0)
+        return;
+
+    zero_step_state_t* st = a.st;
+    const double norm = sqrt(total);
+    const bool overflow = st->overflow != 0;
+    float L = st->loss_scale;
+    st->sumsq = total;
+    st->norm = norm;
+    if (overflow) {
+        st->skip = 1;
+        st->clip_coef = 1.0f;
+        st->n_skipped += 1;
+        if (st->dynamic) {
+            const float half = L * 0.5f;
+            L = half < 1.0f ? 1.0f : half;
+            st->good_steps = 0;
+        }
+    } else {
+        const uint32_t t = st->t + 1;
+        st->t = t;
+        st->skip = 0;
+        float c = 1.0f;
+        if (a.hp.max_grad_norm > 0.0f) {
+            const double cc = (double)a.hp.max_grad_norm / (norm + 1e-6);
+            c = cc < 1.0 ? (float)cc : 1.0f;
+        }
+        st->clip_coef = c;
+        const double bc1 = 1.0 - pow((double)a.hp.beta1, (double)t);
+        const double bc2 = 1.0 - pow((double)a.hp.beta2, (double)t);
+        st->step_size = (float)((double)a.hp.lr / bc1);
+        st->rbc2 = (float)sqrt(bc2);
+        st->decay = (float)(1.0 - (double)a.hp.lr * (double)a.hp.weight_decay);
+        if (st->dynamic && st->growth_interval > 0) {
+            st->good_steps += 1;
+            if (st->good_steps == st->growth_interval) {
+                const float twice = L * 2.0f;
+                L = twice > 16777216.0f ? 16777216.0f : twice;
+                st->good_steps = 0;
+            }
+        }
+    }
+    st->loss_scale = L;
+    st->inv_scale = (float)(1.0 / ((double)N * (double)L));
+    st->overflow = 0;
+    st->n_steps += 1;
+}
+
+__global__ void k_state_init(const __grid_constant__ InitArgs a)
+{
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < a.n_tiles; i += stride)
+        a.partials[i] = 0.0;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        zero_step_state_t s;
+        memset(&s, 0, sizeof s);
+        s.clip_coef = 1.0f;
+        s.loss_scale = a.loss_scale;
+        s.inv_scale = (float)(1.0 / ((double)a.n_ranks * (double)a.loss_scale));
+        s.rbc2 = 1.0f;
+        s.decay = 1.0f;
+        s.dynamic = a.dynamic;
+        s.growth_interval = a.growth_interval;
+        s.n_ranks = a.n_ranks;
+        *a.st = s;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s)
+{
+    k_finalize<<<1, kFinalizeThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_state_init(const InitArgs& a, cudaStream_t s)
+{
+    const uint64_t want = (a.n_tiles + 255) / 256;
+    const uint64_t cap = (uint64_t)sm_count() * 4;
+    unsigned grid = (unsigned)(want < cap ? want : cap);
+    if (grid == 0)
+        grid = 1;
+    k_state_init<<<grid, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace zero

@@ -1,0 +1,251 @@
+/*
+ * reduce.cu -- reduce-scatter arithmetic, unscale, overflow flag, sum of squares.
+ *
+ * "【论文解读】ZeRO" sec. 6(1)-(2): data-parallel ranks average their gradients; with
+ * gradient partitioning the average is reduce-scattered, so the owner of flat [r*S,(r+1)*S)
+ * receives the mean of every rank's copy of that range (the page's 4-GPU example: GPU0
+ * ends with G0,G1, GPU1 with G2,G3, ...).  All N ranks live on this GPU as N buffers, so
+ * the collective's arithmetic is a streaming N-way sum:
+ *
+ *   g[i] = (x_0[i] + x_1[i] + ... + x_{N-1}[i]) * f32(1/(N*L))   (fp32, ascending rank)
+ *
+ * fused with the inf/NaN check of fp16 loss scaling and with the per-rank sum of g^2
+ * that the global-norm all-reduce of the Megatron distributed-optimizer page (sec. 1)
+ * combines.
+ *
+ * GB300 design.  Pure HBM streaming (2N bytes in, 4 out per element, a few flops), so:
+ *  - a persistent grid (SM count x resident blocks) walks rank-local tiles of 8192
+ *    elements; one block owns a tile, so its partial is written by exactly one block per
+ *    launch (deterministic, no atomics on the data path);
+ *  - every thread moves 8 elements per replica with one 128-bit non-coherent load that
+ *    skips L1 (ld.global.nc.L1::no_allocate.v4), all N replica loads issued before the
+ *    sum, and writes g with streaming 128-bit stores;
+ *  - the sum of squares is carried per thread as an unevaluated fp32 pair with error-free
+ *    TwoProduct (FMA) and TwoSum steps, which keeps it at ~2^-48 relative accuracy without
+ *    per-element fp64 (GB300's fp64 rate is a small fraction of fp32), then folded into
+ *    fp64 once per thread and reduced in a fixed shuffle tree per tile;
+ *  - elements whose squares leave the fp32 range are summed in fp64 instead.
+ */
+#include "zero_internal.h"
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace zero {
+namespace {
+
+constexpr int kBlock = 256;
+constexpr int kLoadBatch = 8;  // replica loads in flight per thread before summing
+
+template <zero_dtype_t DT>
+__device__ __forceinline__ float lo16(uint32_t w);
+template <zero_dtype_t DT>
+__device__ __forceinline__ float hi16(uint32_t w);
+
+template <>
+__device__ __forceinline__ float lo16<ZERO_BF16>(uint32_t w) { return __uint_as_float(w << 16); }
+template <>
+__device__ __forceinline__ float hi16<ZERO_BF16>(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+template <>
+__device__ __forceinline__ float lo16<ZERO_F16>(uint32_t w)
+{
+    return __half2float(__ushort_as_half((unsigned short)(w & 0xffffu)));
+}
+template <>
+__device__ __forceinline__ float hi16<ZERO_F16>(uint32_t w)
+{
+    return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+}
+
+template <zero_dtype_t DT>
+__device__ __forceinline__ float one16(uint16_t b)
+{
+    return lo16<DT>((uint32_t)b);
+}
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p)
+{
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint16_t ld_stream_u16(const void* p)
+{
+    unsigned short v;
+    asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+template <zero_dtype_t DT>
+__device__ __forceinline__ void add8(float (&s)[8], const uint4& v)
+{
+    s[0] = __fadd_rn(s[0], lo16<DT>(v.x));
+    s[1] = __fadd_rn(s[1], hi16<DT>(v.x));
+    s[2] = __fadd_rn(s[2], lo16<DT>(v.y));
+    s[3] = __fadd_rn(s[3], hi16<DT>(v.y));
+    s[4] = __fadd_rn(s[4], lo16<DT>(v.z));
+    s[5] = __fadd_rn(s[5], hi16<DT>(v.z));
+    s[6] = __fadd_rn(s[6], lo16<DT>(v.w));
+    s[7] = __fadd_rn(s[7], hi16<DT>(v.w));
+}
+
+/* Sum of squares as hi + lo (both fp32) plus an fp64 side sum for squares outside the
+ * fp32 range.  TwoProduct: x*x = p + pe exactly (FMA).  TwoSum: hi + p = s + err exactly. */
+struct SumSq {
+    float hi = 0.0f, lo = 0.0f;
+    double wide = 0.0;
+
+    __device__ __forceinline__ void add(float x)
+    {
+        const float ax = fabsf(x);
+        if (ax < 0x1p+62f && (ax >= 0x1p-50f || ax == 0.0f)) {
+            const float p = __fmul_rn(x, x);
+            const float pe = __fmaf_rn(x, x, -p);
+            const float s = __fadd_rn(hi, p);
+            const float bb = __fsub_rn(s, hi);
+            const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(p, bb));
+            hi = s;
+            lo = __fadd_rn(lo, __fadd_rn(err, pe));
+        } else {
+            wide += (double)x * (double)x;  // tiny, huge or non-finite
+        }
+    }
+
+    __device__ __forceinline__ double total() const { return ((double)hi + (double)lo) + wide; }
+};
+
+__device__ __forceinline__ bool not_finite(float x)
+{
+    return (__float_as_uint(x) & 0x7f800000u) == 0x7f800000u;
+}
+
+template <zero_dtype_t DT, int NR>
+__global__ void __launch_bounds__(kBlock) k_reduce(const __grid_constant__ ReduceArgs a)
+{
+    const int N = NR > 0 ? NR : (int)a.n_ranks;
+    const float inv = a.st->inv_scale;
+    __shared__ double warp_part[kBlock / 32];
+    bool bad = false;
+
+    for (uint64_t u = blockIdx.x; u < a.unit_count; u += gridDim.x) {
+        const uint64_t unit = a.unit_first + u;
+        const uint64_t r = unit / a.tiles_per_rank;
+        const uint64_t j = unit - r * a.tiles_per_rank;
+        const uint64_t shard_lo = r * a.shard;
+        uint64_t lo = shard_lo + j * a.tile;
+        uint64_t hi = lo + a.tile < shard_lo + a.shard ? lo + a.tile : shard_lo + a.shard;
+        lo = lo > a.begin ? lo : a.begin;
+        hi = hi < a.end ? hi : a.end;
+
+        SumSq acc;
+        for (uint64_t b = (lo & ~7ull) + 8ull * threadIdx.x; b < hi; b += 8ull * kBlock) {
+            float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            const bool full = b >= lo && b + 8 <= hi;
+            const uint64_t off = b - a.begin;  // a multiple of 8: begin is
+            if (full) {
+#pragma unroll 1
+                for (int k0 = 0; k0 < N; k0 += kLoadBatch) {
+                    uint4 v[kLoadBatch];
+#pragma unroll
+                    for (int kk = 0; kk < kLoadBatch; ++kk)
+                        if (NR > 0 ? (k0 + kk < NR) : (k0 + kk < N))
+                            v[kk] = ld_stream_v4((const uint16_t*)a.rep[k0 + kk] + off);
+#pragma unroll
+                    for (int kk = 0; kk < kLoadBatch; ++kk)
+                        if (NR > 0 ? (k0 + kk < NR) : (k0 + kk < N))
+                            add8<DT>(s, v[kk]);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint64_t i = b + e;
+                    if (i >= lo && i < hi)
+                        for (int k = 0; k < N; ++k)
+                            s[e] = __fadd_rn(s[e], one16<DT>(ld_stream_u16((const uint16_t*)a.rep[k] + off + e)));
+                }
+            }
+            float gv[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint64_t i = b + e;
+                gv[e] = i < a.psi ? __fmul_rn(s[e], inv) : 0.0f;
+                if (i >= lo && i < hi) {
+                    bad |= not_finite(gv[e]);
+                    acc.add(gv[e]);
+                }
+            }
+            if (full) {
+                __stcs(reinterpret_cast<float4*>(a.g + b), make_float4(gv[0], gv[1], gv[2], gv[3]));
+                __stcs(reinterpret_cast<float4*>(a.g + b + 4), make_float4(gv[4], gv[5], gv[6], gv[7]));
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if (b + e >= lo && b + e < hi)
+                        a.g[b + e] = gv[e];
+            }
+        }
+
+        // fixed-order reduction of the tile's partial: shuffle tree, then warps in order
+        double d = acc.total();
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            d += __shfl_xor_sync(0xffffffffu, d, o);
+        if ((threadIdx.x & 31) == 0)
+            warp_part[threadIdx.x >> 5] = d;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            double t = 0.0;
+#pragma unroll
+            for (int w = 0; w < kBlock / 32; ++w)
+                t += warp_part[w];
+            a.partials[unit] += t;  // windows of one step meet a tile in stream order
+        }
+        __syncthreads();
+    }
+    if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0)
+        atomicOr(&a.st->overflow, 1u);
+}
+
+template <zero_dtype_t DT, int NR>
+cudaError_t launch_t(const ReduceArgs& a, cudaStream_t s)
+{
+    static int per_sm[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int& occ = per_sm[dev & 63];
+    if (occ == 0) {
+        int o = 0;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, k_reduce<DT, NR>, kBlock, 0);
+        occ = o > 0 ? o : 1;
+    }
+    const uint64_t cap = (uint64_t)sm_count() * (uint64_t)occ;
+    const unsigned grid = (unsigned)(a.unit_count < cap ? a.unit_count : cap);
+    if (grid == 0)
+        return cudaSuccess;
+    k_reduce<DT, NR><<<grid, kBlock, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <zero_dtype_t DT>
+cudaError_t launch_dt(const ReduceArgs& a, cudaStream_t s)
+{
+    switch (a.n_ranks) {
+    case 2: return launch_t<DT, 2>(a, s);
+    case 4: return launch_t<DT, 4>(a, s);
+    case 8: return launch_t<DT, 8>(a, s);
+    case 16: return launch_t<DT, 16>(a, s);
+    default: return launch_t<DT, 0>(a, s);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_reduce(const ReduceArgs& a, zero_dtype_t dtype, cudaStream_t s)
+{
+    return dtype == ZERO_F16 ? launch_dt<ZERO_F16>(a, s) : launch_dt<ZERO_BF16>(a, s);
+}
+
+}  // namespace zero

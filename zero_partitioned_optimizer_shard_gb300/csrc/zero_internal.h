@@ -1,0 +1,63 @@
+/*
+ * zero_internal.h -- shared declarations of the CUDA library behind include/zero.h.
+ */
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/zero.h"
+
+namespace zero {
+
+/* Kernel arguments of the reduce-scatter / unscale / sum-of-squares pass. */
+struct ReduceArgs {
+    const void* rep[ZERO_MAX_KERNEL_RANKS];  // replica k, pointing at flat `begin`
+    float* g;                                // flat fp32 gradient, psi_padded
+    double* partials;                        // one fp64 slot per rank-local tile
+    zero_step_state_t* st;
+    uint64_t begin, end;                     // window [begin, end)
+    uint64_t psi, shard;
+    uint64_t tiles_per_rank;
+    uint64_t unit_first, unit_count;         // rank-local tiles that meet the window
+    uint32_t n_ranks;
+    uint32_t tile;
+};
+
+struct FinalizeArgs {
+    double* partials;
+    zero_step_state_t* st;
+    uint64_t tiles_per_rank;
+    uint32_t n_ranks;
+    zero_adamw_hparams_t hp;
+};
+
+struct AdamwArgs {
+    const float* g;
+    float* master;
+    float* m;
+    float* v;
+    uint16_t* out;
+    const zero_step_state_t* st;
+    uint64_t psi, psi_padded;
+    float beta1, beta2, eps;
+};
+
+struct InitArgs {
+    zero_step_state_t* st;
+    double* partials;
+    uint64_t n_tiles;
+    float loss_scale;
+    uint32_t dynamic, growth_interval, n_ranks;
+};
+
+/* Launchers (enqueue only; return the launch's cudaError_t). */
+cudaError_t launch_reduce(const ReduceArgs& a, zero_dtype_t dtype, cudaStream_t s);
+cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s);
+cudaError_t launch_adamw(const AdamwArgs& a, cudaStream_t s);
+cudaError_t launch_state_init(const InitArgs& a, cudaStream_t s);
+
+/* Resident blocks per SM times SM count for a kernel, cached per device. */
+int sm_count();
+
+}  // namespace zero
