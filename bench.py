@@ -319,10 +319,11 @@ def run_ours(args):
         "final_state": {"t": stt.t, "norm": stt.norm, "clip_coef": stt.clip_coef},
     }
     if rank == 0 and not args.no_cpu_baseline:
-        v, dt, swl = cpu_oracle_baseline(1, 1 << 24)
+        v, dt, swl = cpu_oracle_baseline(6, 1 << 26)
         line["cpu_baseline"] = {"value": v, "unit": "params/s", "cores": 1, "kind": "oracle",
-                                "sample": f"one oracle step of the GPT-2-1.5B recipe at psi={swl.psi} "
-                                          f"(N=8 bf16 copies, random fp32 state), {dt:.1f} s"}
+                                "sample": f"6 oracle steps of the GPT-2-1.5B recipe at psi={swl.psi} "
+                                          f"(N=8 bf16 copies, random fp32 state), {dt:.1f} s "
+                                          f"single-threaded"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -331,11 +332,19 @@ def run_ours(args):
 
 
 def _traffic_from_profile():
-    """DRAM bytes per k_adamw launch from the committed ncu summary, if current."""
+    """DRAM bytes per k_adamw launch from the committed ncu summary, or None when the
+    kernel source has changed since those counters were taken."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "k_adamw_traffic.json")
+    src = os.path.join(ROOT, "zero_partitioned_optimizer_shard_gb300", "csrc", "adamw.cu")
     try:
         with open(path) as f:
-            return json.load(f).get("traffic_bytes_per_launch_full_size")
+            rec = json.load(f)
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        if not sha.startswith(rec["source_sha256_prefix"]):
+            return None
+        return rec["traffic_bytes_per_launch_full_size"]
     except Exception:
         return None
 
