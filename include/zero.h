@@ -252,6 +252,37 @@ int zero_step_host(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,
                    zero_step_state_t* host_state_out, zero_stream_t stream,
                    zero_stream_t copy_stream);
 
+/* -------------------------------------------------------------------------------------
+ * zero_step_static_workspace -- zero_step for callers that cannot allocate device memory.
+ * The ZeRO pages have no counterpart of this call; it exists for how the library is used.
+ * Some callers cannot give the library a scratch buffer: their memory manager already
+ * holds all of the GPU's memory, or they must not take the device-wide synchronisation
+ * that a cudaMalloc or cudaFree can cause in the middle of a training step.  This call
+ * runs the same step as zero_step, but keeps the step's only scratch, the per-tile
+ * sum-of-squares partials, in a static device array of ZERO_STATIC_WORKSPACE_SLOTS
+ * 8-byte slots (8 MiB) inside the library.  It calls no cudaMalloc, no cudaFree and no
+ * other allocating routine.
+ *   - The array is held on every GPU where the library's device code is loaded, from
+ *     load until the process exits.
+ *   - Layouts with n_tiles > ZERO_STATIC_WORKSPACE_SLOTS (more than about 8.6e9 padded
+ *     parameters) are rejected with ZERO_ENOMEM before anything is enqueued.
+ *   - The first call on each device looks up the array's device address (a one-time
+ *     set-up, with that device current); make that first call before any stream capture
+ *     begins.
+ *   - Every call shares the one array and clears the slots it uses at its start, so two
+ *     calls whose work overlaps on the GPU (different streams or threads) race: issue them
+ *     one after another on one stream.
+ *   - Arguments as in zero_step, without `partials`.  To initialise st with
+ *     zero_step_state_init without allocating, pass any 16-byte-aligned device buffer of
+ *     at least zero_workspace_bytes(layout) bytes as its `partials` argument, e.g. `g`
+ *     whenever the shard size S is at least 2 (every step overwrites g before reading it).
+ * ------------------------------------------------------------------------------------- */
+#define ZERO_STATIC_WORKSPACE_SLOTS (1u << 20)
+int zero_step_static_workspace(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,
+                               zero_dtype_t dtype, const void* const* replicas, float* g,
+                               float* master, float* m, float* v, uint16_t* params,
+                               zero_step_state_t* st, zero_stream_t stream);
+
 /* Text for a status code. */
 const char* zero_strerror(int status);
 

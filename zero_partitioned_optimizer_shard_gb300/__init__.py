@@ -207,9 +207,24 @@ def zero_step_host(layout: Layout, hp: HParams, dtype: int, host_replicas: Seque
         _ptr(st), _ptr(host_state_out), _stream(stream), _stream(copy_stream)))
 
 
+def zero_step_static_workspace(layout: Layout, hp: HParams, dtype: int, replicas: Sequence, g,
+                               master, m, v, params, st, stream=None) -> None:
+    """zero_step without a caller workspace: for callers that cannot allocate device
+    memory.  The per-tile partials live in the library's static device array (8 MiB per
+    GPU); calls must not overlap on the GPU.  See include/zero.h."""
+    f = _lib().zero_step_static_workspace
+    f.argtypes = [C.POINTER(Layout), C.POINTER(HParams), C.c_int, C.POINTER(_P), _P, _P, _P, _P,
+                  _P, _P, _P]
+    f.restype = C.c_int
+    _check("zero_step_static_workspace", f(
+        C.byref(layout), C.byref(hp), dtype, _ptr_array(replicas), _ptr(g), _ptr(master), _ptr(m),
+        _ptr(v), _ptr(params), _ptr(st), _stream(stream)))
+
+
 __all__ = [
     "Layout", "HParams", "StepState", "ZeroError", "hparams", "lib", "STATE_BYTES",
     "ZERO_F16", "ZERO_BF16", "zero_partition", "zero_workspace_bytes", "zero_step_state_init",
     "zero_step_state_read", "zero_step_state_write", "zero_reduce_shard_unscale",
     "zero_grad_norm", "zero_adamw_cast_gather", "zero_step", "zero_step_host",
+    "zero_step_static_workspace",
 ]

@@ -153,6 +153,8 @@ int adamw(const zero_layout_t* L, const zero_adamw_hparams_t* hp, const float* g
 
 }  // namespace
 
+void record_cuda_error(int e) { g_last_cuda_error = e; }
+
 int sm_count()
 {
     static std::mutex mu;

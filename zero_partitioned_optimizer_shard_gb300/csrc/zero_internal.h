@@ -60,4 +60,7 @@ cudaError_t launch_state_init(const InitArgs& a, cudaStream_t s);
 /* Resident blocks per SM times SM count for a kernel, cached per device. */
 int sm_count();
 
+/* Make zero_last_cuda_error() report `e` on this thread. */
+void record_cuda_error(int e);
+
 }  // namespace zero
