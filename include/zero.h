@@ -116,7 +116,9 @@ typedef struct zero_step_state {
     uint32_t n_steps;       /* finalised steps, applied or skipped */
     uint32_t n_skipped;
     uint32_t error;         /* device error word, 0 = none (reserved) */
-    uint32_t reserved[12];
+    uint32_t arrivals;      /* internal to zero_grad_norm: its blocks that have finished
+                               (0 between steps; keep it 0 when writing a state) */
+    uint32_t reserved[11];
 } zero_step_state_t;        /* 128 bytes */
 
 /* -------------------------------------------------------------------------------------

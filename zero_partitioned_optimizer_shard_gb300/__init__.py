@@ -53,7 +53,8 @@ class StepState(C.Structure):
         ("rbc2", C.c_float), ("decay", C.c_float), ("overflow", C.c_uint32), ("skip", C.c_uint32),
         ("t", C.c_uint32), ("good_steps", C.c_uint32), ("growth_interval", C.c_uint32),
         ("dynamic", C.c_uint32), ("n_ranks", C.c_uint32), ("n_steps", C.c_uint32),
-        ("n_skipped", C.c_uint32), ("error", C.c_uint32), ("reserved", C.c_uint32 * 12),
+        ("n_skipped", C.c_uint32), ("error", C.c_uint32), ("arrivals", C.c_uint32),
+        ("reserved", C.c_uint32 * 11),
     ]
 
 

@@ -13,10 +13,14 @@
  * (cap 2^24).  Everything stays on the device, so a training loop never waits for the
  * host between steps.
  *
- * One block of 1024 threads: warps split the ranks' partial ranges (fixed assignment
- * that depends only on N and the tile count), each lane sums a strided subset in fp64,
- * a shuffle tree folds the warp, thread 0 folds warps and ranks in order.  The partials
- * are zeroed as they are read, ready for the next step's reduce windows.
+ * The sum is spread over up to 128 blocks (GB300's fp64 rate is a few operations per SM
+ * per clock, so one block summing every tile partial would take tens of microseconds).
+ * Block b sums the fixed chunk b of every rank's tile partials (a fixed tree per block),
+ * leaves that chunk's sum in the chunk's first slot and zeroes the rest; the last block
+ * to arrive (an atomic counter in the step state, no waiting) adds the chunk sums of
+ * each rank in order, then the ranks in order, and runs the scalar logic.  The chunking
+ * depends only on N and the tile count, so the result is the same on any GPU.  All
+ * partial slots end at zero, ready for the next step's reduce windows.
  */
 #include "zero_internal.h"
 
@@ -25,54 +29,83 @@
 namespace zero {
 namespace {
 
-constexpr int kFinalizeThreads = 1024;
+constexpr int kFinThreads = 256;
+constexpr int kFinMaxBlocks = 128;
 
-__global__ void __launch_bounds__(kFinalizeThreads) k_finalize(const __grid_constant__ FinalizeArgs a)
+/* Fixed-order block sum; the result is valid in thread 0. */
+__device__ __forceinline__ double block_sum(double v, double* red)
 {
-    __shared__ double warp_sum[32];
-    const int w = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    double t = 0.0;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < kFinThreads / 32; ++w)
+            t += red[w];
+    __syncthreads();
+    return t;
+}
+
+__global__ void __launch_bounds__(kFinThreads) k_finalize(const __grid_constant__ FinalizeArgs a)
+{
+    __shared__ double red[kFinThreads / 32];
+    __shared__ double rank_sum[ZERO_MAX_KERNEL_RANKS];
+    __shared__ int is_last;
     const uint32_t N = a.n_ranks;
     const uint64_t tpr = a.tiles_per_rank;
-    const int warps_per_rank = N >= 32 ? 1 : 32 / (int)N;
-    const int ranks_per_pass = 32 / warps_per_rank;
-    double total = 0.0;  // meaningful in thread 0
+    const uint64_t chunk = (tpr + gridDim.x - 1) / gridDim.x;
+    const uint64_t j0 = (uint64_t)blockIdx.x * chunk;
+    const uint64_t j1 = j0 + chunk < tpr ? j0 + chunk : tpr;
 
-    for (uint32_t r0 = 0; r0 < N; r0 += ranks_per_pass) {
-        const int slot = w / warps_per_rank;
-        const int sub = w % warps_per_rank;
-        const uint32_t r = r0 + slot;
+    // this block's chunk of every rank
+    for (uint32_t r = 0; r < N; ++r) {
+        double* p = a.partials + (uint64_t)r * tpr;
         double s = 0.0;
-        if (slot < ranks_per_pass && r < N) {
-            const uint64_t chunk = (tpr + warps_per_rank - 1) / warps_per_rank;
-            const uint64_t j0 = (uint64_t)sub * chunk;
-            const uint64_t j1 = j0 + chunk < tpr ? j0 + chunk : tpr;
-            double* p = a.partials + (uint64_t)r * tpr;
-            for (uint64_t jj = j0 + lane; jj < j1; jj += 32) {
-                s += p[jj];
-                p[jj] = 0.0;
-            }
+        for (uint64_t j = j0 + threadIdx.x; j < j1; j += kFinThreads) {
+            s += p[j];
+            p[j] = 0.0;
+        }
+        s = block_sum(s, red);
+        if (threadIdx.x == 0 && j0 < j1)
+            p[j0] = s;
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0)
+        is_last = atomicAdd(&a.st->arrivals, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!is_last)
+        return;
+    __threadfence();
+
+    // the last block: chunk sums in order per rank (one warp per rank), ranks in order
+    const uint64_t n_chunks = (tpr + chunk - 1) / chunk;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (uint32_t r = w; r < N; r += kFinThreads / 32) {
+        double* p = a.partials + (uint64_t)r * tpr;
+        double s = 0.0;
+        for (uint64_t c = lane; c < n_chunks; c += 32) {
+            s += __ldcg(p + c * chunk);
+            p[c * chunk] = 0.0;
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
             s += __shfl_xor_sync(0xffffffffu, s, o);
         if (lane == 0)
-            warp_sum[w] = s;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            for (int rr = 0; rr < ranks_per_pass && r0 + rr < N; ++rr) {
-                double q = 0.0;
-                for (int k = 0; k < warps_per_rank; ++k)
-                    q += warp_sum[rr * warps_per_rank + k];
-                total += q;
-            }
-        }
-        __syncthreads();
+            rank_sum[r] = s;
     }
+    __syncthreads();
     if (threadIdx.x != 0)
         return;
+    double total = 0.0;
+    for (uint32_t r = 0; r < N; ++r)
+        total += rank_sum[r];
 
     zero_step_state_t* st = a.st;
+    st->arrivals = 0;
     const double norm = sqrt(total);
     const bool overflow = st->overflow != 0;
     float L = st->loss_scale;
@@ -141,7 +174,9 @@ __global__ void k_state_init(const __grid_constant__ InitArgs a)
 
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s)
 {
-    k_finalize<<<1, kFinalizeThreads, 0, s>>>(a);
+    const uint64_t blocks = a.tiles_per_rank < (uint64_t)kFinMaxBlocks ? a.tiles_per_rank
+                                                                       : (uint64_t)kFinMaxBlocks;
+    k_finalize<<<(unsigned)(blocks > 0 ? blocks : 1), kFinThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -92,30 +92,61 @@ __device__ __forceinline__ void add8(float (&s)[8], const uint4& v)
     s[7] = __fadd_rn(s[7], hi16<DT>(v.w));
 }
 
-/* Sum of squares as hi + lo (both fp32) plus an fp64 side sum for squares outside the
- * fp32 range.  TwoProduct: x*x = p + pe exactly (FMA).  TwoSum: hi + p = s + err exactly. */
+/* Sum of squares of the fp32 gradient, carried as an unevaluated pair hi + lo of fp32
+ * values.  TwoProduct: x*x = p + pe exactly (FMA); TwoSum: hi + p = s + err exactly.
+ * Exact for every |x| in [2^-50, 2^62) and for zeros; groups holding anything else take
+ * the fp64 path below (never in normal training data). */
 struct SumSq {
     float hi = 0.0f, lo = 0.0f;
     double wide = 0.0;
 
-    __device__ __forceinline__ void add(float x)
+    __device__ __forceinline__ void add_fast(float x)
     {
-        const float ax = fabsf(x);
-        if (ax < 0x1p+62f && (ax >= 0x1p-50f || ax == 0.0f)) {
-            const float p = __fmul_rn(x, x);
-            const float pe = __fmaf_rn(x, x, -p);
-            const float s = __fadd_rn(hi, p);
-            const float bb = __fsub_rn(s, hi);
-            const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(p, bb));
-            hi = s;
-            lo = __fadd_rn(lo, __fadd_rn(err, pe));
-        } else {
-            wide += (double)x * (double)x;  // tiny, huge or non-finite
-        }
+        const float p = __fmul_rn(x, x);
+        const float pe = __fmaf_rn(x, x, -p);
+        const float s = __fadd_rn(hi, p);
+        const float bb = __fsub_rn(s, hi);
+        const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(p, bb));
+        hi = s;
+        lo = __fadd_rn(lo, __fadd_rn(err, pe));
     }
-
-    __device__ __forceinline__ double total() const { return ((double)hi + (double)lo) + wide; }
 };
+
+/* True when every square of the 8 values is exact in the fp32 pair arithmetic. */
+__device__ __forceinline__ bool squares_in_range(const float (&x)[8])
+{
+    float mx = 0.0f, mn = 1.0f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float a = fabsf(x[e]);
+        mx = fmaxf(mx, a);
+        mn = fminf(mn, a == 0.0f ? 1.0f : a);
+    }
+    return mx < 0x1p+62f && mn >= 0x1p-50f;  // NaN fails the first test
+}
+
+/* fp64 sum of squares of the elements of a group selected by mask; a real call, so the
+ * fp64 work runs only for the rare groups that need it. */
+__device__ __noinline__ double sumsq_wide(float x0, float x1, float x2, float x3, float x4, float x5,
+                                          float x6, float x7, uint32_t mask)
+{
+    const float x[8] = {x0, x1, x2, x3, x4, x5, x6, x7};
+    double t = 0.0;
+    for (int e = 0; e < 8; ++e)
+        if (mask >> e & 1u)
+            t += (double)x[e] * (double)x[e];
+    return t;
+}
+
+/* hi1 + lo1 += hi2 + lo2 in pair arithmetic (TwoSum on the leading parts). */
+__device__ __forceinline__ void pair_add(float& hi, float& lo, float h2, float l2)
+{
+    const float s = __fadd_rn(hi, h2);
+    const float bb = __fsub_rn(s, hi);
+    const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(h2, bb));
+    hi = s;
+    lo = __fadd_rn(__fadd_rn(lo, l2), err);
+}
 
 __device__ __forceinline__ bool not_finite(float x)
 {
@@ -168,14 +199,23 @@ __global__ void __launch_bounds__(kBlock) k_reduce(const __grid_constant__ Reduc
                 }
             }
             float gv[8];
+            uint32_t in = 0xffu;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const uint64_t i = b + e;
                 gv[e] = i < a.psi ? __fmul_rn(s[e], inv) : 0.0f;
-                if (i >= lo && i < hi) {
-                    bad |= not_finite(gv[e]);
-                    acc.add(gv[e]);
-                }
+                if (!full && !(i >= lo && i < hi))
+                    in &= ~(1u << e);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                bad |= (in >> e & 1u) && not_finite(gv[e]);
+            if (full && squares_in_range(gv)) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    acc.add_fast(gv[e]);
+            } else {
+                acc.wide += sumsq_wide(gv[0], gv[1], gv[2], gv[3], gv[4], gv[5], gv[6], gv[7], in);
             }
             if (full) {
                 __stcs(reinterpret_cast<float4*>(a.g + b), make_float4(gv[0], gv[1], gv[2], gv[3]));
@@ -183,18 +223,28 @@ __global__ void __launch_bounds__(kBlock) k_reduce(const __grid_constant__ Reduc
             } else {
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
-                    if (b + e >= lo && b + e < hi)
+                    if (in >> e & 1u)
                         a.g[b + e] = gv[e];
             }
         }
 
-        // fixed-order reduction of the tile's partial: shuffle tree, then warps in order
-        double d = acc.total();
+        // fixed-order reduction of the tile's partial: pair-arithmetic shuffle tree in fp32,
+        // then fp64 once per warp and the warps in order
+        float ph = acc.hi, pl = acc.lo;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            d += __shfl_xor_sync(0xffffffffu, d, o);
+        for (int o = 16; o > 0; o >>= 1) {
+            const float h2 = __shfl_xor_sync(0xffffffffu, ph, o);
+            const float l2 = __shfl_xor_sync(0xffffffffu, pl, o);
+            pair_add(ph, pl, h2, l2);
+        }
+        double wide = acc.wide;
+        if (__any_sync(0xffffffffu, wide != 0.0)) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                wide += __shfl_xor_sync(0xffffffffu, wide, o);
+        }
         if ((threadIdx.x & 31) == 0)
-            warp_part[threadIdx.x >> 5] = d;
+            warp_part[threadIdx.x >> 5] = ((double)ph + (double)pl) + wide;
         __syncthreads();
         if (threadIdx.x == 0) {
             double t = 0.0;
