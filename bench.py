@@ -359,7 +359,7 @@ def _e2e(args, z, torch, dev, wl, hp, reps, g, partials, master, m, v, out, st, 
     if avail < 2 * need:
         return {"value": None, "unit": "params/s", "h2d_bytes_per_step": need,
                 "d2h_bytes_per_step": z.STATE_BYTES, "note": f"skipped: {avail/1e9:.0f} GB host RAM free"}
-    W = 1 << 26
+    W = 1 << 24  # 2^24-element buckets: 256 MB of copies per bucket keeps the pipeline short
     lay = z.zero_partition(wl.psi, wl.n_ranks, wl.stage, 1, W)
     hreps = [torch.empty(P, dtype=torch.int16, pin_memory=True) for _ in range(N)]
     for h, r in zip(hreps, reps):
@@ -379,9 +379,86 @@ def _e2e(args, z, torch, dev, wl, hp, reps, g, partials, master, m, v, out, st, 
     dt = time.perf_counter() - t0
     return {"value": wl.psi * steps / dt, "unit": "params/s", "h2d_bytes_per_step": need,
             "d2h_bytes_per_step": z.STATE_BYTES, "steps": steps, "ms_per_step": dt / steps * 1e3,
-            "path": "zero_step_host: N pinned host gradient copies -> 2 x 64M-element staging "
+            "path": "zero_step_host: N pinned host gradient copies -> 2 x 16M-element staging "
                     "ring (H2D on a copy stream, overlapped with the bucket reduces) -> norm -> "
                     "AdamW; step state copied back to pinned host memory"}
+
+
+def run_sweep(args):
+    """Bandwidth sweep (one JSON line per point): psi = 2^k and 2^k+1, N in {2,4,8,16,64},
+    bf16 gradients ~N(0,1e-3).  Points whose N gradient copies do not fit beside the
+    state run bucketed: 2^27-element windows, each read from one bucket buffer per rank
+    (every window's copies are re-read from HBM; the buffers are far larger than L2)."""
+    import torch
+
+    import synth
+    import zero_partitioned_optimizer_shard_gb300 as z
+    from synth import workloads as W
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    s_ = stream.cuda_stream
+    ks = [int(k) for k in args.sweep_k.split(",")]
+    ns = [int(n) for n in args.sweep_n.split(",")]
+    free_total = torch.cuda.mem_get_info(dev)[1]
+    for k in ks:
+        for plus in (0, 1):
+            for N in ns:
+                for stage in ([1, 2, 3] if (k == ks[0] and plus == 0) else [2]):
+                    psi = (1 << k) + plus
+                    wl = W.sweep_point(psi, N, stage)
+                    lay0 = z.zero_partition(psi, N, stage)
+                    P = lay0.psi_padded
+                    state_bytes = 18 * P + 8 * lay0.n_tiles
+                    bucketed = N * P * 2 + state_bytes > 0.8 * free_total
+                    W_ = 1 << 27 if bucketed else 0
+                    lay = z.zero_partition(psi, N, stage, 1, W_)
+                    rep_len = lay.bucket_elems
+                    reps = [torch.empty(rep_len, dtype=torch.int16, device=dev) for _ in range(N)]
+                    for kk, r in enumerate(reps):
+                        synth.fill_dev(r.data_ptr(), wl.grad_out, wl.grad_kind, wl.grad_key(1, kk), 0,
+                                       rep_len, psi, wl.grad_sigma, 1.0, s_)
+                    bufs = {n: torch.empty(P, dtype=torch.float32, device=dev)
+                            for n in ("g", "master", "m", "v")}
+                    for t_, role, kind, sig in ((bufs["master"], synth.ROLE_MASTER, synth.NORMAL, 0.02),
+                                                (bufs["m"], synth.ROLE_MOM, synth.NORMAL, 1e-4),
+                                                (bufs["v"], synth.ROLE_VAR, synth.NORMAL_SQ, 1e-4)):
+                        synth.fill_dev(t_.data_ptr(), synth.OUT_F32, kind, wl.state_key(role), 0, P,
+                                       psi, sig, 1.0, s_)
+                    out = torch.empty(P, dtype=torch.int16, device=dev)
+                    partials = torch.empty(lay.n_tiles, dtype=torch.float64, device=dev)
+                    st = torch.empty(z.STATE_BYTES, dtype=torch.uint8, device=dev)
+                    z.zero_step_state_init(lay, 1.0, False, 1000, st, partials, stream)
+                    ptrs = [reps[kk].data_ptr() for b in range(lay.n_buckets) for kk in range(N)]
+                    hp = z.hparams()
+
+                    def step():
+                        z.zero_step(lay, hp, z.ZERO_BF16, ptrs, bufs["g"], partials, bufs["master"],
+                                    bufs["m"], bufs["v"], out, st, stream)
+
+                    for _ in range(3):
+                        step()
+                    torch.cuda.synchronize(dev)
+                    steps = max(3, min(200, int(2e9 / ((34 + 2 * N) * P)) + 1))
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    for _ in range(steps):
+                        step()
+                    e1.record(stream)
+                    torch.cuda.synchronize(dev)
+                    ms = e0.elapsed_time(e1) / steps
+                    print(json.dumps({
+                        "sweep": True, "psi": psi, "n_ranks": N, "stage": stage,
+                        "mode": "bucketed 2^27" if bucketed else "resident", "steps": steps,
+                        "ms_per_step": ms, "params_per_s": psi / (ms / 1e3),
+                        "gbs_at_26p2n": (26 + 2 * N) * P / (ms / 1e3) / 1e9,
+                        "gbs_moved_34p2n": (34 + 2 * N) * P / (ms / 1e3) / 1e9,
+                        "l2": "L2-resident regime" if (34 + 2 * N) * P < 129e6 else "HBM"}), flush=True)
+                    del reps, bufs, out, partials, st
+                    torch.cuda.empty_cache()
+    return 0
 
 
 def main():
@@ -393,6 +470,10 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="bandwidth sweep over psi and N (one JSON line per point)")
+    ap.add_argument("--sweep-k", default="20,24,27,29,30,31")
+    ap.add_argument("--sweep-n", default="2,4,8,16,64")
     ap.add_argument("--psi", type=int, default=None,
                     help="profiling only: the same recipe at another size (default: the "
                          "GPT-2-1.5B buffer)")
@@ -409,6 +490,8 @@ def main():
         fcntl.flock(lock, fcntl.LOCK_EX)  # ranks of one node build once, in turn
         __graft_entry__.build()
         fcntl.flock(lock, fcntl.LOCK_UN)
+    if args.sweep:
+        return run_sweep(args)
     return run_ours(args)
 
 

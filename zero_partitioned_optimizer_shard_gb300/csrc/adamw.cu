@@ -16,10 +16,16 @@
  * c, step_size, rbc2 and decay come from the step state written by the norm kernel; a
  * skipped step (overflow) leaves every byte untouched.
  *
- * GB300 design: HBM streaming, 16 bytes read and 14 written per element.  A persistent
- * grid-stride loop moves 8 elements per thread per iteration: two 128-bit loads from each
- * of g (non-coherent, L1 bypass), master, m, v (streaming), two 128-bit streaming stores
- * to each of master, m, v and one 128-bit store of 8 bf16 parameters.
+ * GB300 design: HBM streaming, 16 bytes read and 14 written per element.  The inputs
+ * are staged by the Blackwell bulk-copy engine: one thread per block issues
+ * cp.async.bulk copies of 4096-element chunks of g, master, m and v (64 KiB per chunk)
+ * into a three-stage shared-memory ring tracked by mbarriers, so up to 192 KiB per SM are
+ * in flight without holding registers.  One 256-thread block per SM (persistent,
+ * grid-stride over chunks) computes from shared memory and writes master, m, v and 8
+ * bf16 parameters per thread with streaming 128/64-bit stores.  The ragged end (the part
+ * after the last whole chunk, and the padding) is done element by element.  Every
+ * mbarrier wait is bounded (~2 s); on a timeout the block records an error in the step
+ * state, waits (bounded) for its copies in flight and leaves.
  */
 #include "zero_internal.h"
 
@@ -44,23 +50,41 @@ __device__ __forceinline__ float adamw_one(float g, float& p, float& m, float& v
     return p;
 }
 
-__device__ __forceinline__ float4 ld_nc_v4(const float* p)
-{
-    float4 v;
-    asm("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
-        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-        : "l"(p));
-    return v;
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-__global__ void __launch_bounds__(kBlock) k_adamw(const __grid_constant__ AdamwArgs a)
+__device__ __forceinline__ uint32_t smem_addr(const void* p)
 {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+/* Wait for phase `parity` of an mbarrier, at most ~2 s (4e9 cycles); 0 on timeout. */
+__device__ __forceinline__ uint32_t wait_parity_bounded(uint32_t bar, uint32_t parity)
+{
+    const long long t0 = clock64();
+    uint32_t ok = 0;
+    while (true) {
+        asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; "
+                     "selp.u32 %0, 1, 0, p; }"
+                     : "=r"(ok)
+                     : "r"(bar), "r"(parity)
+                     : "memory");
+        if (ok || clock64() - t0 > 4000000000LL)
+            return ok;
+    }
+}
+
+constexpr int kChunk = 4096;  // elements per bulk-copied chunk of each array
+constexpr int kStages = 3;
+constexpr size_t kSmemBytes = (size_t)kStages * 4 * kChunk * sizeof(float);  // 192 KiB
+
+__global__ void __launch_bounds__(kBlock, 1) k_adamw(const __grid_constant__ AdamwArgs a)
+{
+    extern __shared__ __align__(128) float ring[];  // kStages x {g, master, m, v} x kChunk
+    __shared__ __align__(8) uint64_t full[kStages];
     const zero_step_state_t* st = a.st;
     if (st->skip)
         return;
@@ -75,50 +99,84 @@ __global__ void __launch_bounds__(kBlock) k_adamw(const __grid_constant__ AdamwA
     s.omb2 = __fsub_rn(1.0f, a.beta2);
     s.eps = a.eps;
 
-    const uint64_t stride = (uint64_t)gridDim.x * kBlock;
-    const uint64_t tid = (uint64_t)blockIdx.x * kBlock + threadIdx.x;
-    const uint64_t n_full = a.psi / 8;  // groups of 8 with no padding
+    const uint64_t n_chunks = a.psi / kChunk;  // whole chunks, none holding padding
+    uint64_t mine = 0;                         // chunks of this block: blockIdx.x + i*gridDim.x
+    if (blockIdx.x < n_chunks)
+        mine = (n_chunks - 1 - blockIdx.x) / gridDim.x + 1;
+    const float* src[4] = {a.g, a.master, a.m, a.v};
 
-    for (uint64_t q = tid; q < n_full; q += stride) {
-        const uint64_t b = q * 8;
-        const float4 g0 = ld_nc_v4(a.g + b), g1 = ld_nc_v4(a.g + b + 4);
-        float4 p0 = __ldcs(reinterpret_cast<const float4*>(a.master + b));
-        float4 p1 = __ldcs(reinterpret_cast<const float4*>(a.master + b + 4));
-        float4 m0 = __ldcs(reinterpret_cast<const float4*>(a.m + b));
-        float4 m1 = __ldcs(reinterpret_cast<const float4*>(a.m + b + 4));
-        float4 v0 = __ldcs(reinterpret_cast<const float4*>(a.v + b));
-        float4 v1 = __ldcs(reinterpret_cast<const float4*>(a.v + b + 4));
-        uint4 o;
-        o.x = pack_bf16x2(adamw_one(g0.x, p0.x, m0.x, v0.x, s), adamw_one(g0.y, p0.y, m0.y, v0.y, s));
-        o.y = pack_bf16x2(adamw_one(g0.z, p0.z, m0.z, v0.z, s), adamw_one(g0.w, p0.w, m0.w, v0.w, s));
-        o.z = pack_bf16x2(adamw_one(g1.x, p1.x, m1.x, v1.x, s), adamw_one(g1.y, p1.y, m1.y, v1.y, s));
-        o.w = pack_bf16x2(adamw_one(g1.z, p1.z, m1.z, v1.z, s), adamw_one(g1.w, p1.w, m1.w, v1.w, s));
-        __stcs(reinterpret_cast<float4*>(a.master + b), p0);
-        __stcs(reinterpret_cast<float4*>(a.master + b + 4), p1);
-        __stcs(reinterpret_cast<float4*>(a.m + b), m0);
-        __stcs(reinterpret_cast<float4*>(a.m + b + 4), m1);
-        __stcs(reinterpret_cast<float4*>(a.v + b), v0);
-        __stcs(reinterpret_cast<float4*>(a.v + b + 4), v1);
-        __stcs(reinterpret_cast<uint4*>(a.out + b), o);
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < kStages; ++k)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&full[k])));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    auto issue = [&](uint64_t i) {  // chunk i of this block into stage i % kStages
+        const int k = (int)(i % kStages);
+        const uint64_t base = (blockIdx.x + i * gridDim.x) * (uint64_t)kChunk;
+        const uint32_t bar = smem_addr(&full[k]);
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                     ::"r"(bar), "r"((uint32_t)(4 * kChunk * sizeof(float))) : "memory");
+        for (int q = 0; q < 4; ++q)
+            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+                         "[%0], [%1], %2, [%3];"
+                         ::"r"(smem_addr(ring + (k * 4 + q) * kChunk)), "l"(src[q] + base),
+                         "r"((uint32_t)(kChunk * sizeof(float))), "r"(bar)
+                         : "memory");
+    };
+    if (threadIdx.x == 0)
+        for (uint64_t i = 0; i < mine && i < kStages; ++i)
+            issue(i);
+
+    for (uint64_t i = 0; i < mine; ++i) {
+        const int k = (int)(i % kStages);
+        const uint32_t ok = wait_parity_bounded(smem_addr(&full[k]), (uint32_t)((i / kStages) & 1));
+        if (__syncthreads_or(!ok)) {  // the whole block leaves together
+            if (threadIdx.x == 0) {
+                atomicOr(a.err, 1u);
+                for (uint64_t j = i; j < mine && j < i + kStages; ++j)
+                    wait_parity_bounded(smem_addr(&full[j % kStages]), (uint32_t)((j / kStages) & 1));
+            }
+            __syncthreads();
+            return;
+        }
+        const float* sg = ring + (k * 4 + 0) * kChunk;
+        const float* sp = ring + (k * 4 + 1) * kChunk;
+        const float* sm = ring + (k * 4 + 2) * kChunk;
+        const float* sv = ring + (k * 4 + 3) * kChunk;
+        const uint64_t base = (blockIdx.x + i * gridDim.x) * (uint64_t)kChunk;
+#pragma unroll
+        for (int e = threadIdx.x * 4; e < kChunk; e += kBlock * 4) {
+            const float4 g0 = *reinterpret_cast<const float4*>(sg + e);
+            float4 p0 = *reinterpret_cast<const float4*>(sp + e);
+            float4 m0 = *reinterpret_cast<const float4*>(sm + e);
+            float4 v0 = *reinterpret_cast<const float4*>(sv + e);
+            uint2 o;
+            o.x = pack_bf16x2(adamw_one(g0.x, p0.x, m0.x, v0.x, s), adamw_one(g0.y, p0.y, m0.y, v0.y, s));
+            o.y = pack_bf16x2(adamw_one(g0.z, p0.z, m0.z, v0.z, s), adamw_one(g0.w, p0.w, m0.w, v0.w, s));
+            __stcs(reinterpret_cast<float4*>(a.master + base + e), p0);
+            __stcs(reinterpret_cast<float4*>(a.m + base + e), m0);
+            __stcs(reinterpret_cast<float4*>(a.v + base + e), v0);
+            __stcs(reinterpret_cast<uint2*>(a.out + base + e), o);
+        }
+        __syncthreads();  // stage k fully read: refill it
+        if (threadIdx.x == 0 && i + kStages < mine)
+            issue(i + kStages);
     }
 
-    // the ragged end: the group holding psi, and whole padding groups up to psi_padded
-    const uint64_t n_groups = (a.psi_padded + 7) / 8;
-    for (uint64_t q = n_full + tid; q < n_groups; q += stride) {
-        for (int e = 0; e < 8; ++e) {
-            const uint64_t i = q * 8 + e;
-            if (i >= a.psi_padded)
-                break;
-            if (i < a.psi) {
-                float p = a.master[i], m = a.m[i], v = a.v[i];
-                const float r = adamw_one(a.g[i], p, m, v, s);
-                a.master[i] = p;
-                a.m[i] = m;
-                a.v[i] = v;
-                a.out[i] = __bfloat16_as_ushort(__float2bfloat16_rn(r));
-            } else {
-                a.out[i] = 0;  // padding: gathered value 0, state untouched
-            }
+    // the ragged end: after the last whole chunk, up to psi_padded (padding gets out = 0)
+    const uint64_t stride = (uint64_t)gridDim.x * kBlock;
+    const uint64_t tid = (uint64_t)blockIdx.x * kBlock + threadIdx.x;
+    for (uint64_t i = n_chunks * kChunk + tid; i < a.psi_padded; i += stride) {
+        if (i < a.psi) {
+            float p = a.master[i], m = a.m[i], v = a.v[i];
+            const float r = adamw_one(a.g[i], p, m, v, s);
+            a.master[i] = p;
+            a.m[i] = m;
+            a.v[i] = v;
+            a.out[i] = __bfloat16_as_ushort(__float2bfloat16_rn(r));
+        } else {
+            a.out[i] = 0;  // padding: gathered value 0, state untouched
         }
     }
 }
@@ -127,20 +185,22 @@ __global__ void __launch_bounds__(kBlock) k_adamw(const __grid_constant__ AdamwA
 
 cudaError_t launch_adamw(const AdamwArgs& a, cudaStream_t s)
 {
-    static int per_sm[64] = {0};
+    static bool configured[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
-    int& occ = per_sm[dev & 63];
-    if (occ == 0) {
-        int o = 0;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, k_adamw, kBlock, 0);
-        occ = o > 0 ? o : 1;
+    if (!configured[dev & 63]) {
+        cudaError_t e = cudaFuncSetAttribute(k_adamw, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytes);
+        if (e != cudaSuccess)
+            return e;
+        configured[dev & 63] = true;
     }
-    const uint64_t groups = (a.psi_padded + 7) / 8;
-    const uint64_t want = (groups + kBlock - 1) / kBlock;
-    const uint64_t cap = (uint64_t)sm_count() * (uint64_t)occ;
+    const uint64_t chunks = a.psi / kChunk;
+    const uint64_t tail_blocks = (a.psi_padded - chunks * kChunk + kBlock - 1) / kBlock;
+    const uint64_t want = chunks > tail_blocks ? chunks : tail_blocks;
+    const uint64_t cap = (uint64_t)sm_count();  // one 192 KiB block per SM
     const unsigned grid = (unsigned)(want < cap ? want : cap);
-    k_adamw<<<grid > 0 ? grid : 1, kBlock, 0, s>>>(a);
+    k_adamw<<<grid > 0 ? grid : 1, kBlock, kSmemBytes, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -143,6 +143,7 @@ int adamw(const zero_layout_t* L, const zero_adamw_hparams_t* hp, const float* g
     a.v = v;
     a.out = params;
     a.st = st;
+    a.err = const_cast<uint32_t*>(&st->error);
     a.psi = L->psi;
     a.psi_padded = L->psi_padded;
     a.beta1 = hp->beta1;

@@ -32,26 +32,11 @@ namespace {
 constexpr int kFinThreads = 256;
 constexpr int kFinMaxBlocks = 128;
 
-/* Fixed-order block sum; the result is valid in thread 0. */
-__device__ __forceinline__ double block_sum(double v, double* red)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        v += __shfl_xor_sync(0xffffffffu, v, o);
-    if ((threadIdx.x & 31) == 0)
-        red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    double t = 0.0;
-    if (threadIdx.x == 0)
-        for (int w = 0; w < kFinThreads / 32; ++w)
-            t += red[w];
-    __syncthreads();
-    return t;
-}
+constexpr int kBatch = 8;  // ranks summed together by one block pass
 
 __global__ void __launch_bounds__(kFinThreads) k_finalize(const __grid_constant__ FinalizeArgs a)
 {
-    __shared__ double red[kFinThreads / 32];
+    __shared__ double red[kFinThreads / 32][kBatch];
     __shared__ double rank_sum[ZERO_MAX_KERNEL_RANKS];
     __shared__ int is_last;
     const uint32_t N = a.n_ranks;
@@ -59,18 +44,40 @@ __global__ void __launch_bounds__(kFinThreads) k_finalize(const __grid_constant_
     const uint64_t chunk = (tpr + gridDim.x - 1) / gridDim.x;
     const uint64_t j0 = (uint64_t)blockIdx.x * chunk;
     const uint64_t j1 = j0 + chunk < tpr ? j0 + chunk : tpr;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // this block's chunk of every rank
-    for (uint32_t r = 0; r < N; ++r) {
-        double* p = a.partials + (uint64_t)r * tpr;
-        double s = 0.0;
+    // this block's chunk of every rank, kBatch ranks at a time: each thread sums its
+    // slots in order, a shuffle tree folds each warp, warps are folded in order
+    for (uint32_t r0 = 0; r0 < N; r0 += kBatch) {
+        double acc[kBatch];
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q)
+            acc[q] = 0.0;
         for (uint64_t j = j0 + threadIdx.x; j < j1; j += kFinThreads) {
-            s += p[j];
-            p[j] = 0.0;
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q)
+                if (r0 + q < N) {
+                    double* p = a.partials + (uint64_t)(r0 + q) * tpr + j;
+                    acc[q] += *p;
+                    *p = 0.0;
+                }
         }
-        s = block_sum(s, red);
-        if (threadIdx.x == 0 && j0 < j1)
-            p[j0] = s;
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
+            if (lane == 0)
+                red[w][q] = acc[q];
+        }
+        __syncthreads();
+        if (threadIdx.x < kBatch && r0 + threadIdx.x < N && j0 < j1) {
+            double t = 0.0;
+            for (int ww = 0; ww < kFinThreads / 32; ++ww)
+                t += red[ww][threadIdx.x];
+            a.partials[(uint64_t)(r0 + threadIdx.x) * tpr + j0] = t;
+        }
+        __syncthreads();
     }
     __threadfence();
     __syncthreads();
@@ -82,14 +89,23 @@ __global__ void __launch_bounds__(kFinThreads) k_finalize(const __grid_constant_
     __threadfence();
 
     // the last block: chunk sums in order per rank (one warp per rank), ranks in order
-    const uint64_t n_chunks = (tpr + chunk - 1) / chunk;
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t n_chunks = (tpr + chunk - 1) / chunk;  // at most kFinMaxBlocks = 4 x 32
     for (uint32_t r = w; r < N; r += kFinThreads / 32) {
         double* p = a.partials + (uint64_t)r * tpr;
+        double v[kFinMaxBlocks / 32];
+#pragma unroll
+        for (int q = 0; q < kFinMaxBlocks / 32; ++q) {
+            const uint64_t c = lane + 32u * q;
+            v[q] = c < n_chunks ? __ldcg(p + c * chunk) : 0.0;
+        }
         double s = 0.0;
-        for (uint64_t c = lane; c < n_chunks; c += 32) {
-            s += __ldcg(p + c * chunk);
-            p[c * chunk] = 0.0;
+#pragma unroll
+        for (int q = 0; q < kFinMaxBlocks / 32; ++q) {
+            const uint64_t c = lane + 32u * q;
+            if (c < n_chunks) {
+                s += v[q];
+                p[c * chunk] = 0.0;
+            }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)

@@ -165,6 +165,7 @@ extern "C" int zero_step_static_workspace(const zero_layout_t* layout,
     u.v = v;
     u.out = params;
     u.st = st;
+    u.err = &st->error;
     u.psi = layout->psi;
     u.psi_padded = P;
     u.beta1 = hp->beta1;

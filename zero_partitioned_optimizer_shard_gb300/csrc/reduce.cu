@@ -112,17 +112,19 @@ struct SumSq {
     }
 };
 
-/* True when every square of the 8 values is exact in the fp32 pair arithmetic. */
+/* True when all 8 values are finite and every square is exact in the fp32 pair
+ * arithmetic: magnitudes in [2^-50, 2^62) or zero.  Integer compares on the magnitude
+ * bits, so NaN (above inf) and inf fail the test too. */
 __device__ __forceinline__ bool squares_in_range(const float (&x)[8])
 {
-    float mx = 0.0f, mn = 1.0f;
+    uint32_t mx = 0u, mn = 0x3f800000u;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-        const float a = fabsf(x[e]);
-        mx = fmaxf(mx, a);
-        mn = fminf(mn, a == 0.0f ? 1.0f : a);
+        const uint32_t u = __float_as_uint(x[e]) & 0x7fffffffu;
+        mx = max(mx, u);
+        mn = min(mn, u == 0u ? 0x3f800000u : u);
     }
-    return mx < 0x1p+62f && mn >= 0x1p-50f;  // NaN fails the first test
+    return mx < 0x5e800000u && mn >= 0x26800000u;  // 2^62 and 2^-50
 }
 
 /* fp64 sum of squares of the elements of a group selected by mask; a real call, so the
@@ -199,22 +201,28 @@ __global__ void __launch_bounds__(kBlock) k_reduce(const __grid_constant__ Reduc
                 }
             }
             float gv[8];
-            uint32_t in = 0xffu;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const uint64_t i = b + e;
-                gv[e] = i < a.psi ? __fmul_rn(s[e], inv) : 0.0f;
-                if (!full && !(i >= lo && i < hi))
-                    in &= ~(1u << e);
-            }
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                bad |= (in >> e & 1u) && not_finite(gv[e]);
-            if (full && squares_in_range(gv)) {
+                gv[e] = __fmul_rn(s[e], inv);
+            uint32_t in = 0xffu;
+            if (b + 8 > a.psi || !full) {  // the padding, or a group cut by the tile/window
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint64_t i = b + e;
+                    if (i >= a.psi)
+                        gv[e] = 0.0f;
+                    if (!(i >= lo && i < hi))
+                        in &= ~(1u << e);
+                }
+            }
+            if (full && squares_in_range(gv)) {  // all finite: no overflow to record
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
                     acc.add_fast(gv[e]);
             } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    bad |= (in >> e & 1u) && not_finite(gv[e]);
                 acc.wide += sumsq_wide(gv[0], gv[1], gv[2], gv[3], gv[4], gv[5], gv[6], gv[7], in);
             }
             if (full) {

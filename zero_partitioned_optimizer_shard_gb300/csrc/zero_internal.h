@@ -39,6 +39,7 @@ struct AdamwArgs {
     float* v;
     uint16_t* out;
     const zero_step_state_t* st;
+    uint32_t* err;                           // the state's error word (bounded waits)
     uint64_t psi, psi_padded;
     float beta1, beta2, eps;
 };
