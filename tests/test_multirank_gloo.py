@@ -1,0 +1,146 @@
+"""The ZeRO step across real processes (torch.distributed, gloo, CPU): one process per rank.
+
+Every rank holds its own gradient copy of the whole flat buffer and only its own shard of
+the fp32 master/m/v state, as ZeRO-2 prescribes ("【论文解读】ZeRO" sec. 4(2), 6(2)):
+  1. reduce-scatter: rank r receives every rank's copy of shard r and averages it (here
+     an all-gather of the copies followed by the rank-ordered sum, the same arithmetic
+     the single-GPU kernels use);
+  2. the global-norm all-reduce (the Megatron page, sec. 1): the per-rank sums of squares
+     and overflow flags are all-gathered and added in rank order;
+  3. each rank applies AdamW to its own shard, then the bf16 shards are all-gathered into
+     the full parameter vector.
+The gathered parameters, the norm and every rank's shard state must equal the
+single-process oracle's bit for bit.  World size 4 uses the pages' 8-parameter, 4-GPU
+example shape as one of its cases.  No GPU is used.
+"""
+import os
+import queue
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import oracle
+import synth
+
+SIGMA = 1e-3
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _state(role, kind, sig, begin, count, psi, seed):
+    return synth.fill_host(synth.OUT_F32, kind, synth.key(seed, role), begin, count, psi, sig)
+
+
+def _rank_main(rank, world, port, psi, seed, steps, clip, out_q):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        orc = oracle.load()
+        lay = orc.partition(psi, world, 2)
+        S, P = lay.shard, lay.psi_padded
+        lo = rank * S
+        hp = oracle.hparams(max_grad_norm=clip)
+        sc = oracle.scaler(1.0, False)
+        # this rank's shard of the optimizer state, laid out at its flat offsets
+        master = np.zeros(P, np.float32)
+        m = np.zeros(P, np.float32)
+        v = np.zeros(P, np.float32)
+        master[lo:lo + S] = _state(synth.ROLE_MASTER, synth.NORMAL, 0.02, lo, S, psi, seed)
+        m[lo:lo + S] = _state(synth.ROLE_MOM, synth.NORMAL, 1e-4, lo, S, psi, seed)
+        v[lo:lo + S] = _state(synth.ROLE_VAR, synth.NORMAL_SQ, 1e-4, lo, S, psi, seed)
+        g = np.zeros(P, np.float32)
+        out = np.zeros(P, np.uint16)
+        results = []
+        for step in range(1, steps + 1):
+            mine = synth.fill_host(synth.OUT_BF16, synth.NORMAL,
+                                   synth.key(seed, synth.ROLE_GRAD, step, rank), 0, P, psi, SIGMA)
+            # gloo has no 16-bit collectives: the bit patterns travel as int32
+            copies = [torch.empty(P, dtype=torch.int32) for _ in range(world)]
+            dist.all_gather(copies, torch.from_numpy(mine.astype(np.int32)))
+            shard_copies = [c.numpy()[lo:lo + S].astype(np.uint16) for c in copies]
+            sumsq = np.zeros(world, np.float64)
+            ov = np.zeros(1, np.uint32)
+            orc.reduce_window(lay, oracle.BF16, shard_copies, lo, S, orc.inv_scale(world, 1.0),
+                              g[lo:lo + S], sumsq, ov)
+            parts = [torch.zeros(2, dtype=torch.float64) for _ in range(world)]
+            dist.all_gather(parts, torch.tensor([sumsq[rank], float(ov[0])], dtype=torch.float64))
+            q = np.array([float(p[0]) for p in parts])
+            overflow = int(any(float(p[1]) != 0.0 for p in parts))
+            norm, _ = orc.global_norm(q)
+            applied = orc.scaler_update(sc, overflow)
+            c = orc.clip_coef(norm, hp.max_grad_norm) if applied else 1.0
+            if applied:
+                orc.adamw_shard(lay, hp, c, sc.t, rank, g, master, m, v, out)
+            shards = [torch.empty(S, dtype=torch.int32) for _ in range(world)]
+            dist.all_gather(shards, torch.from_numpy(out[lo:lo + S].astype(np.int32)))
+            gathered = np.concatenate([t.numpy().astype(np.uint16) for t in shards])
+            results.append((norm, c, gathered))
+        out_q.put((rank, results, master[lo:lo + S].copy(), m[lo:lo + S].copy(),
+                   v[lo:lo + S].copy(), g[lo:lo + S].copy()))
+    finally:
+        dist.destroy_process_group()
+
+
+def _single_process(world, psi, seed, steps, clip):
+    orc = oracle.load()
+    lay = orc.partition(psi, world, 2)
+    P = lay.psi_padded
+    hp = oracle.hparams(max_grad_norm=clip)
+    sc = oracle.scaler(1.0, False)
+    master = _state(synth.ROLE_MASTER, synth.NORMAL, 0.02, 0, P, psi, seed)
+    m = _state(synth.ROLE_MOM, synth.NORMAL, 1e-4, 0, P, psi, seed)
+    v = _state(synth.ROLE_VAR, synth.NORMAL_SQ, 1e-4, 0, P, psi, seed)
+    g = np.zeros(P, np.float32)
+    out = np.zeros(P, np.uint16)
+    res = []
+    for step in range(1, steps + 1):
+        reps = [synth.fill_host(synth.OUT_BF16, synth.NORMAL,
+                                synth.key(seed, synth.ROLE_GRAD, step, k), 0, P, psi, SIGMA)
+                for k in range(world)]
+        rep = orc.step(lay, hp, oracle.BF16, reps, g, master, m, v, out, sc)
+        res.append((rep.norm, rep.clip_coef, out.copy()))
+    return lay, res, master, m, v, g
+
+
+@pytest.mark.parametrize("world,psi,clip", [(2, 10_001, 1e-3), (4, 8, 0.0), (4, 333, 1.0)])
+def test_ranks_as_processes_match_single_process(world, psi, clip):
+    seed, steps = 11, 3
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, psi, seed, steps, clip, q))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    got = {}
+    try:
+        for _ in range(world):
+            rank, results, master, m, v, g = q.get(timeout=300)
+            got[rank] = (results, master, m, v, g)
+    except queue.Empty:
+        pytest.fail(f"ranks {sorted(set(range(world)) - set(got))} returned nothing")
+    finally:
+        for p in procs:
+            p.join(timeout=60)
+            if p.is_alive():
+                p.terminate()
+    assert all(p.exitcode == 0 for p in procs)
+    lay, ref, master, m, v, g = _single_process(world, psi, seed, steps, clip)
+    S = lay.shard
+    for r in range(world):
+        results, ms, mm, mv, mg = got[r]
+        for (n_a, c_a, out_a), (n_b, c_b, out_b) in zip(results, ref):
+            assert n_a == n_b and c_a == c_b
+            assert np.array_equal(out_a, out_b)
+        sl = slice(r * S, (r + 1) * S)
+        for a, b in ((ms, master[sl]), (mm, m[sl]), (mv, v[sl]), (mg, g[sl])):
+            assert np.array_equal(a.view(np.uint32), b.view(np.uint32))

@@ -176,9 +176,11 @@ __global__ void __launch_bounds__(kBlock) k_reduce(const __grid_constant__ Reduc
         SumSq acc;
         for (uint64_t b = (lo & ~7ull) + 8ull * threadIdx.x; b < hi; b += 8ull * kBlock) {
             float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            const bool full = b >= lo && b + 8 <= hi;
-            const uint64_t off = b - a.begin;  // a multiple of 8: begin is
-            if (full) {
+            const bool full = b >= lo && b + 8 <= hi;  // all 8 elements belong to this tile
+            const uint64_t off = b - a.begin;            // a multiple of 8: begin is
+            if (b + 8 <= a.end) {
+                // the whole group lies inside the window's buffers: 128-bit loads, even
+                // where it straddles a tile edge (the other tile's elements are masked)
 #pragma unroll 1
                 for (int k0 = 0; k0 < N; k0 += kLoadBatch) {
                     uint4 v[kLoadBatch];
@@ -191,7 +193,7 @@ __global__ void __launch_bounds__(kBlock) k_reduce(const __grid_constant__ Reduc
                         if (NR > 0 ? (k0 + kk < NR) : (k0 + kk < N))
                             add8<DT>(s, v[kk]);
                 }
-            } else {
+            } else {  // the window's last, ragged group: element loads inside [lo, hi) only
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const uint64_t i = b + e;
@@ -200,12 +202,12 @@ __global__ void __launch_bounds__(kBlock) k_reduce(const __grid_constant__ Reduc
                             s[e] = __fadd_rn(s[e], one16<DT>(ld_stream_u16((const uint16_t*)a.rep[k] + off + e)));
                 }
             }
-            float gv[8];
+            float gv[8], sq[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                gv[e] = __fmul_rn(s[e], inv);
+                gv[e] = sq[e] = __fmul_rn(s[e], inv);
             uint32_t in = 0xffu;
-            if (b + 8 > a.psi || !full) {  // the padding, or a group cut by the tile/window
+            if (b + 8 > a.psi || !full) {  // padding, or a group cut by the tile/window edge
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const uint64_t i = b + e;
@@ -213,12 +215,13 @@ __global__ void __launch_bounds__(kBlock) k_reduce(const __grid_constant__ Reduc
                         gv[e] = 0.0f;
                     if (!(i >= lo && i < hi))
                         in &= ~(1u << e);
+                    sq[e] = (in >> e & 1u) ? gv[e] : 0.0f;
                 }
             }
-            if (full && squares_in_range(gv)) {  // all finite: no overflow to record
+            if (squares_in_range(sq)) {  // every counted element finite: no overflow
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
-                    acc.add_fast(gv[e]);
+                    acc.add_fast(sq[e]);
             } else {
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
