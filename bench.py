@@ -397,7 +397,7 @@ def run_sweep(args):
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    stream = torch.cuda.current_stream(dev)
+    stream = torch.cuda.Stream(dev)  # a side stream: CUDA graphs cannot capture the default one
     s_ = stream.cuda_stream
     ks = [int(k) for k in args.sweep_k.split(",")]
     ns = [int(n) for n in args.sweep_n.split(",")]
@@ -441,23 +441,137 @@ def run_sweep(args):
                         step()
                     torch.cuda.synchronize(dev)
                     steps = max(3, min(200, int(2e9 / ((34 + 2 * N) * P)) + 1))
+                    run = step
+                    graph = None
+                    if args.graph:  # replay the step's launches from a CUDA graph
+                        graph = torch.cuda.CUDAGraph()
+                        with torch.cuda.graph(graph, stream=stream):
+                            step()
+                        run = graph.replay
+                        for _ in range(3):
+                            run()
+                        torch.cuda.synchronize(dev)
                     e0 = torch.cuda.Event(enable_timing=True)
                     e1 = torch.cuda.Event(enable_timing=True)
                     e0.record(stream)
                     for _ in range(steps):
-                        step()
+                        run()
                     e1.record(stream)
                     torch.cuda.synchronize(dev)
                     ms = e0.elapsed_time(e1) / steps
                     print(json.dumps({
                         "sweep": True, "psi": psi, "n_ranks": N, "stage": stage,
                         "mode": "bucketed 2^27" if bucketed else "resident", "steps": steps,
+                        "launch": "cuda graph replay" if args.graph else "direct",
                         "ms_per_step": ms, "params_per_s": psi / (ms / 1e3),
                         "gbs_at_26p2n": (26 + 2 * N) * P / (ms / 1e3) / 1e9,
                         "gbs_moved_34p2n": (34 + 2 * N) * P / (ms / 1e3) / 1e9,
                         "l2": "L2-resident regime" if (34 + 2 * N) * P < 129e6 else "HBM"}), flush=True)
-                    del reps, bufs, out, partials, st
+                    del reps, bufs, out, partials, st, graph
                     torch.cuda.empty_cache()
+    return 0
+
+
+def run_overlap(args):
+    """Gradient buckets arriving from a synthetic backward pass, reduced as they arrive.
+
+    The Llama-7B-shaped buffer (psi = 6,738,415,616, N = 8, ZeRO-3) with its gradients in
+    2^27-element buckets through a two-slot ring of constant-size buffers: a producer
+    stream writes bucket b+1's N gradient copies (the seeded generator stands in for the
+    backward pass) while the compute stream reduces bucket b; then the norm and AdamW.
+    Reported: the overlapped step, the producer alone, the consumer alone (reduces of
+    already-produced buckets + norm + AdamW), and the overlap efficiency
+    (producer + consumer) / overlapped - 1 relative to its maximum."""
+    import torch
+
+    import synth
+    import zero_partitioned_optimizer_shard_gb300 as z
+    from synth import workloads as W
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl = W.C3
+    lay = z.zero_partition(wl.psi, wl.n_ranks, wl.stage, 1, wl.bucket_elems)
+    P, N, Wb, nb = lay.psi_padded, lay.n_ranks, lay.bucket_elems, lay.n_buckets
+    # the reduce runs on a high-priority stream; the producer (the synthetic backward)
+    # leaves room on every SM (4 of the generator's blocks per SM) so the two can co-reside
+    comp = torch.cuda.Stream(dev, priority=-1)
+    prod = torch.cuda.Stream(dev)
+    PRODUCER_BLOCKS_PER_SM = 4
+    ring = [[torch.empty(Wb, dtype=torch.int16, device=dev) for _ in range(N)] for _ in range(2)]
+    bufs = {n: torch.empty(P, dtype=torch.float32, device=dev) for n in ("g", "master", "m", "v")}
+    for t_, role, kind, sig in ((bufs["master"], synth.ROLE_MASTER, synth.NORMAL, wl.master_sigma),
+                                (bufs["m"], synth.ROLE_MOM, synth.NORMAL, wl.mom_sigma),
+                                (bufs["v"], synth.ROLE_VAR, synth.NORMAL_SQ, wl.mom_sigma)):
+        synth.fill_dev(t_.data_ptr(), synth.OUT_F32, kind, wl.state_key(role), 0, P, wl.psi, sig,
+                       1.0, comp.cuda_stream)
+    out = torch.empty(P, dtype=torch.int16, device=dev)
+    partials = torch.empty(lay.n_tiles, dtype=torch.float64, device=dev)
+    st = torch.empty(z.STATE_BYTES, dtype=torch.uint8, device=dev)
+    z.zero_step_state_init(lay, 1.0, False, 1000, st, partials, comp)
+    hp = z.hparams(**wl.hp.__dict__)
+    filled = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
+
+    def produce(step, b, slot, stream):
+        begin, count = b * Wb, min(Wb, P - b * Wb)
+        for k in range(N):
+            synth.fill_dev(ring[slot][k].data_ptr(), wl.grad_out, wl.grad_kind, wl.grad_key(step, k),
+                           begin, count, wl.psi, wl.grad_sigma, 1.0, stream.cuda_stream,
+                           PRODUCER_BLOCKS_PER_SM)
+        return begin, count
+
+    def reduce(b, slot):
+        begin, count = b * Wb, min(Wb, P - b * Wb)
+        z.zero_reduce_shard_unscale(lay, z.ZERO_BF16, [r.data_ptr() for r in ring[slot]], begin, count,
+                                    bufs["g"], partials, st, comp)
+
+    def tail():
+        z.zero_grad_norm(lay, hp, partials, st, comp)
+        z.zero_adamw_cast_gather(lay, hp, bufs["g"], bufs["master"], bufs["m"], bufs["v"], out, st, comp)
+
+    def overlapped(step):
+        prod.wait_stream(comp)
+        for b in range(nb):
+            slot = b & 1
+            if b >= 2:
+                prod.wait_event(consumed[slot])
+            produce(step, b, slot, prod)
+            filled[slot].record(prod)
+            comp.wait_event(filled[slot])
+            reduce(b, slot)
+            consumed[slot].record(comp)
+        tail()
+
+    def timed(fn, reps):
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(comp)
+        for r in range(reps):
+            fn(r)
+        e1.record(comp)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / reps
+
+    reps = max(1, args.steps // 10)
+    for w in range(args.warmup):
+        overlapped(1 + w)
+    t_over = timed(lambda r: overlapped(100 + r), reps)
+    t_prod = timed(lambda r: [produce(200 + r, b, b & 1, comp) for b in range(nb)], reps)
+
+    def consumer_only(r):  # the ring already holds data; reduce every bucket from it
+        for b in range(nb):
+            reduce(b, b & 1)
+        tail()
+    t_cons = timed(consumer_only, reps)
+    line = {"overlap": True, "workload": wl.name, "buckets": nb, "bucket_elems": Wb,
+            "ring_bytes": 2 * N * Wb * 2, "steps": reps,
+            "ms_overlapped_step": t_over, "ms_producer_alone": t_prod, "ms_consumer_alone": t_cons,
+            "ms_serial_sum": t_prod + t_cons,
+            "overlap_efficiency": (t_prod + t_cons - t_over) / min(t_prod, t_cons),
+            "params_per_s_overlapped": wl.psi / (t_over / 1e3)}
+    print(json.dumps(line), flush=True)
     return 0
 
 
@@ -473,6 +587,10 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="bandwidth sweep over psi and N (one JSON line per point)")
     ap.add_argument("--sweep-k", default="20,24,27,29,30,31")
+    ap.add_argument("--graph", action="store_true", help="sweep: replay each step from a CUDA graph")
+    ap.add_argument("--overlap", action="store_true",
+                    help="bucket arrival overlapped with a synthetic backward producer "
+                         "(Llama-7B buffer, 2^27-element buckets)")
     ap.add_argument("--sweep-n", default="2,4,8,16,64")
     ap.add_argument("--psi", type=int, default=None,
                     help="profiling only: the same recipe at another size (default: the "
@@ -492,6 +610,8 @@ def main():
         fcntl.flock(lock, fcntl.LOCK_UN)
     if args.sweep:
         return run_sweep(args)
+    if args.overlap:
+        return run_overlap(args)
     return run_ours(args)
 
 

@@ -88,7 +88,8 @@ def dev():
     if _dev is None:
         L = C.CDLL(build_dev())
         L.zsynth_fill_dev.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_uint64, C.c_uint64,
-                                      C.c_uint64, C.c_uint64, C.c_float, C.c_float, C.c_void_p]
+                                      C.c_uint64, C.c_uint64, C.c_float, C.c_float, C.c_void_p,
+                                      C.c_int]
         L.zsynth_fill_dev.restype = C.c_int
         _dev = L
     return _dev
@@ -117,7 +118,8 @@ def gather_host(out: int, kind: int, k: int, idx: np.ndarray, valid_end: int, si
 
 
 def fill_dev(ptr: int, out: int, kind: int, k: int, begin: int, count: int, valid_end: int,
-             sigma: float, scale: float = 1.0, stream: int = 0) -> None:
-    rc = dev().zsynth_fill_dev(ptr, out, kind, k, begin, count, valid_end, sigma, scale, stream)
+             sigma: float, scale: float = 1.0, stream: int = 0, blocks_per_sm: int = 0) -> None:
+    rc = dev().zsynth_fill_dev(ptr, out, kind, k, begin, count, valid_end, sigma, scale, stream,
+                               blocks_per_sm)
     if rc != 0:
         raise RuntimeError(f"zsynth_fill_dev failed ({rc})")

@@ -26,9 +26,11 @@ __global__ void k_zsynth_fill(void* __restrict__ dst, int kind, uint64_t key, ui
     }
 }
 
+/* blocks_per_sm caps the grid (0 = 16 per SM, the whole GPU); a small cap leaves SMs for
+ * kernels that run beside the generator. */
 extern "C" int zsynth_fill_dev(void* dst, int out, int kind, uint64_t key, uint64_t begin,
                                uint64_t count, uint64_t valid_end, float sigma, float scale,
-                               void* stream)
+                               void* stream, int blocks_per_sm)
 {
     if (count == 0)
         return 0;
@@ -38,7 +40,7 @@ extern "C" int zsynth_fill_dev(void* dst, int out, int kind, uint64_t key, uint6
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     uint64_t want = (count + 255) / 256;
-    uint64_t cap = (uint64_t)(sms > 0 ? sms : 1) * 16;
+    uint64_t cap = (uint64_t)(sms > 0 ? sms : 1) * (uint64_t)(blocks_per_sm > 0 ? blocks_per_sm : 16);
     unsigned grid = (unsigned)(want < cap ? want : cap);
     cudaStream_t s = (cudaStream_t)stream;
     if (out == ZS_OUT_F32)

@@ -292,3 +292,74 @@ def test_generator_twins_agree():
         synth.fill_dev(d.data_ptr(), out, kind, k, begin, n, begin + n - 100, sigma, scale)
         h = synth.fill_host(out, kind, k, begin, n, begin + n - 100, sigma, scale)
         assert np.array_equal(d.cpu().numpy().view(np.uint8), h.view(np.uint8))
+
+
+def test_zero_step_replays_from_a_cuda_graph():
+    """zero_step enqueues kernels only (no host sync, no allocation), so a caller can
+    capture it in a CUDA graph; replaying the graph gives the same bits as direct calls."""
+    wl = W.scaled(W.C2, 200_003, steps=3)
+    direct = GpuRun(wl)
+    graphed = GpuRun(wl, guarded=False)
+    stream = torch.cuda.Stream()
+    graphed.stream = stream
+    with torch.cuda.stream(stream):
+        graphed.gen_grads(1)
+        dt = z.ZERO_BF16
+        ptrs = graphed.bucket_ptrs()
+        # first call outside the capture (per-device set-up: occupancy, shared-memory size)
+        z.zero_step(graphed.lay, graphed.hp, dt, ptrs, graphed.g, graphed.partials, graphed.master,
+                    graphed.m, graphed.v, graphed.out, graphed.st, stream)
+        direct.step(1)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            z.zero_step(graphed.lay, graphed.hp, dt, ptrs, graphed.g, graphed.partials,
+                        graphed.master, graphed.m, graphed.v, graphed.out, graphed.st, stream)
+        for s in (2, 3):
+            graphed.gen_grads(s)
+            g.replay()
+            direct.step(s)
+        torch.cuda.synchronize()
+    a, b = direct.arrays(), graphed.arrays()
+    for k in a:
+        assert np.array_equal(a[k].view(np.uint8), b[k].view(np.uint8)), k
+    sa, sb = direct.state(), graphed.state()
+    assert (sa.t, sa.norm, sa.clip_coef) == (sb.t, sb.norm, sb.clip_coef) and sa.t == 3
+
+
+def test_buckets_reduced_while_a_producer_writes_the_next():
+    """Gradient buckets produced on one stream and reduced on another through a two-slot
+    ring of constant-size buffers give the same bits as one zero_step on all copies."""
+    wl = W.scaled(W.C3, 5 * 65536 + 1000, steps=2)
+    Wb = 65536
+    ref = GpuRun(wl, bucket_elems=Wb)
+    pipe = GpuRun(wl, bucket_elems=Wb, guarded=False)
+    lay, N, P = pipe.lay, pipe.lay.n_ranks, pipe.lay.psi_padded
+    comp = pipe.stream
+    prod = torch.cuda.Stream()
+    ring = [[torch.empty(Wb, dtype=torch.int16, device="cuda") for _ in range(N)] for _ in range(2)]
+    filled = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
+    for step in (1, 2):
+        ref.step(step)
+        prod.wait_stream(comp)
+        for b in range(lay.n_buckets):
+            slot, begin = b & 1, b * Wb
+            count = min(Wb, P - begin)
+            if b >= 2:
+                prod.wait_event(consumed[slot])
+            for k in range(N):
+                synth.fill_dev(ring[slot][k].data_ptr(), wl.grad_out, wl.grad_kind,
+                               wl.grad_key(step, k), begin, count, wl.psi, wl.grad_sigma, 1.0,
+                               prod.cuda_stream)
+            filled[slot].record(prod)
+            comp.wait_event(filled[slot])
+            z.zero_reduce_shard_unscale(lay, z.ZERO_BF16, [r.data_ptr() for r in ring[slot]], begin,
+                                        count, pipe.g, pipe.partials, pipe.st, comp)
+            consumed[slot].record(comp)
+        z.zero_grad_norm(lay, pipe.hp, pipe.partials, pipe.st, comp)
+        z.zero_adamw_cast_gather(lay, pipe.hp, pipe.g, pipe.master, pipe.m, pipe.v, pipe.out, pipe.st,
+                                 comp)
+    torch.cuda.synchronize()
+    a, b = ref.arrays(), pipe.arrays()
+    for k in a:
+        assert np.array_equal(a[k].view(np.uint8), b[k].view(np.uint8)), k
