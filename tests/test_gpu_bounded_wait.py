@@ -1,0 +1,88 @@
+"""A device wait that runs out reports an error status and leaves the GPU usable.
+
+k_adamw waits on mbarriers for its bulk copies, and every such wait is bounded (~2 s).
+To exercise the timeout path without any fault, the test builds a test-only variant of
+the library (-DZERO_TEST_HOOKS; the product library has no such switch) in which one
+chunk's barrier is armed but its copies are withheld: a flag that nothing sets.  The
+kernel must give up, record 1 in the step state's error word, wait (bounded) for its
+other copies in flight and leave; the host sees a normal completion and reads the
+status; and the same process then runs a full step through the product library that
+still matches the oracle.
+"""
+import ctypes as C
+import os
+import subprocess
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import zero_partitioned_optimizer_shard_gb300 as z
+from synth import workloads as W
+from tests.gpu_harness import GpuRun, OracleRun, assert_scalars, assert_state_close
+from zero_partitioned_optimizer_shard_gb300 import _build
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def hooked(tmp_path_factory):
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available()
+    d = tmp_path_factory.mktemp("hooked")
+    objs = []
+    procs = []
+    for src in _build.SOURCES:
+        o = str(d / (os.path.splitext(src)[0] + ".o"))
+        procs.append(subprocess.Popen(["nvcc", *_build.NVCC_FLAGS, "-DZERO_TEST_HOOKS", "-c",
+                                       os.path.join(_build.CSRC, src), "-o", o]))
+        objs.append(o)
+    assert all(p.wait() == 0 for p in procs)
+    lib = str(d / "libzero_shard_hooked.so")
+    arch = _build.ARCH
+    subprocess.run(["nvcc", "-shared", f"-gencode=arch=compute_{arch},code=sm_{arch}", "-o", lib,
+                    *objs, "-lcudart"], check=True)
+    L = C.CDLL(lib)
+    L.zero_test_withhold_adamw_chunk.argtypes = [C.c_ulonglong]
+    L.zero_test_withhold_adamw_chunk.restype = C.c_int
+    L.zero_adamw_cast_gather.argtypes = [C.POINTER(z.Layout), C.POINTER(z.HParams)] + [C.c_void_p] * 7
+    L.zero_adamw_cast_gather.restype = C.c_int
+    return L
+
+
+def test_adamw_wait_runs_out_reports_error_and_gpu_stays_usable(hooked):
+    # every block owns at least 3 chunks of 4096 elements
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    wl = W.scaled(W.C2, sms * 4096 * 3 + 123, steps=1)
+    gpu = GpuRun(wl, guarded=False)
+    gpu.gen_grads(1)
+    dt = z.ZERO_BF16
+    z.zero_reduce_shard_unscale(gpu.lay, dt, gpu.reps, 0, gpu.lay.psi_padded, gpu.g, gpu.partials,
+                                gpu.st)
+    z.zero_grad_norm(gpu.lay, gpu.hp, gpu.partials, gpu.st)
+    assert gpu.state().error == 0
+    assert hooked.zero_test_withhold_adamw_chunk(sms + 5) == 0  # block 5's second chunk
+    t0 = time.time()
+    rc = hooked.zero_adamw_cast_gather(C.byref(gpu.lay), C.byref(gpu.hp), gpu.g.data_ptr(),
+                                       gpu.master.data_ptr(), gpu.m.data_ptr(), gpu.v.data_ptr(),
+                                       gpu.out.data_ptr(), gpu.st.data_ptr(),
+                                       torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()  # completes: the wait gave up, no fault
+    waited = time.time() - t0
+    assert hooked.zero_test_withhold_adamw_chunk(~0 & 0xFFFFFFFFFFFFFFFF) == 0
+    s = gpu.state()
+    assert s.error == 1, s.error
+    assert 1.0 < waited < 60.0, waited
+    # the context is still good: a full step through the product library matches the oracle
+    wl2 = W.scaled(W.C2, 300_007, steps=1)
+    fresh = GpuRun(wl2)
+    orc = OracleRun(wl2)
+    st = fresh.step(1)
+    rep = orc.step(1)
+    assert st.error == 0
+    assert_scalars(st, rep)
+    assert_state_close(fresh.arrays(), orc.arrays(), wl2.psi, exact_expected=st.clip_coef == rep.clip_coef)
+    fresh.check_guards()

@@ -77,6 +77,12 @@ __device__ __forceinline__ uint32_t wait_parity_bounded(uint32_t bar, uint32_t p
     }
 }
 
+#ifdef ZERO_TEST_HOOKS
+/* Test builds only (never the product library): the bounded-wait test names one chunk
+ * whose copies are withheld, so that chunk's mbarrier wait runs out without any fault. */
+__device__ unsigned long long zero_test_withheld_chunk = ~0ull;
+#endif
+
 constexpr int kChunk = 4096;  // elements per bulk-copied chunk of each array
 constexpr int kStages = 3;
 constexpr size_t kSmemBytes = (size_t)kStages * 4 * kChunk * sizeof(float);  // 192 KiB
@@ -123,6 +129,10 @@ __global__ void __launch_bounds__(kBlock, 1) k_adamw(const __grid_constant__ Ada
         const uint32_t bar = smem_addr(&full[k]);
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
                      ::"r"(bar), "r"((uint32_t)(4 * kChunk * sizeof(float))) : "memory");
+#ifdef ZERO_TEST_HOOKS
+        if (base / kChunk == zero_test_withheld_chunk)
+            return;  // test builds only: this chunk's barrier never completes
+#endif
         for (int q = 0; q < 4; ++q)
             asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
                          "[%0], [%1], %2, [%3];"
@@ -188,6 +198,13 @@ __global__ void __launch_bounds__(kBlock, 1) k_adamw(const __grid_constant__ Ada
 }
 
 }  // namespace
+
+#ifdef ZERO_TEST_HOOKS
+extern "C" int zero_test_withhold_adamw_chunk(unsigned long long chunk)
+{
+    return cudaMemcpyToSymbol(zero_test_withheld_chunk, &chunk, sizeof chunk) == cudaSuccess ? 0 : -4;
+}
+#endif
 
 cudaError_t launch_adamw(const AdamwArgs& a, cudaStream_t s)
 {
