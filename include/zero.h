@@ -92,6 +92,9 @@ typedef struct zero_adamw_hparams {
     float eps;              /* > 0 */
     float weight_decay;     /* decoupled: p *= 1 - lr*weight_decay */
     float max_grad_norm;    /* global-norm clip threshold; <= 0 disables clipping */
+    uint32_t params_dtype;  /* gathered parameters: 0 or ZERO_BF16 = bf16 (the default);
+                               ZERO_F16 = fp16, the FP16 replicated parameters of
+                               "【论文解读】ZeRO" sec. 4(1) */
 } zero_adamw_hparams_t;
 
 /* Scalar step state.  Lives in DEVICE memory (caller allocates sizeof(zero_step_state_t)
@@ -207,7 +210,8 @@ int zero_grad_norm(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,
                    double* partials, zero_step_state_t* st, zero_stream_t stream);
 
 /* -------------------------------------------------------------------------------------
- * zero_adamw_cast_gather -- fused AdamW on every shard plus the bf16 gathered write.
+ * zero_adamw_cast_gather -- fused AdamW on every shard plus the gathered write (bf16, or
+ * fp16 when hp->params_dtype == ZERO_F16).
  * [ZW] sec. 6(2): each rank updates its own parameters from its own reduced gradient and
  * the all-gather rebuilds [p0' ... p7'] in order; [ZS]: AdamW, bf16 weights.
  * Does nothing (on the device) when st->skip.  Otherwise, per flat i < psi, in fp32:
@@ -215,7 +219,7 @@ int zero_grad_norm(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,
  *   p  = p*decay - step_size * (m / (sqrt(v)/rbc2 + eps));  params[i] = bf16_rne(p)
  * and params[i] = 0 for padding (master/m/v there untouched).
  *   g, master, m, v   DEVICE fp32, psi_padded elements each (master/m/v updated in place)
- *   params            DEVICE bf16 bit patterns (uint16), psi_padded elements
+ *   params            DEVICE bf16 (or fp16) bit patterns (uint16), psi_padded elements
  *   hp                must equal the hp given to zero_grad_norm for this step
  * ------------------------------------------------------------------------------------- */
 int zero_adamw_cast_gather(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,

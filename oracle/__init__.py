@@ -45,7 +45,8 @@ class Layout(C.Structure):
 
 class HParams(C.Structure):
     _fields_ = [("lr", C.c_float), ("beta1", C.c_float), ("beta2", C.c_float),
-                ("eps", C.c_float), ("weight_decay", C.c_float), ("max_grad_norm", C.c_float)]
+                ("eps", C.c_float), ("weight_decay", C.c_float), ("max_grad_norm", C.c_float),
+                ("params_dtype", C.c_uint32)]
 
 
 class Scaler(C.Structure):
@@ -80,6 +81,8 @@ class Oracle:
         L.oracle_bf16_to_f32.restype = C.c_float
         L.oracle_f32_to_bf16.argtypes = [C.c_float]
         L.oracle_f32_to_bf16.restype = C.c_uint16
+        L.oracle_f32_to_f16.argtypes = [C.c_float]
+        L.oracle_f32_to_f16.restype = C.c_uint16
         L.oracle_partition.argtypes = [C.c_uint64, C.c_uint64, C.c_uint32, C.c_uint64,
                                        C.c_uint64, C.POINTER(Layout)]
         L.oracle_partition.restype = C.c_int
@@ -119,6 +122,9 @@ class Oracle:
 
     def f32_to_bf16(self, x: float) -> int:
         return self.lib.oracle_f32_to_bf16(x)
+
+    def f32_to_f16(self, x: float) -> int:
+        return self.lib.oracle_f32_to_f16(x)
 
     # -- layout ----------------------------------------------------------------------------
     def partition(self, psi, n_ranks, stage=2, align=1, bucket_elems=0) -> Layout:
@@ -205,8 +211,9 @@ def load(path: str | None = None) -> Oracle:
     return _cache[path]
 
 
-def hparams(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, max_grad_norm=1.0):
-    return HParams(lr, beta1, beta2, eps, weight_decay, max_grad_norm)
+def hparams(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, max_grad_norm=1.0,
+            params_dtype=0):
+    return HParams(lr, beta1, beta2, eps, weight_decay, max_grad_norm, params_dtype)
 
 
 def scaler(loss_scale=1.0, dynamic=False, growth_interval=1000, t=0):

@@ -90,6 +90,41 @@ uint16_t oracle_f32_to_bf16(float x)
     return (uint16_t)kept;
 }
 
+/* IEEE binary16 from binary32, round to nearest, ties to even.  Magnitudes from 65520
+ * (halfway between the largest finite binary16, 65504, and 2^16) up round to inf; below
+ * 2^-14 the result is a multiple of 2^-24 (subnormal); NaN stays a quiet NaN. */
+uint16_t oracle_f32_to_f16(float x)
+{
+    uint32_t u;
+    memcpy(&u, &x, sizeof u);
+    uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+    if (isnan(x))
+        return (uint16_t)(sign | 0x7e00u);
+    float a = fabsf(x);
+    if (a >= 65520.0f)
+        return (uint16_t)(sign | 0x7c00u);
+    /* scale so that one unit in the last binary16 place becomes 1, round the scaled value
+     * to an integer with ties to even, and rebuild the bits from exponent and fraction */
+    int e;
+    frexpf(a, &e);                 /* a = f * 2^e, f in [0.5, 1) (a > 0) */
+    int exp16 = e - 1;             /* a in [2^exp16, 2^(exp16+1)) */
+    if (a == 0.0f || exp16 < -14)
+        exp16 = -14;               /* subnormal range: the unit is 2^-24 */
+    float unit = ldexpf(1.0f, exp16 - 10);
+    float q = a / unit;            /* exact: a power-of-two scaling */
+    float r = nearbyintf(q);       /* round-half-even in the default rounding mode */
+    uint32_t mant = (uint32_t)r;   /* up to 2048 when rounding carries into the next binade */
+    if (mant == 0)
+        return sign;
+    if (exp16 == -14 && mant < 1024)
+        return (uint16_t)(sign | mant);                      /* subnormal */
+    if (mant == 2048) {
+        mant = 1024;
+        exp16 += 1;
+    }
+    return (uint16_t)(sign | (uint32_t)(exp16 + 15) << 10 | (mant - 1024));
+}
+
 static float replica_value(int dtype, uint16_t bits)
 {
     return dtype == ORACLE_F16 ? oracle_f16_to_f32(bits) : oracle_bf16_to_f32(bits);
@@ -269,7 +304,8 @@ void oracle_adamw_scalars(const oracle_hparams_t* hp, uint32_t t, float* step_si
  * with bias correction and decoupled weight decay, one element at a time in fp32:
  *   gc = c*g;  m = b1*m + (1-b1)*gc;  v = b2*v + (1-b2)*(gc*gc)
  *   p  = p*(1 - lr*wd) - step_size * (m / (sqrt(v)/rbc2 + eps))
- * and the fp32 master is cast to bf16 with round-to-nearest-even. */
+ * and the fp32 master is cast to bf16 with round-to-nearest-even (or, as a variant, to
+ * fp16: [ZW] sec. 4(1) keeps the replicated parameters in FP16). */
 static uint16_t adamw_one(const oracle_hparams_t* hp, float c, float step_size, float rbc2,
                           float decay, float g, float* p, float* m, float* v)
 {
@@ -285,7 +321,7 @@ static uint16_t adamw_one(const oracle_hparams_t* hp, float c, float step_size, 
     *m = m_new;
     *v = v_new;
     *p = p_new;
-    return oracle_f32_to_bf16(p_new);
+    return hp->params_dtype == ORACLE_F16 ? oracle_f32_to_f16(p_new) : oracle_f32_to_bf16(p_new);
 }
 
 void oracle_adamw_elements(const oracle_hparams_t* hp, float clip_coef, uint32_t t, uint64_t n,

@@ -49,6 +49,7 @@ typedef struct oracle_layout {
 
 typedef struct oracle_hparams {
     float lr, beta1, beta2, eps, weight_decay, max_grad_norm;
+    uint32_t params_dtype;     /* gathered parameters: 0 or ORACLE_BF16 = bf16, ORACLE_F16 = fp16 */
 } oracle_hparams_t;
 
 /* Loss scaler and step counter. */
@@ -77,6 +78,7 @@ typedef struct oracle_report {
 float oracle_f16_to_f32(uint16_t h);
 float oracle_bf16_to_f32(uint16_t b);
 uint16_t oracle_f32_to_bf16(float x);
+uint16_t oracle_f32_to_f16(float x);
 
 /* layout and ledger; returns 0 or -1 on invalid arguments */
 int oracle_partition(uint64_t psi, uint64_t n_ranks, uint32_t stage, uint64_t align,
@@ -107,7 +109,8 @@ int oracle_scaler_update(oracle_scaler_t* s, uint32_t overflow);
 void oracle_adamw_scalars(const oracle_hparams_t* hp, uint32_t t, float* step_size,
                           float* rbc2, float* decay);
 
-/* AdamW on n independent elements (no padding rule); writes bf16 bit patterns to out. */
+/* AdamW on n independent elements (no padding rule); writes the gathered parameters'
+ * bit patterns (bf16, or fp16 when hp->params_dtype == ORACLE_F16) to out. */
 void oracle_adamw_elements(const oracle_hparams_t* hp, float clip_coef, uint32_t t, uint64_t n,
                            const float* g, float* master, float* m, float* v, uint16_t* out);
 

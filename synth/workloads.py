@@ -36,6 +36,7 @@ class HP:
     eps: float = 1e-8
     weight_decay: float = 0.01
     max_grad_norm: float = 1.0
+    params_dtype: int = 0           # gathered parameters: 0 = bf16, 1 = fp16
 
 
 @dataclass(frozen=True)

@@ -72,6 +72,24 @@ def pin_bf16_encode_vs_torch(orc):
         assert (r & 0x7f80) == 0x7f80 and (r & 0x7f) != 0 and (r >> 15) == (b >> 31)
 
 
+def pin_f16_encode_vs_numpy(orc):
+    rng = np.random.default_rng(2)
+    u = rng.integers(0, 2 ** 32, size=30000, dtype=np.uint64).astype(np.uint32)
+    mags = (np.sign(rng.uniform(-1, 1, 30000)) * 2.0 ** rng.uniform(-30, 17, 30000)).astype(np.float32)
+    h16 = rng.integers(0, 0x7BFF, 6000).astype(np.uint16).view(np.float16)
+    ties = ((h16.astype(np.float64) + np.nextafter(h16, np.float16(np.inf)).astype(np.float64)) / 2)
+    edge = np.array([65504, 65519.99, 65520, 65536, 2 ** -24, 2 ** -25, 3 * 2 ** -26, 2 ** -14,
+                     2 ** -14 * (1 - 2 ** -11), 0.0, -0.0, np.inf, -np.inf, 1.0, -2.5], np.float32)
+    x = np.concatenate([u.view(np.float32), mags, ties.astype(np.float32), edge, -edge])
+    x = x[~np.isnan(x)]
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)  # numpy: IEEE round-to-nearest-even
+    got = np.array([orc.f32_to_f16(float(v)) for v in x], dtype=np.uint16)
+    assert np.array_equal(got, ref), np.flatnonzero(got != ref)[:5]
+    r = orc.f32_to_f16(float("nan"))
+    assert (r & 0x7c00) == 0x7c00 and (r & 0x3ff) != 0
+
+
 # ------------------------------------------------------------------------------------------
 # partition, ledger, communication
 # ------------------------------------------------------------------------------------------
@@ -509,6 +527,19 @@ def pin_adamw_bf16_output(orc):
     orc.adamw_elements(hp, 1.0, 1, g, p, np.zeros(n, np.float32), np.zeros(n, np.float32), out)
     ref = torch.from_numpy(p.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(out, ref)
+
+
+def pin_adamw_f16_output(orc):
+    """The fp16 gathered-parameter variant writes numpy's binary16 of the fp32 master."""
+    import oracle
+    rng = np.random.default_rng(21)
+    n = 3000
+    hp = oracle.hparams(params_dtype=F16)
+    p = rng.normal(0, 0.02, n).astype(np.float32)
+    g = rng.normal(0, 1e-3, n).astype(np.float32)
+    out = np.zeros(n, np.uint16)
+    orc.adamw_elements(hp, 1.0, 1, g, p, np.zeros(n, np.float32), np.zeros(n, np.float32), out)
+    assert np.array_equal(out, p.astype(np.float16).view(np.uint16))
 
 
 def pin_adamw_shard_pads(orc):

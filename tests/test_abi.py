@@ -130,7 +130,8 @@ def test_norm_adamw_step_rejections(lib):
     lay = z.zero_partition(1000, 4)
     hp = z.hparams()
     bad_hps = [z.hparams(beta1=1.0), z.hparams(beta2=-0.1), z.hparams(eps=0.0),
-               z.hparams(lr=float("nan")), z.hparams(lr=-1.0), z.hparams(weight_decay=float("inf"))]
+               z.hparams(lr=float("nan")), z.hparams(lr=-1.0), z.hparams(weight_decay=float("inf")),
+               z.hparams(params_dtype=3)]
     for b in bad_hps:
         assert lib.zero_grad_norm(C.byref(lay), C.byref(b), A, A, None) == z.ZERO_EINVAL
         assert lib.zero_adamw_cast_gather(C.byref(lay), C.byref(b), A, A, A, A, A, A, None) == z.ZERO_EINVAL

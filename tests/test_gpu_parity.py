@@ -61,6 +61,14 @@ def test_tiny_and_ragged(n):
         _run_pair(wl, 2)
 
 
+@pytest.mark.parametrize("recipe", ["C1", "C2"])
+def test_fp16_gathered_parameters(recipe):
+    """The fp16 variant of the gathered parameters (the FP16 replicated parameters of the
+    ZeRO walkthrough's stage 1), for fp16 and bf16 gradients."""
+    base = getattr(W, recipe)
+    _run_pair(replace(W.scaled(base, 300_007, steps=2), hp=W.HP(params_dtype=z.ZERO_F16)), 2)
+
+
 def test_tiles_shards_windows_bucketed_equals_whole():
     """Bucketed windows (tile pieces reduced in several launches) give the same bits."""
     psi = 4 * 3 * 8192 + 12345

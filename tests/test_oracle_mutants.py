@@ -20,6 +20,9 @@ MUTANTS = [
     ("bf16 ties away from zero", "if (low > 0x8000u || (low == 0x8000u && (kept & 1u)))",
      "if (low >= 0x8000u)"),
     ("bf16 decode shift", "uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b << 15;"),
+    ("f16 ties away", "float r = nearbyintf(q);", "float r = roundf(q);"),
+    ("f16 unit", "float unit = ldexpf(1.0f, exp16 - 10);", "float unit = ldexpf(1.0f, exp16 - 9);"),
+    ("f16 subnormal threshold", "if (a == 0.0f || exp16 < -14)", "if (a == 0.0f || exp16 < -15)"),
     # partition / ledger / communication
     ("shard floor", "uint64_t S = (psi + n_ranks - 1) / n_ranks;", "uint64_t S = psi / n_ranks + 1;"),
     ("align ignored", "S = (S + align - 1) / align * align;", "S = S;"),

@@ -43,7 +43,8 @@ class Layout(C.Structure):
 
 class HParams(C.Structure):
     _fields_ = [("lr", C.c_float), ("beta1", C.c_float), ("beta2", C.c_float), ("eps", C.c_float),
-                ("weight_decay", C.c_float), ("max_grad_norm", C.c_float)]
+                ("weight_decay", C.c_float), ("max_grad_norm", C.c_float),
+                ("params_dtype", C.c_uint32)]
 
 
 class StepState(C.Structure):
@@ -134,8 +135,9 @@ def _ptr_array(xs: Sequence) -> C.Array:
 
 
 def hparams(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01,
-            max_grad_norm=1.0) -> HParams:
-    return HParams(lr, beta1, beta2, eps, weight_decay, max_grad_norm)
+            max_grad_norm=1.0, params_dtype=0) -> HParams:
+    """params_dtype: 0 or ZERO_BF16 for bf16 gathered parameters, ZERO_F16 for fp16."""
+    return HParams(lr, beta1, beta2, eps, weight_decay, max_grad_norm, params_dtype)
 
 
 # --------------------------------------------------------------------------------------

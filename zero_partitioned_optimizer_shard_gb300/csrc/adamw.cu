@@ -14,7 +14,8 @@
  *   gc = c*g;  m = b1*m + (1-b1)*gc;  v = b2*v + (1-b2)*(gc*gc)
  *   p  = p*decay - step_size * (m / (sqrt(v)/rbc2 + eps));  out = bf16_rne(p)
  * c, step_size, rbc2 and decay come from the step state written by the norm kernel; a
- * skipped step (overflow) leaves every byte untouched.
+ * skipped step (overflow) leaves every byte untouched.  The gathered parameters are bf16,
+ * or fp16 when asked (the FP16 replicated parameters of "【论文解读】ZeRO" sec. 4(1)).
  *
  * GB300 design: HBM streaming, 16 bytes read and 14 written per element.  The inputs
  * are staged by the Blackwell bulk-copy engine: one thread per block issues
@@ -30,6 +31,7 @@
 #include "zero_internal.h"
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace zero {
 namespace {
@@ -50,10 +52,22 @@ __device__ __forceinline__ float adamw_one(float g, float& p, float& m, float& v
     return p;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+/* Two gathered parameters, rounded to nearest even, in one 32-bit word (lo first). */
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi)
 {
+    if (F16) {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
     const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <bool F16>
+__device__ __forceinline__ uint16_t pack1(float x)
+{
+    return F16 ? __half_as_ushort(__float2half_rn(x)) : __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p)
@@ -87,6 +101,7 @@ constexpr int kChunk = 4096;  // elements per bulk-copied chunk of each array
 constexpr int kStages = 3;
 constexpr size_t kSmemBytes = (size_t)kStages * 4 * kChunk * sizeof(float);  // 192 KiB
 
+template <bool F16>
 __global__ void __launch_bounds__(kBlock, 1) k_adamw(const __grid_constant__ AdamwArgs a)
 {
     extern __shared__ __align__(128) float ring[];  // kStages x {g, master, m, v} x kChunk
@@ -168,8 +183,8 @@ __global__ void __launch_bounds__(kBlock, 1) k_adamw(const __grid_constant__ Ada
             float4 m0 = *reinterpret_cast<const float4*>(sm + e);
             float4 v0 = *reinterpret_cast<const float4*>(sv + e);
             uint2 o;
-            o.x = pack_bf16x2(adamw_one(g0.x, p0.x, m0.x, v0.x, s), adamw_one(g0.y, p0.y, m0.y, v0.y, s));
-            o.y = pack_bf16x2(adamw_one(g0.z, p0.z, m0.z, v0.z, s), adamw_one(g0.w, p0.w, m0.w, v0.w, s));
+            o.x = pack2<F16>(adamw_one(g0.x, p0.x, m0.x, v0.x, s), adamw_one(g0.y, p0.y, m0.y, v0.y, s));
+            o.y = pack2<F16>(adamw_one(g0.z, p0.z, m0.z, v0.z, s), adamw_one(g0.w, p0.w, m0.w, v0.w, s));
             __stcs(reinterpret_cast<float4*>(a.master + base + e), p0);
             __stcs(reinterpret_cast<float4*>(a.m + base + e), m0);
             __stcs(reinterpret_cast<float4*>(a.v + base + e), v0);
@@ -190,7 +205,7 @@ __global__ void __launch_bounds__(kBlock, 1) k_adamw(const __grid_constant__ Ada
             a.master[i] = p;
             a.m[i] = m;
             a.v[i] = v;
-            a.out[i] = __bfloat16_as_ushort(__float2bfloat16_rn(r));
+            a.out[i] = pack1<F16>(r);
         } else {
             a.out[i] = 0;  // padding: gathered value 0, state untouched
         }
@@ -212,10 +227,12 @@ cudaError_t launch_adamw(const AdamwArgs& a, cudaStream_t s)
     int dev = 0;
     cudaGetDevice(&dev);
     if (!configured[dev & 63]) {
-        cudaError_t e = cudaFuncSetAttribute(k_adamw, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
-        if (e != cudaSuccess)
-            return e;
+        for (auto kern : {k_adamw<false>, k_adamw<true>}) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)kSmemBytes);
+            if (e != cudaSuccess)
+                return e;
+        }
         configured[dev & 63] = true;
     }
     const uint64_t chunks = a.psi / kChunk;
@@ -223,7 +240,10 @@ cudaError_t launch_adamw(const AdamwArgs& a, cudaStream_t s)
     const uint64_t want = chunks > tail_blocks ? chunks : tail_blocks;
     const uint64_t cap = (uint64_t)sm_count();  // one 192 KiB block per SM
     const unsigned grid = (unsigned)(want < cap ? want : cap);
-    k_adamw<<<grid > 0 ? grid : 1, kBlock, kSmemBytes, s>>>(a);
+    if (a.out_f16)
+        k_adamw<true><<<grid > 0 ? grid : 1, kBlock, kSmemBytes, s>>>(a);
+    else
+        k_adamw<false><<<grid > 0 ? grid : 1, kBlock, kSmemBytes, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -58,7 +58,8 @@ bool hparams_ok(const zero_adamw_hparams_t* hp)
         if (!(x == x) || x > 3.0e38f || x < -3.0e38f)
             return false;
     return hp->beta1 >= 0.0f && hp->beta1 < 1.0f && hp->beta2 >= 0.0f && hp->beta2 < 1.0f &&
-           hp->eps > 0.0f && hp->lr >= 0.0f;
+           hp->eps > 0.0f && hp->lr >= 0.0f &&
+           (hp->params_dtype == 0 || hp->params_dtype == ZERO_BF16 || hp->params_dtype == ZERO_F16);
 }
 
 int reduce_window(const zero_layout_t* L, zero_dtype_t dtype, const void* const* replicas,
@@ -149,6 +150,7 @@ int adamw(const zero_layout_t* L, const zero_adamw_hparams_t* hp, const float* g
     a.beta1 = hp->beta1;
     a.beta2 = hp->beta2;
     a.eps = hp->eps;
+    a.out_f16 = hp->params_dtype == ZERO_F16 ? 1u : 0u;
     return cuda_status(launch_adamw(a, stream));
 }
 

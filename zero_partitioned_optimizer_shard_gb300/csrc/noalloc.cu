@@ -62,7 +62,8 @@ bool hp_valid(const zero_adamw_hparams_t* hp)
         if (!(x == x) || x > 3.0e38f || x < -3.0e38f)
             return false;
     return hp->beta1 >= 0.0f && hp->beta1 < 1.0f && hp->beta2 >= 0.0f && hp->beta2 < 1.0f &&
-           hp->eps > 0.0f && hp->lr >= 0.0f;
+           hp->eps > 0.0f && hp->lr >= 0.0f &&
+           (hp->params_dtype == 0 || hp->params_dtype == ZERO_BF16 || hp->params_dtype == ZERO_F16);
 }
 
 /* Device address of the static array on the current device, looked up once. */
@@ -171,6 +172,7 @@ extern "C" int zero_step_static_workspace(const zero_layout_t* layout,
     u.beta1 = hp->beta1;
     u.beta2 = hp->beta2;
     u.eps = hp->eps;
+    u.out_f16 = hp->params_dtype == ZERO_F16 ? 1u : 0u;
     e = zero::launch_adamw(u, s);
     return e == cudaSuccess ? ZERO_OK : fail_cuda(e);
 }

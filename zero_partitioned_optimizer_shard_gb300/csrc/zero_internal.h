@@ -42,6 +42,7 @@ struct AdamwArgs {
     uint32_t* err;                           // the state's error word (bounded waits)
     uint64_t psi, psi_padded;
     float beta1, beta2, eps;
+    uint32_t out_f16;                        // gathered parameters as fp16 instead of bf16
 };
 
 struct InitArgs {
