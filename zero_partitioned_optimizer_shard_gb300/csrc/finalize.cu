@@ -13,6 +13,11 @@
  * (cap 2^24).  Everything stays on the device, so a training loop never waits for the
  * host between steps.
  *
+ * Block 0 starts with everything that does not need the norm (skip, t, the scaler, the
+ * bias corrections with their two fp64 pow, which GB300's slow fp64 pipe makes the
+ * longest chain), split over three warps; that overlaps the other blocks' sums.  The
+ * last block then only takes the square root and the clip coefficient.
+ *
  * The sum is spread over up to 128 blocks (GB300's fp64 rate is a few operations per SM
  * per clock, so one block summing every tile partial would take tens of microseconds).
  * Block b sums the fixed chunk b of every rank's tile partials (a fixed tree per block),
@@ -45,6 +50,51 @@ __global__ void __launch_bounds__(kFinThreads) k_finalize(const __grid_constant_
     const uint64_t j0 = (uint64_t)blockIdx.x * chunk;
     const uint64_t j1 = j0 + chunk < tpr ? j0 + chunk : tpr;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    zero_step_state_t* st = a.st;
+
+    // Block 0 first does everything that does not need the norm, in three warps at once.
+    // It depends only on the overflow flag, which every reduce window has already set;
+    // the fp64 work (two pow) overlaps the other blocks' partial sums.  Block 0's arrival
+    // below publishes it to the last block.
+    if (blockIdx.x == 0) {
+        __shared__ uint32_t s_t, s_overflow;
+        if (threadIdx.x == 0) {
+            s_t = st->t;
+            s_overflow = st->overflow != 0;
+        }
+        __syncthreads();
+        const uint32_t t = s_t + 1;  // the step count if this step is applied
+        if (lane == 0 && w == 1 && !s_overflow)
+            st->step_size = (float)((double)a.hp.lr / (1.0 - pow((double)a.hp.beta1, (double)t)));
+        if (lane == 0 && w == 2 && !s_overflow)
+            st->rbc2 = (float)sqrt(1.0 - pow((double)a.hp.beta2, (double)t));
+        if (lane == 0 && w == 3) {
+            float L = st->loss_scale;
+            if (s_overflow) {
+                st->skip = 1;
+                st->n_skipped += 1;
+                if (st->dynamic) {
+                    const float half = L * 0.5f;
+                    L = half < 1.0f ? 1.0f : half;
+                    st->good_steps = 0;
+                }
+            } else {
+                st->t = t;
+                st->skip = 0;
+                st->decay = (float)(1.0 - (double)a.hp.lr * (double)a.hp.weight_decay);
+                if (st->dynamic && st->growth_interval > 0) {
+                    st->good_steps += 1;
+                    if (st->good_steps == st->growth_interval) {
+                        const float twice = L * 2.0f;
+                        L = twice > 16777216.0f ? 16777216.0f : twice;
+                        st->good_steps = 0;
+                    }
+                }
+            }
+            st->loss_scale = L;
+            st->inv_scale = (float)(1.0 / ((double)N * (double)L));
+        }
+    }
 
     // this block's chunk of every rank, kBatch ranks at a time: each thread sums its
     // slots in order, a shuffle tree folds each warp, warps are folded in order
@@ -120,48 +170,17 @@ __global__ void __launch_bounds__(kFinThreads) k_finalize(const __grid_constant_
     for (uint32_t r = 0; r < N; ++r)
         total += rank_sum[r];
 
-    zero_step_state_t* st = a.st;
+    // the skip decision and the rest were written by block 0 before it arrived
     st->arrivals = 0;
     const double norm = sqrt(total);
-    const bool overflow = st->overflow != 0;
-    float L = st->loss_scale;
     st->sumsq = total;
     st->norm = norm;
-    if (overflow) {
-        st->skip = 1;
-        st->clip_coef = 1.0f;
-        st->n_skipped += 1;
-        if (st->dynamic) {
-            const float half = L * 0.5f;
-            L = half < 1.0f ? 1.0f : half;
-            st->good_steps = 0;
-        }
-    } else {
-        const uint32_t t = st->t + 1;
-        st->t = t;
-        st->skip = 0;
-        float c = 1.0f;
-        if (a.hp.max_grad_norm > 0.0f) {
-            const double cc = (double)a.hp.max_grad_norm / (norm + 1e-6);
-            c = cc < 1.0 ? (float)cc : 1.0f;
-        }
-        st->clip_coef = c;
-        const double bc1 = 1.0 - pow((double)a.hp.beta1, (double)t);
-        const double bc2 = 1.0 - pow((double)a.hp.beta2, (double)t);
-        st->step_size = (float)((double)a.hp.lr / bc1);
-        st->rbc2 = (float)sqrt(bc2);
-        st->decay = (float)(1.0 - (double)a.hp.lr * (double)a.hp.weight_decay);
-        if (st->dynamic && st->growth_interval > 0) {
-            st->good_steps += 1;
-            if (st->good_steps == st->growth_interval) {
-                const float twice = L * 2.0f;
-                L = twice > 16777216.0f ? 16777216.0f : twice;
-                st->good_steps = 0;
-            }
-        }
+    float c = 1.0f;
+    if (!__ldcg(&st->skip) && a.hp.max_grad_norm > 0.0f) {
+        const double cc = (double)a.hp.max_grad_norm / (norm + 1e-6);
+        c = cc < 1.0 ? (float)cc : 1.0f;
     }
-    st->loss_scale = L;
-    st->inv_scale = (float)(1.0 / ((double)N * (double)L));
+    st->clip_coef = c;
     st->overflow = 0;
     st->n_steps += 1;
 }
