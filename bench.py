@@ -584,6 +584,120 @@ def run_overlap(args):
     return 0
 
 
+def _link_bandwidth(torch, dev, nbytes=1 << 31):
+    """Copy-engine bandwidth of the CPU-GPU link, measured here: pinned host -> HBM,
+    HBM -> pinned host, and both at once on two streams (GB/s each way)."""
+    h = [torch.empty(nbytes, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
+    d = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    s = [torch.cuda.Stream(dev) for _ in range(2)]
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+
+    def one(dst, src, stream):
+        with torch.cuda.stream(stream):
+            dst.copy_(src, non_blocking=True)
+
+    best = {"h2d": 0.0, "d2h": 0.0, "both_each": 0.0}
+    for _ in range(3):
+        torch.cuda.synchronize(dev)
+        e[0].record(s[0]); one(d[0], h[0], s[0]); e[1].record(s[0])
+        torch.cuda.synchronize(dev)
+        best["h2d"] = max(best["h2d"], nbytes / e[0].elapsed_time(e[1]) / 1e6)
+        e[0].record(s[0]); one(h[1], d[1], s[0]); e[1].record(s[0])
+        torch.cuda.synchronize(dev)
+        best["d2h"] = max(best["d2h"], nbytes / e[0].elapsed_time(e[1]) / 1e6)
+        e[0].record(s[0])
+        s[1].wait_event(e[0])
+        one(d[0], h[0], s[0])
+        one(h[1], d[1], s[1])
+        e[1].record(s[0]); e[2].record(s[1])
+        torch.cuda.synchronize(dev)
+        ms = max(e[0].elapsed_time(e[1]), e[0].elapsed_time(e[2]))
+        best["both_each"] = max(best["both_each"], nbytes / ms / 1e6)
+    return best
+
+
+def run_offload(args):
+    """The GPT-2-1.5B step with the optimizer state offloaded to host memory.
+
+    master, m and v (18.7 GB) live in page-locked Grace memory; the N gradient copies,
+    g and the gathered parameters stay in HBM.  Per step: the reduce and the norm on the
+    device, then zero_adamw_cast_gather_host_state, which reads and writes the state in
+    place over NVLink-C2C (12 B per parameter each way).  Reported against the link's
+    copy bandwidth measured in the same run."""
+    import torch
+
+    import synth
+    import zero_partitioned_optimizer_shard_gb300 as z
+    from synth import workloads as W
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    link = _link_bandwidth(torch, dev)
+    wl = W.C2 if args.psi in (None, W.C2.psi) else W.scaled(W.C2, args.psi)
+    lay = z.zero_partition(wl.psi, wl.n_ranks, wl.stage)
+    P, N = lay.psi_padded, lay.n_ranks
+    hp = z.hparams(**wl.hp.__dict__)
+    stream = torch.cuda.current_stream(dev)
+    s = stream.cuda_stream
+    reps = [torch.empty(P, dtype=torch.int16, device=dev) for _ in range(N)]
+    for k, r in enumerate(reps):
+        synth.fill_dev(r.data_ptr(), wl.grad_out, wl.grad_kind, wl.grad_key(1, k), 0, P, wl.psi,
+                       wl.grad_sigma, 1.0, s)
+    g = torch.empty(P, dtype=torch.float32, device=dev)
+    host = {}
+    for name, role, kind, sig in (("master", synth.ROLE_MASTER, synth.NORMAL, wl.master_sigma),
+                                  ("m", synth.ROLE_MOM, synth.NORMAL, wl.mom_sigma),
+                                  ("v", synth.ROLE_VAR, synth.NORMAL_SQ, wl.mom_sigma)):
+        synth.fill_dev(g.data_ptr(), synth.OUT_F32, kind, wl.state_key(role), 0, P, wl.psi, sig, 1.0, s)
+        host[name] = torch.empty(P, dtype=torch.float32, pin_memory=True)
+        host[name].copy_(g)
+    out = torch.empty(P, dtype=torch.int16, device=dev)
+    partials = torch.empty(lay.n_tiles, dtype=torch.float64, device=dev)
+    st = torch.empty(z.STATE_BYTES, dtype=torch.uint8, device=dev)
+    z.zero_step_state_init(lay, 1.0, False, 1000, st, partials, stream)
+    ptrs = [r.data_ptr() for r in reps]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps + 1)]
+
+    def step(e=None):
+        z.zero_reduce_shard_unscale(lay, z.ZERO_BF16, ptrs, 0, P, g, partials, st, stream)
+        z.zero_grad_norm(lay, hp, partials, st, stream)
+        if e:
+            e[1].record(stream)
+        z.zero_adamw_cast_gather_host_state(lay, hp, g, host["master"], host["m"], host["v"], out,
+                                            st, stream)
+        if e:
+            e[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(0)
+    clocks.start()
+    clocks.mark(True)
+    ev[0][2].record(stream)
+    for i in range(args.steps):
+        step(ev[i + 1])
+    torch.cuda.synchronize(dev)
+    clocks.mark(False)
+    clk = clocks.stop()
+    total = ev[0][2].elapsed_time(ev[args.steps][2])
+    adamw = [ev[i + 1][1].elapsed_time(ev[i + 1][2]) for i in range(args.steps)]
+    stt = z.zero_step_state_read(st, stream)
+    assert stt.t == args.warmup + args.steps and stt.skip == 0 and stt.error == 0
+    a_ms = statistics.mean(adamw)
+    link_gbs_each = 12 * P / (a_ms / 1e3) / 1e9
+    line = {"offload": True, "workload": wl.name, "psi": wl.psi, "n_ranks": N,
+            "state_in_host_memory_gb": 12 * P / 1e9, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total / args.steps, "params_per_s": wl.psi / (total / args.steps / 1e3),
+            "ms_adamw_host_state": a_ms,
+            "link_gbs_each_way": link_gbs_each,
+            "link_copy_peak_gbs": link,
+            "frac_of_copy_both_ways": link_gbs_each / link["both_each"],
+            "clocks": clk}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -602,6 +716,9 @@ def main():
     ap.add_argument("--overlap", action="store_true",
                     help="bucket arrival overlapped with a synthetic backward producer "
                          "(Llama-7B buffer, 2^27-element buckets)")
+    ap.add_argument("--offload", action="store_true",
+                    help="optimizer state (master/m/v) in pinned host memory, updated over "
+                         "the CPU-GPU link")
     ap.add_argument("--sweep-n", default="2,4,8,16,64")
     ap.add_argument("--psi", type=int, default=None,
                     help="profiling only: the same recipe at another size (default: the "
@@ -623,6 +740,8 @@ def main():
         return run_sweep(args)
     if args.overlap:
         return run_overlap(args)
+    if args.offload:
+        return run_offload(args)
     return run_ours(args)
 
 

@@ -141,6 +141,34 @@ typedef struct zero_step_state {
 int zero_partition(uint64_t psi, uint32_t n_ranks, uint32_t stage, uint32_t align,
                    uint64_t bucket_elems, zero_layout_t* out);
 
+/* One piece of a model tensor inside one rank's shard. */
+typedef struct zero_segment {
+    uint64_t tensor;         /* index in the caller's tensor list */
+    uint64_t rank;           /* owner of the piece */
+    uint64_t tensor_offset;  /* first element of the piece within the tensor */
+    uint64_t shard_offset;   /* the same element's position in the owner's shard
+                                (flat index - rank*S) */
+    uint64_t count;          /* elements in the piece (>= 1) */
+} zero_segment_t;            /* 40 bytes */
+
+/* -------------------------------------------------------------------------------------
+ * zero_segment_map -- host only, no CUDA call.
+ * [ZW] sec. 4(2): gradients are bucketed by partition and reduced at the partition
+ * boundary, so a tensor that crosses a shard boundary belongs to two or more ranks.
+ * The model's tensors are laid end to end over the flat buffer [0, psi) in list order;
+ * this lists each tensor's piece on each rank, in flat order (so by rank, then tensor).
+ * Empty tensors have no piece; padding [psi, psi_padded) belongs to no tensor.
+ *   tensor_elems   HOST array of n_tensors element counts; they must sum to layout->psi
+ *   out            HOST array of `capacity` pieces, or NULL to only count them
+ *   n_segments     HOST, receives the number of pieces (always, on ZERO_OK or ZERO_ENOMEM)
+ * Returns ZERO_OK; ZERO_EINVAL (bad layout or pointers, sizes not summing to psi);
+ * ZERO_ENOMEM when capacity is too small (out untouched).  There are
+ * (non-empty tensors) + (shard boundaries strictly inside a tensor) pieces.
+ * ------------------------------------------------------------------------------------- */
+int zero_segment_map(const zero_layout_t* layout, const uint64_t* tensor_elems,
+                     uint64_t n_tensors, zero_segment_t* out, uint64_t capacity,
+                     uint64_t* n_segments);
+
 /* Bytes of the fp64 partials workspace the device entry points need:
  * layout->n_tiles * 8.  0 for an invalid layout. */
 size_t zero_workspace_bytes(const zero_layout_t* layout);
@@ -204,7 +232,8 @@ int zero_reduce_shard_unscale(const zero_layout_t* layout, zero_dtype_t dtype,
  *   else:     skip = 0, t += 1, step_size = f32(lr/(1-beta1^t)), rbc2 = f32(sqrt(1-beta2^t)),
  *             decay = f32(1 - lr*wd); dynamic L doubles after growth_interval good steps
  *   inv_scale = f32(1/(N*L)) for the next step; overflow flag and partials reset to 0.
- * One single-block kernel; no host synchronisation.
+ * One kernel (the partial sums spread over up to 128 blocks, the last block to finish
+ * forms the norm); no host synchronisation.
  * ------------------------------------------------------------------------------------- */
 int zero_grad_norm(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,
                    double* partials, zero_step_state_t* st, zero_stream_t stream);
@@ -225,6 +254,26 @@ int zero_grad_norm(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,
 int zero_adamw_cast_gather(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,
                            const float* g, float* master, float* m, float* v, uint16_t* params,
                            const zero_step_state_t* st, zero_stream_t stream);
+
+/* -------------------------------------------------------------------------------------
+ * zero_adamw_cast_gather_host_state -- zero_adamw_cast_gather with the optimizer state
+ * (master, m, v) resident in HOST memory.
+ * [ZM] sec. 6: when device memory is short the optimizer state can be offloaded to the
+ * CPU, at a transfer cost that has to be measured on the machine.  Here the state stays
+ * in the host memory of the Grace CPU and the kernel reads and writes it in place over
+ * the CPU-GPU link (NVLink-C2C on GB300) while g is read from, and the gathered
+ * parameters written to, device memory; 12 B per element cross the link each way.
+ * Same update, same bits as zero_adamw_cast_gather.
+ *   master, m, v   HOST fp32, psi_padded elements each, PAGE-LOCKED (cudaHostAlloc /
+ *                  cudaMallocHost / cudaHostRegister, e.g. torch pin_memory); updated in
+ *                  place.  Pageable or device memory is refused with ZERO_EINVAL.  The
+ *                  host must not touch them until the stream has passed this call.
+ *   g, params, st  DEVICE, as in zero_adamw_cast_gather
+ * ------------------------------------------------------------------------------------- */
+int zero_adamw_cast_gather_host_state(const zero_layout_t* layout,
+                                      const zero_adamw_hparams_t* hp, const float* g,
+                                      float* master, float* m, float* v, uint16_t* params,
+                                      const zero_step_state_t* st, zero_stream_t stream);
 
 /* -------------------------------------------------------------------------------------
  * zero_step -- one whole step: every bucket's reduce, the norm, AdamW + cast.

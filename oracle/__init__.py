@@ -112,6 +112,8 @@ class Oracle:
         L.oracle_step_unsharded.argtypes = [C.c_uint64, C.POINTER(HParams), _P, _P, _P, _P, _P,
                                             C.POINTER(Scaler), C.POINTER(Report)]
         L.oracle_step_unsharded.restype = C.c_int
+        L.oracle_segment_map.argtypes = [C.POINTER(Layout), _P, C.c_uint64, _P, C.c_uint64]
+        L.oracle_segment_map.restype = C.c_int64
 
     # -- number formats ------------------------------------------------------------------
     def f16_to_f32(self, bits: int) -> float:
@@ -198,6 +200,19 @@ class Oracle:
         self.lib.oracle_step_unsharded(g_mean.size, C.byref(hp), _ptr(g_mean), _ptr(master),
                                        _ptr(m), _ptr(v), _ptr(out), C.byref(sc), C.byref(rep))
         return rep
+
+    # -- per-tensor segment map -------------------------------------------------------------
+    def segment_map(self, lay, tensor_elems) -> np.ndarray:
+        """Rows (tensor, rank, tensor_offset, shard_offset, count), in flat order."""
+        sizes = np.ascontiguousarray(tensor_elems, dtype=np.uint64)
+        n = self.lib.oracle_segment_map(C.byref(lay), _ptr(sizes) if sizes.size else None,
+                                        sizes.size, None, 0)
+        if n < 0:
+            raise ValueError("tensor sizes do not sum to psi")
+        out = np.zeros((max(n, 1), 5), dtype=np.uint64)
+        self.lib.oracle_segment_map(C.byref(lay), _ptr(sizes) if sizes.size else None, sizes.size,
+                                    _ptr(out), n)
+        return out[:n]
 
 
 _cache: dict[str, Oracle] = {}

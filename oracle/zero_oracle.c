@@ -443,3 +443,46 @@ int oracle_step_unsharded(uint64_t psi, const oracle_hparams_t* hp, const float*
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------------------ */
+/* Per-tensor segment map.                                                               */
+/* [ZW] sec. 4(2): gradients are bucketed by partition and each bucket is reduced at the */
+/* partition boundary, so a tensor that crosses a boundary is split between two owners. */
+/* Brute force, one flat element at a time.                                              */
+/* ------------------------------------------------------------------------------------ */
+
+int64_t oracle_segment_map(const oracle_layout_t* lay, const uint64_t* tensor_elems,
+                           uint64_t n_tensors, oracle_segment_t* out, uint64_t capacity)
+{
+    uint64_t total = 0;
+    for (uint64_t k = 0; k < n_tensors; ++k)
+        total += tensor_elems[k];
+    if (total != lay->psi)
+        return -1;
+    int64_t n = 0;
+    uint64_t k = 0, start_of_k = 0;   /* tensor k covers flat [start_of_k, start_of_k + size) */
+    uint64_t cur_tensor = UINT64_MAX, cur_rank = UINT64_MAX;
+    for (uint64_t i = 0; i < lay->psi; ++i) {
+        while (i >= start_of_k + tensor_elems[k]) {   /* skips empty tensors too */
+            start_of_k += tensor_elems[k];
+            ++k;
+        }
+        uint64_t r = i / lay->shard;
+        if (k != cur_tensor || r != cur_rank) {
+            cur_tensor = k;
+            cur_rank = r;
+            if ((uint64_t)n < capacity) {
+                out[n].tensor = k;
+                out[n].rank = r;
+                out[n].tensor_offset = i - start_of_k;
+                out[n].shard_offset = i - r * lay->shard;
+                out[n].count = 0;
+            }
+            ++n;
+        }
+        if ((uint64_t)(n - 1) < capacity)
+            out[n - 1].count += 1;
+    }
+    return n;
+}
+

@@ -134,6 +134,22 @@ int oracle_step_unsharded(uint64_t psi, const oracle_hparams_t* hp, const float*
                           float* master, float* m, float* v, uint16_t* out, oracle_scaler_t* sc,
                           oracle_report_t* rep);
 
+/* One piece of a model tensor inside one rank's shard. */
+typedef struct oracle_segment {
+    uint64_t tensor;           /* index in the tensor list */
+    uint64_t rank;             /* owner of the piece */
+    uint64_t tensor_offset;    /* first element of the piece within the tensor */
+    uint64_t shard_offset;     /* the same element's position within the owner's shard */
+    uint64_t count;            /* elements in the piece */
+} oracle_segment_t;
+
+/* Tensors of the given sizes laid end to end over the flat buffer [0, psi), in list
+ * order, cut at the shard boundaries: walks every flat element and starts a new piece
+ * whenever the (tensor, rank) pair changes.  Writes at most `capacity` pieces in flat
+ * order and returns how many there are, or -1 if the sizes do not sum to psi. */
+int64_t oracle_segment_map(const oracle_layout_t* lay, const uint64_t* tensor_elems,
+                           uint64_t n_tensors, oracle_segment_t* out, uint64_t capacity);
+
 #ifdef __cplusplus
 }
 #endif

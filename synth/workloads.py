@@ -25,6 +25,42 @@ PSI_LLAMA_7B = 32 * _LAYER_LLAMA + 2 * 32000 * _D7 + _D7
 assert PSI_GPT2_1_5B == 1_557_611_200
 assert PSI_LLAMA_7B == 6_738_415_616
 
+
+
+def tensors_gpt2_1_5b() -> list[tuple[str, int]]:
+    """(name, elements) of GPT-2 1.5B's tensors in checkpoint order (the flat buffer's
+    order): token and position embeddings, 48 blocks, the final LayerNorm; the LM head is
+    tied to the token embedding."""
+    d, ff = _D2, _FF2
+    t = [("wte", 50257 * d), ("wpe", 1024 * d)]
+    for i in range(48):
+        h = f"h.{i}."
+        t += [(h + "ln_1.weight", d), (h + "ln_1.bias", d),
+              (h + "attn.c_attn.weight", d * 3 * d), (h + "attn.c_attn.bias", 3 * d),
+              (h + "attn.c_proj.weight", d * d), (h + "attn.c_proj.bias", d),
+              (h + "ln_2.weight", d), (h + "ln_2.bias", d),
+              (h + "mlp.c_fc.weight", d * ff), (h + "mlp.c_fc.bias", ff),
+              (h + "mlp.c_proj.weight", ff * d), (h + "mlp.c_proj.bias", d)]
+    return t + [("ln_f.weight", d), ("ln_f.bias", d)]
+
+
+def tensors_llama_7b() -> list[tuple[str, int]]:
+    """(name, elements) of Llama 7B's tensors in checkpoint order: embedding, 32 blocks
+    (attention q/k/v/o, MLP gate/up/down, two RMSNorm weights), final norm, untied head."""
+    d, ff = _D7, _FF7
+    t = [("embed_tokens.weight", 32000 * d)]
+    for i in range(32):
+        h = f"layers.{i}."
+        t += [(h + f"self_attn.{x}_proj.weight", d * d) for x in "qkvo"]
+        t += [(h + "mlp.gate_proj.weight", ff * d), (h + "mlp.up_proj.weight", ff * d),
+              (h + "mlp.down_proj.weight", d * ff),
+              (h + "input_layernorm.weight", d), (h + "post_attention_layernorm.weight", d)]
+    return t + [("norm.weight", d), ("lm_head.weight", 32000 * d)]
+
+
+assert sum(n for _, n in tensors_gpt2_1_5b()) == PSI_GPT2_1_5B
+assert sum(n for _, n in tensors_llama_7b()) == PSI_LLAMA_7B
+
 F16_POS_INF, F16_NAN, F16_NEG_INF = 0x7C00, 0x7E00, 0xFC00
 
 

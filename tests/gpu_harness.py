@@ -25,8 +25,11 @@ def dtype_code(wl) -> int:
 
 class GpuRun:
     def __init__(self, wl, bucket_elems: int = 0, device: str = "cuda:0", guarded: bool = True,
-                 hp=None):
+                 hp=None, host_state: bool = False):
+        """host_state: master/m/v in page-locked host memory (the offloaded optimizer
+        state), updated by zero_adamw_cast_gather_host_state."""
         self.wl = wl
+        self.host_state = host_state
         self.dev = torch.device(device)
         self.stream = torch.cuda.current_stream(self.dev)
         self.guarded = guarded
@@ -36,9 +39,9 @@ class GpuRun:
         self.hp = hp if hp is not None else z.hparams(**wl.hp.__dict__)
         self.reps = [self.alloc(P, torch.int16) for _ in range(wl.n_ranks)]
         self.g = self.alloc(P, torch.float32)
-        self.master = self.alloc(P, torch.float32)
-        self.m = self.alloc(P, torch.float32)
-        self.v = self.alloc(P, torch.float32)
+        self.master = self.alloc(P, torch.float32, host_state)
+        self.m = self.alloc(P, torch.float32, host_state)
+        self.v = self.alloc(P, torch.float32, host_state)
         self.out = self.alloc(P, torch.int16)
         self.partials = self.alloc(max(self.lay.n_tiles, 1), torch.float64)
         self.st = self.alloc(z.STATE_BYTES, torch.uint8)
@@ -55,12 +58,14 @@ class GpuRun:
         z.zero_step_state_init(self.lay, wl.loss_scale, wl.dynamic, wl.growth_interval, self.st,
                                self.partials, self.stream)
 
-    def alloc(self, n: int, dtype) -> torch.Tensor:
+    def alloc(self, n: int, dtype, pinned_host: bool = False) -> torch.Tensor:
         nbytes = n * _ESZ[dtype]
+        where = dict(device="cpu", pin_memory=True) if pinned_host else dict(device=self.dev)
         if not self.guarded:
-            return torch.empty(n, dtype=dtype, device=self.dev)
+            return torch.empty(n, dtype=dtype, **where)
         body = (nbytes + 255) // 256 * 256
-        raw = torch.full((GUARD + body + GUARD,), CANARY, dtype=torch.uint8, device=self.dev)
+        raw = torch.empty((GUARD + body + GUARD,), dtype=torch.uint8, **where)
+        raw.fill_(CANARY)
         self._raw.append((raw, nbytes))
         return raw[GUARD:GUARD + nbytes].view(dtype)
 
@@ -72,6 +77,11 @@ class GpuRun:
 
     def _fill(self, t, out, kind, key, sigma, scale=1.0, begin=0, count=None):
         count = t.numel() if count is None else count
+        if not t.is_cuda:  # host-resident state: generate on the device, then copy
+            d = torch.empty_like(t, device=self.dev)
+            self._fill(d, out, kind, key, sigma, scale, begin, count)
+            t.copy_(d)
+            return
         synth.fill_dev(t.data_ptr(), out, kind, key, begin, count, self.wl.psi, sigma, scale,
                        self.stream.cuda_stream)
 
@@ -96,14 +106,25 @@ class GpuRun:
 
     def step(self, step: int) -> z.StepState:
         self.gen_grads(step)
-        z.zero_step(self.lay, self.hp, dtype_code(self.wl), self.bucket_ptrs(), self.g,
-                    self.partials, self.master, self.m, self.v, self.out, self.st, self.stream)
+        if self.host_state:
+            W, N, P = self.lay.bucket_elems, self.lay.n_ranks, self.lay.psi_padded
+            ptrs = self.bucket_ptrs()
+            for b in range(self.lay.n_buckets):
+                z.zero_reduce_shard_unscale(self.lay, dtype_code(self.wl), ptrs[b * N:(b + 1) * N],
+                                            b * W, min(W, P - b * W), self.g, self.partials,
+                                            self.st, self.stream)
+            z.zero_grad_norm(self.lay, self.hp, self.partials, self.st, self.stream)
+            z.zero_adamw_cast_gather_host_state(self.lay, self.hp, self.g, self.master, self.m,
+                                                self.v, self.out, self.st, self.stream)
+        else:
+            z.zero_step(self.lay, self.hp, dtype_code(self.wl), self.bucket_ptrs(), self.g,
+                        self.partials, self.master, self.m, self.v, self.out, self.st, self.stream)
         return self.state()
 
     def arrays(self) -> dict:
         torch.cuda.synchronize(self.dev)
-        return dict(g=self.g.cpu().numpy(), master=self.master.cpu().numpy(),
-                    m=self.m.cpu().numpy(), v=self.v.cpu().numpy(),
+        return dict(g=self.g.cpu().numpy(), master=self.master.cpu().numpy().copy(),
+                    m=self.m.cpu().numpy().copy(), v=self.v.cpu().numpy().copy(),
                     out=self.out.cpu().numpy().view(np.uint16))
 
 

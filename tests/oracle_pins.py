@@ -697,4 +697,71 @@ def pin_step_skip_untouched(orc):
         assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
 
 
+# ------------------------------------------------------------------------------------------
+# per-tensor segment map
+# ------------------------------------------------------------------------------------------
+def _segment_cases():
+    cases, cur = [], None
+    with open(os.path.join(GOLDEN, "segment_map_examples.txt"), encoding="utf-8") as f:
+        for line in f:
+            if not line.strip() or line.startswith("#"):
+                continue
+            if line.startswith("case"):
+                psi, n, *sizes = (int(x) for x in line.split()[1:])
+                cur = (psi, n, sizes, [])
+                cases.append(cur)
+            else:
+                cur[3].append([int(x) for x in line.split()])
+    return cases
+
+
+def pin_segment_map_examples(orc):
+    """Hand-worked maps, including the 8-parameter, 4-GPU example of [ZW] sec. 6(2)."""
+    for psi, n, sizes, want in _segment_cases():
+        got = orc.segment_map(orc.partition(psi, n), sizes)
+        assert got.tolist() == want, (psi, n, sizes, got.tolist())
+
+
+def _segments_by_runs(psi, shard, sizes):
+    """The same map derived another way: label every element with (tensor, rank) using
+    numpy and cut where the label changes."""
+    tensor = np.repeat(np.arange(len(sizes)), sizes)
+    flat = np.arange(psi)
+    rank = flat // shard
+    start = np.concatenate([[0], np.cumsum(sizes)[:-1]]).astype(np.int64)
+    cut = np.flatnonzero(np.r_[True, (tensor[1:] != tensor[:-1]) | (rank[1:] != rank[:-1])])
+    ends = np.r_[cut[1:], psi]
+    return [[int(tensor[c]), int(rank[c]), int(c - start[tensor[c]]), int(c - rank[c] * shard),
+             int(e - c)] for c, e in zip(cut, ends)]
+
+
+def pin_segment_map_runs_and_count(orc):
+    rng = np.random.default_rng(11)
+    for _ in range(60):
+        n = int(rng.integers(1, 18))
+        k = int(rng.integers(1, 30))
+        sizes = [int(x) for x in rng.integers(0, 400, k)]
+        sizes[int(rng.integers(0, k))] += 1  # psi >= 1
+        psi = sum(sizes)
+        lay = orc.partition(psi, n, 2, int(rng.choice([1, 8])))
+        got = orc.segment_map(lay, sizes).tolist()
+        assert got == _segments_by_runs(psi, lay.shard, sizes)
+        # one piece per non-empty tensor plus one per shard boundary strictly inside a tensor
+        starts = np.cumsum([0] + sizes)
+        inside = sum(1 for b in range(1, n) for t in range(k)
+                     if starts[t] < b * lay.shard < starts[t + 1])
+        assert len(got) == sum(1 for x in sizes if x) + inside
+        assert sum(row[4] for row in got) == psi
+
+
+def pin_segment_map_rejects_bad_sums(orc):
+    lay = orc.partition(100, 4)
+    for sizes in ([99], [50, 51], [], [100, 1]):
+        try:
+            orc.segment_map(lay, sizes)
+        except ValueError:
+            continue
+        raise AssertionError(f"sizes {sizes} accepted for psi=100")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

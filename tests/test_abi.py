@@ -139,6 +139,15 @@ def test_norm_adamw_step_rejections(lib):
     assert lib.zero_grad_norm(C.byref(lay), C.byref(hp), A + 8, A, None) == z.ZERO_EALIGN
     assert lib.zero_adamw_cast_gather(C.byref(lay), C.byref(hp), A, A, A, 0, A, A, None) == z.ZERO_EINVAL
     assert lib.zero_adamw_cast_gather(C.byref(lay), C.byref(hp), A, A, A, A, A + 2, A, None) == z.ZERO_EALIGN
+    hs = lib.zero_adamw_cast_gather_host_state
+    hs.argtypes, hs.restype = lib.zero_adamw_cast_gather.argtypes, C.c_int
+    for b in bad_hps:
+        assert hs(C.byref(lay), C.byref(b), A, A, A, A, A, A, None) == z.ZERO_EINVAL
+    assert hs(C.byref(lay), C.byref(hp), A, A, 0, A, A, A, None) == z.ZERO_EINVAL
+    assert hs(C.byref(lay), C.byref(hp), A, A + 4, A, A, A, A, None) == z.ZERO_EALIGN
+    # an address that is not page-locked host memory known to CUDA is refused before any
+    # launch (here: no GPU, or a made-up address)
+    assert hs(C.byref(lay), C.byref(hp), A, A, A, A, A, A, None) == z.ZERO_EINVAL
     reps = (C.c_void_p * 4)(A, A, A, A)
     # a bad bucket pointer anywhere rejects the whole step before any launch
     assert lib.zero_step(C.byref(lay), C.byref(hp), z.ZERO_BF16, reps, A, A, A, A, A, A + 1, A, None) == z.ZERO_EALIGN

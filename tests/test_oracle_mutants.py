@@ -55,6 +55,13 @@ MUTANTS = [
     ("clip eps sign", "double c = (double)max_norm / (norm + 1e-6);",
      "double c = (double)max_norm / (norm - 1e-6);"),
     ("clip comparison", "return c < 1.0 ? (float)c : 1.0f;", "return c > 1.0 ? (float)c : 1.0f;"),
+    # per-tensor segment map
+    ("segment rank", "uint64_t r = i / lay->shard;", "uint64_t r = i / (lay->shard + 1);"),
+    ("segment shard offset", "out[n].shard_offset = i - r * lay->shard;",
+     "out[n].shard_offset = i - start_of_k;"),
+    ("segment tensor offset", "out[n].tensor_offset = i - start_of_k;", "out[n].tensor_offset = i;"),
+    ("segment ignores shard cuts", "if (k != cur_tensor || r != cur_rank) {", "if (k != cur_tensor) {"),
+    ("segment size check", "if (total != lay->psi)", "if (total > lay->psi)"),
     # scaler
     ("backoff factor", "float half = s->loss_scale * 0.5f;", "float half = s->loss_scale * 0.25f;"),
     ("t on overflow", "        s->n_skipped += 1;\n        return 0;", "        s->n_skipped += 1;\n        s->t += 1;\n        return 0;"),

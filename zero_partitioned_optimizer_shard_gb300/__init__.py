@@ -75,6 +75,8 @@ def _lib() -> C.CDLL:
         L = C.CDLL(LIB_PATH)
         L.zero_partition.argtypes = [C.c_uint64, C.c_uint32, C.c_uint32, C.c_uint32, C.c_uint64,
                                      C.POINTER(Layout)]
+        L.zero_segment_map.argtypes = [C.POINTER(Layout), _P, C.c_uint64, _P, C.c_uint64,
+                                       C.POINTER(C.c_uint64)]
         L.zero_workspace_bytes.argtypes = [C.POINTER(Layout)]
         L.zero_workspace_bytes.restype = C.c_size_t
         L.zero_step_state_init.argtypes = [C.POINTER(Layout), C.c_float, C.c_uint32, C.c_uint32,
@@ -86,6 +88,7 @@ def _lib() -> C.CDLL:
         L.zero_grad_norm.argtypes = [C.POINTER(Layout), C.POINTER(HParams), _P, _P, _P]
         L.zero_adamw_cast_gather.argtypes = [C.POINTER(Layout), C.POINTER(HParams), _P, _P, _P, _P,
                                              _P, _P, _P]
+        L.zero_adamw_cast_gather_host_state.argtypes = L.zero_adamw_cast_gather.argtypes
         L.zero_step.argtypes = [C.POINTER(Layout), C.POINTER(HParams), C.c_int, C.POINTER(_P), _P,
                                 _P, _P, _P, _P, _P, _P, _P]
         L.zero_step_host.argtypes = [C.POINTER(Layout), C.POINTER(HParams), C.c_int, C.POINTER(_P),
@@ -93,10 +96,10 @@ def _lib() -> C.CDLL:
         L.zero_strerror.argtypes = [C.c_int]
         L.zero_strerror.restype = C.c_char_p
         L.zero_last_cuda_error.argtypes = []
-        for name in ("zero_partition", "zero_step_state_init", "zero_step_state_read",
+        for name in ("zero_partition", "zero_segment_map", "zero_step_state_init", "zero_step_state_read",
                      "zero_step_state_write", "zero_reduce_shard_unscale", "zero_grad_norm",
-                     "zero_adamw_cast_gather", "zero_step", "zero_step_host",
-                     "zero_last_cuda_error"):
+                     "zero_adamw_cast_gather", "zero_adamw_cast_gather_host_state", "zero_step",
+                     "zero_step_host", "zero_last_cuda_error"):
             getattr(L, name).restype = C.c_int
         _L = L
     return _L
@@ -151,6 +154,25 @@ def zero_partition(psi: int, n_ranks: int, stage: int = 2, align: int = 1,
     return lay
 
 
+class Segment(C.Structure):
+    """One piece of a model tensor inside one rank's shard (zero_segment_t)."""
+    _fields_ = [("tensor", C.c_uint64), ("rank", C.c_uint64), ("tensor_offset", C.c_uint64),
+                ("shard_offset", C.c_uint64), ("count", C.c_uint64)]
+
+
+def zero_segment_map(layout: Layout, tensor_elems: Sequence[int]) -> list:
+    """Each tensor's piece on each rank, in flat order: a list of Segment."""
+    n_t = len(tensor_elems)
+    sizes = (C.c_uint64 * max(n_t, 1))(*tensor_elems)
+    n = C.c_uint64()
+    _check("zero_segment_map", _lib().zero_segment_map(C.byref(layout), sizes, n_t, None, 0,
+                                                       C.byref(n)))
+    out = (Segment * max(n.value, 1))()
+    _check("zero_segment_map", _lib().zero_segment_map(C.byref(layout), sizes, n_t, out, n.value,
+                                                       C.byref(n)))
+    return list(out[:n.value])
+
+
 def zero_workspace_bytes(layout: Layout) -> int:
     return _lib().zero_workspace_bytes(C.byref(layout))
 
@@ -192,6 +214,14 @@ def zero_adamw_cast_gather(layout: Layout, hp: HParams, g, master, m, v, params,
         _ptr(st), _stream(stream)))
 
 
+def zero_adamw_cast_gather_host_state(layout: Layout, hp: HParams, g, master, m, v, params, st,
+                                      stream=None) -> None:
+    """master, m, v: page-locked host buffers (e.g. torch pin_memory tensors)."""
+    _check("zero_adamw_cast_gather_host_state", _lib().zero_adamw_cast_gather_host_state(
+        C.byref(layout), C.byref(hp), _ptr(g), _ptr(master), _ptr(m), _ptr(v), _ptr(params),
+        _ptr(st), _stream(stream)))
+
+
 def zero_step(layout: Layout, hp: HParams, dtype: int, replicas: Sequence, g, partials, master, m,
               v, params, st, stream=None) -> None:
     """replicas: n_buckets * N device buffers (or addresses), bucket-major."""
@@ -226,8 +256,9 @@ def zero_step_static_workspace(layout: Layout, hp: HParams, dtype: int, replicas
 
 __all__ = [
     "Layout", "HParams", "StepState", "ZeroError", "hparams", "lib", "STATE_BYTES",
-    "ZERO_F16", "ZERO_BF16", "zero_partition", "zero_workspace_bytes", "zero_step_state_init",
+    "ZERO_F16", "ZERO_BF16", "Segment", "zero_partition", "zero_segment_map", "zero_workspace_bytes", "zero_step_state_init",
     "zero_step_state_read", "zero_step_state_write", "zero_reduce_shard_unscale",
-    "zero_grad_norm", "zero_adamw_cast_gather", "zero_step", "zero_step_host",
+    "zero_grad_norm", "zero_adamw_cast_gather", "zero_adamw_cast_gather_host_state", "zero_step",
+    "zero_step_host",
     "zero_step_static_workspace",
 ]

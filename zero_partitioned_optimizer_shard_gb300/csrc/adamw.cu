@@ -212,6 +212,91 @@ __global__ void __launch_bounds__(kBlock, 1) k_adamw(const __grid_constant__ Ada
     }
 }
 
+/*
+ * The same update with master, m and v resident in pinned host memory ("ZeRO 显存优化"
+ * sec. 6: the optimizer state may be offloaded to the CPU, at a transfer cost to be
+ * measured on the machine).  On GB300 the Grace host memory is reached over NVLink-C2C
+ * by ordinary loads and stores, so the step stays one fused kernel: each element's state
+ * crosses the link once in each direction (12 B up, 12 B down) while g is read from and
+ * the gathered parameter written to HBM.  The link, not HBM, bounds it; the kernel keeps
+ * enough 128-bit loads in flight per thread (two groups of four elements from each of
+ * the four arrays) to cover the link's latency.  Bulk-copy rings are not used for host
+ * memory: plain loads measured the link's full rate.  The arithmetic is adamw_one,
+ * so results are bit-identical to k_adamw's.
+ */
+constexpr int kHostUnroll = 2;
+
+template <bool F16>
+__global__ void __launch_bounds__(kBlock) k_adamw_host_state(const __grid_constant__ AdamwArgs a)
+{
+    const zero_step_state_t* st = a.st;
+    if (st->skip)
+        return;
+    __shared__ Scalars s_sh;
+    if (threadIdx.x == 0) {
+        s_sh.c = st->clip_coef;
+        s_sh.step = st->step_size;
+        s_sh.rbc2 = st->rbc2;
+        s_sh.decay = st->decay;
+        s_sh.b1 = a.beta1;
+        s_sh.b2 = a.beta2;
+        s_sh.omb1 = __fsub_rn(1.0f, a.beta1);
+        s_sh.omb2 = __fsub_rn(1.0f, a.beta2);
+        s_sh.eps = a.eps;
+    }
+    __syncthreads();
+    const Scalars& s = s_sh;
+
+    const uint64_t n4 = a.psi / 4;  // whole groups of four, none holding padding
+    const uint64_t stride = (uint64_t)gridDim.x * kBlock;
+    const uint64_t tid = (uint64_t)blockIdx.x * kBlock + threadIdx.x;
+    const float4* g4 = reinterpret_cast<const float4*>(a.g);
+    float4* p4 = reinterpret_cast<float4*>(a.master);
+    float4* m4 = reinterpret_cast<float4*>(a.m);
+    float4* v4 = reinterpret_cast<float4*>(a.v);
+    uint2* o4 = reinterpret_cast<uint2*>(a.out);
+    for (uint64_t j = tid; j < n4; j += kHostUnroll * stride) {
+        float4 g[kHostUnroll], p[kHostUnroll], m[kHostUnroll], v[kHostUnroll];
+#pragma unroll
+        for (int u = 0; u < kHostUnroll; ++u) {
+            const uint64_t q = j + u * stride;
+            if (q < n4) {
+                g[u] = __ldcs(g4 + q);
+                p[u] = __ldcs(p4 + q);
+                m[u] = __ldcs(m4 + q);
+                v[u] = __ldcs(v4 + q);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kHostUnroll; ++u) {
+            const uint64_t q = j + u * stride;
+            if (q < n4) {
+                uint2 o;
+                o.x = pack2<F16>(adamw_one(g[u].x, p[u].x, m[u].x, v[u].x, s),
+                                 adamw_one(g[u].y, p[u].y, m[u].y, v[u].y, s));
+                o.y = pack2<F16>(adamw_one(g[u].z, p[u].z, m[u].z, v[u].z, s),
+                                 adamw_one(g[u].w, p[u].w, m[u].w, v[u].w, s));
+                __stcs(p4 + q, p[u]);
+                __stcs(m4 + q, m[u]);
+                __stcs(v4 + q, v[u]);
+                __stcs(o4 + q, o);
+            }
+        }
+    }
+    for (uint64_t i = n4 * 4 + tid; i < a.psi_padded; i += stride) {
+        if (i < a.psi) {
+            float p = a.master[i], m = a.m[i], v = a.v[i];
+            const float r = adamw_one(a.g[i], p, m, v, s);
+            a.master[i] = p;
+            a.m[i] = m;
+            a.v[i] = v;
+            a.out[i] = pack1<F16>(r);
+        } else {
+            a.out[i] = 0;
+        }
+    }
+}
+
 }  // namespace
 
 #ifdef ZERO_TEST_HOOKS
@@ -244,6 +329,21 @@ cudaError_t launch_adamw(const AdamwArgs& a, cudaStream_t s)
         k_adamw<true><<<grid > 0 ? grid : 1, kBlock, kSmemBytes, s>>>(a);
     else
         k_adamw<false><<<grid > 0 ? grid : 1, kBlock, kSmemBytes, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_adamw_host_state(const AdamwArgs& a, cudaStream_t s)
+{
+    const uint64_t groups = a.psi / 4;
+    const uint64_t tail = a.psi_padded - groups * 4;
+    const uint64_t want_threads = (groups + kHostUnroll - 1) / kHostUnroll;
+    uint64_t want = ((want_threads > tail ? want_threads : tail) + kBlock - 1) / kBlock;
+    const uint64_t cap = (uint64_t)sm_count() * 3;  // 80 registers x 256 threads: 3 blocks per SM
+    const unsigned grid = (unsigned)(want < cap ? (want > 0 ? want : 1) : cap);
+    if (a.out_f16)
+        k_adamw_host_state<true><<<grid, kBlock, 0, s>>>(a);
+    else
+        k_adamw_host_state<false><<<grid, kBlock, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -7,22 +7,10 @@
 #include "zero_internal.h"
 
 #include <mutex>
+#include <stddef.h>
 #include <string.h>
 
 namespace zero {
-
-namespace {
-thread_local int g_last_cuda_error = 0;
-
-int cuda_status(cudaError_t e)
-{
-    if (e == cudaSuccess)
-        return ZERO_OK;
-    g_last_cuda_error = (int)e;
-    return ZERO_ECUDA;
-}
-
-bool aligned16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
 
 /* The invariants zero_partition establishes; the kernels' indexing relies on them. */
 bool layout_ok(const zero_layout_t* L)
@@ -43,6 +31,19 @@ bool layout_ok(const zero_layout_t* L)
         return false;
     return L->n_buckets == (L->psi_padded + W - 1) / W;
 }
+
+namespace {
+thread_local int g_last_cuda_error = 0;
+
+int cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess)
+        return ZERO_OK;
+    g_last_cuda_error = (int)e;
+    return ZERO_ECUDA;
+}
+
+bool aligned16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
 
 bool kernel_layout_ok(const zero_layout_t* L)
 {
@@ -135,7 +136,8 @@ int grad_norm(const zero_layout_t* L, const zero_adamw_hparams_t* hp, double* pa
 }
 
 int adamw(const zero_layout_t* L, const zero_adamw_hparams_t* hp, const float* g, float* master,
-          float* m, float* v, uint16_t* params, const zero_step_state_t* st, cudaStream_t stream)
+          float* m, float* v, uint16_t* params, const zero_step_state_t* st, cudaStream_t stream,
+          bool host_state = false)
 {
     AdamwArgs a;
     a.g = g;
@@ -151,7 +153,30 @@ int adamw(const zero_layout_t* L, const zero_adamw_hparams_t* hp, const float* g
     a.beta2 = hp->beta2;
     a.eps = hp->eps;
     a.out_f16 = hp->params_dtype == ZERO_F16 ? 1u : 0u;
-    return cuda_status(launch_adamw(a, stream));
+    return cuda_status(host_state ? launch_adamw_host_state(a, stream) : launch_adamw(a, stream));
+}
+
+/* The device address of `bytes` of page-locked host memory at p (cudaHostAlloc or
+ * cudaHostRegister, which UVA maps into the device's address space), or null when any
+ * part of it is not such memory: pageable, device or unknown pointers are refused. */
+void* pinned_host_device_ptr(const void* p, uint64_t bytes)
+{
+    const char* ends[2] = {static_cast<const char*>(p), static_cast<const char*>(p) + bytes - 1};
+    void* dev[2] = {nullptr, nullptr};
+    for (int k = 0; k < 2; ++k) {
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, ends[k]) != cudaSuccess) {
+            cudaGetLastError();  // clear the (non-sticky) error the query left
+            return nullptr;
+        }
+        if (at.type != cudaMemoryTypeHost || !at.devicePointer)
+            return nullptr;
+        dev[k] = at.devicePointer;
+    }
+    // one mapping: the last byte's device address lies exactly bytes-1 past the first's
+    if (static_cast<char*>(dev[1]) - static_cast<char*>(dev[0]) != (ptrdiff_t)(bytes - 1))
+        return nullptr;
+    return dev[0];
 }
 
 }  // namespace
@@ -250,6 +275,25 @@ extern "C" int zero_adamw_cast_gather(const zero_layout_t* layout, const zero_ad
     if (rc != ZERO_OK)
         return rc;
     return adamw(layout, hp, g, master, m, v, params, st, (cudaStream_t)stream);
+}
+
+extern "C" int zero_adamw_cast_gather_host_state(const zero_layout_t* layout,
+                                                 const zero_adamw_hparams_t* hp, const float* g,
+                                                 float* master, float* m, float* v,
+                                                 uint16_t* params, const zero_step_state_t* st,
+                                                 zero_stream_t stream)
+{
+    const int rc = check_adamw_args(layout, hp, g, master, m, v, params, st);
+    if (rc != ZERO_OK)
+        return rc;
+    const uint64_t bytes = layout->psi_padded * sizeof(float);
+    float* dm[3] = {master, m, v};
+    for (float*& x : dm) {
+        x = static_cast<float*>(pinned_host_device_ptr(x, bytes));
+        if (!x)
+            return ZERO_EINVAL;
+    }
+    return adamw(layout, hp, g, dm[0], dm[1], dm[2], params, st, (cudaStream_t)stream, true);
 }
 
 extern "C" int zero_step(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,

@@ -67,3 +67,48 @@ extern "C" size_t zero_workspace_bytes(const zero_layout_t* layout)
         return 0;
     return (size_t)layout->n_tiles * sizeof(double);
 }
+
+/*
+ * zero_segment_map -- where each model tensor's elements live among the shards.
+ * "【论文解读】ZeRO" sec. 4(2): gradients are bucketed by partition and reduced at the
+ * partition boundary, so a tensor that crosses a shard boundary is split between two
+ * or more owners.  The tensors are laid end to end over the flat buffer in list order;
+ * tensor k's piece on rank r is its intersection with [r*S, (r+1)*S).  One pass over the
+ * tensors, O(n_tensors + n_ranks); the pieces come out in flat order.
+ */
+extern "C" int zero_segment_map(const zero_layout_t* layout, const uint64_t* tensor_elems,
+                                uint64_t n_tensors, zero_segment_t* out, uint64_t capacity,
+                                uint64_t* n_segments)
+{
+    if (!zero::layout_ok(layout) || !n_segments || (n_tensors > 0 && !tensor_elems))
+        return ZERO_EINVAL;
+    const uint64_t S = layout->shard;
+    uint64_t total = 0, count = 0;
+    for (uint64_t k = 0; k < n_tensors; ++k) {
+        const uint64_t e = tensor_elems[k];
+        if (e > layout->psi - total)  // also catches a sum past 2^64
+            return ZERO_EINVAL;
+        if (e > 0)
+            count += (total + e - 1) / S - total / S + 1;
+        total += e;
+    }
+    if (total != layout->psi)
+        return ZERO_EINVAL;
+    *n_segments = count;
+    if (!out)
+        return ZERO_OK;
+    if (capacity < count)
+        return ZERO_ENOMEM;
+    uint64_t a = 0, w = 0;
+    for (uint64_t k = 0; k < n_tensors; ++k) {
+        const uint64_t b = a + tensor_elems[k];
+        for (uint64_t r = a / S; a < b && r * S < b; ++r) {
+            const uint64_t lo = a > r * S ? a : r * S;
+            const uint64_t hi = b < (r + 1) * S ? b : (r + 1) * S;
+            out[w++] = zero_segment_t{k, r, lo - a, lo - r * S, hi - lo};
+        }
+        a = b;
+    }
+    return ZERO_OK;
+}
+

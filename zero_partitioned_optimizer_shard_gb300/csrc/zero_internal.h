@@ -57,9 +57,11 @@ struct InitArgs {
 cudaError_t launch_reduce(const ReduceArgs& a, zero_dtype_t dtype, cudaStream_t s);
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s);
 cudaError_t launch_adamw(const AdamwArgs& a, cudaStream_t s);
+cudaError_t launch_adamw_host_state(const AdamwArgs& a, cudaStream_t s);  // master/m/v in pinned host memory
 cudaError_t launch_state_init(const InitArgs& a, cudaStream_t s);
 
 /* Resident blocks per SM times SM count for a kernel, cached per device. */
+bool layout_ok(const zero_layout_t* L);  // the invariants zero_partition establishes
 int sm_count();
 
 /* Make zero_last_cuda_error() report `e` on this thread. */
