@@ -277,6 +277,10 @@ def run_ours(args):
 
     peak, peak_kind = _peaks()
     ms = elapsed_ms / args.steps
+    per_step = sorted(a + b + c for a, b, c in zip(reduce_ms, norm_ms, adamw_ms))
+
+    def pct(q):  # nearest-rank percentile of the per-step event times
+        return per_step[min(len(per_step) - 1, max(0, round(q / 100 * len(per_step)) - 1))]
     params_per_s = wl.psi * args.steps * ws / (elapsed_ms / 1e3)
     bytes_26 = (26 + 2 * N) * P
     bytes_mat = (34 + 2 * N) * P
@@ -286,7 +290,9 @@ def run_ours(args):
     red_bytes = (2 * N + 4) * P
     line = {
         "metric": METRIC, "value": params_per_s, "unit": "params/s", "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "ms_per_step_spread": {"p10": pct(10), "p50": pct(50), "p90": pct(90)},
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": _config({"parallelism": f"{ws} independent replica(s) of the simulated "
                                           f"{N}-rank step" if ws > 1 else "1 GPU, 8 simulated ranks"},

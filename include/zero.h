@@ -62,7 +62,7 @@ typedef enum zero_dtype { ZERO_F16 = 1, ZERO_BF16 = 2 } zero_dtype_t;
 
 #define ZERO_MAX_RANKS (1u << 20)   /* zero_partition (ledger and layout) */
 #define ZERO_MAX_KERNEL_RANKS 64u   /* device entry points: replicas summed per element */
-#define ZERO_TILE_ELEMS 8192u       /* rank-local tile of the sum-of-squares partials */
+#define ZERO_TILE_ELEMS 8192u       /* grid of the sum-of-squares partials' tiles */
 
 /* Partition of Psi flat parameters over N ranks.  Filled by zero_partition; pass it back
  * unchanged to the device entry points (they re-check its invariants). */
@@ -73,7 +73,8 @@ typedef struct zero_layout {
     uint64_t pad;                    /* N*S - Psi: trailing padding, gradient 0, output 0 */
     uint64_t bucket_elems;           /* W: window of one reduce launch in zero_step */
     uint64_t n_buckets;              /* ceil(N*S / W) */
-    uint64_t tiles_per_rank;         /* ceil(S / tile_elems) */
+    uint64_t tiles_per_rank;         /* ceil(S / tile_elems) + 1: a shard meets at most this
+                                        many cells of the flat tile grid */
     uint64_t n_tiles;                /* N * tiles_per_rank: fp64 partial slots */
     uint64_t bytes_per_rank[4];      /* model-state bytes per rank: [0] plain DP 16*Psi,
                                         [1] 4*N*S + 12*S, [2] 2*N*S + 14*S, [3] 16*S */
@@ -204,8 +205,11 @@ int zero_step_state_write(zero_step_state_t* st, const zero_step_state_t* host_i
  *   g[i] = (sum over k = 0..N-1, ascending, in fp32, of x_k[i]) * st->inv_scale
  *   with g[i] = 0 for padding (i >= psi; replica values there are ignored);
  *   st->overflow |= any non-finite g[i];
- *   partials[tile of i] += sum of g^2 over the window's part of each rank-local tile
- *   (tile j of rank r = flat r*S + [j*T, min((j+1)*T, S)), T = tile_elems).
+ *   partials[tile of i] += sum of g^2 over the window's part of each tile.  Tiles cut
+ *   each shard at the flat multiples of T = tile_elems (so interior tiles start on
+ *   128-byte lines of every array): tile j of rank r is the intersection of
+ *   [r*S, (r+1)*S) with [(c+j)*T, (c+j+1)*T), c = floor(r*S/T); slot r*tiles_per_rank + j.
+ *   A rank's trailing slots may be empty (always 0).
  *   dtype      ZERO_F16 or ZERO_BF16 (the replicas' element type)
  *   replicas   HOST array of N DEVICE pointers; replicas[k] points at flat element
  *              `begin` of rank k's gradient copy and holds at least `count` elements

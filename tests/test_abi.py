@@ -66,7 +66,7 @@ def test_partition_matches_oracle(lib, stage):
         assert (lz.psi, lz.shard, lz.psi_padded, lz.pad) == (lo.psi, lo.shard, lo.psi_padded, lo.pad)
         assert list(lz.bytes_per_rank) == list(lo.bytes_per_rank)
         assert list(lz.comm_elems_per_rank) == list(lo.comm_elems_per_rank)
-        assert lz.tiles_per_rank == -(-lz.shard // z.ZERO_TILE_ELEMS)
+        assert lz.tiles_per_rank == -(-lz.shard // z.ZERO_TILE_ELEMS) + 1
         assert lz.n_tiles == n * lz.tiles_per_rank
         assert z.zero_workspace_bytes(lz) == 8 * lz.n_tiles
 

@@ -145,6 +145,50 @@ def test_overflow_skips_and_backs_off(bits):
     gpu.check_guards()
 
 
+def _bf16_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 values that are exact in bf16 -> their bf16 bit patterns."""
+    u = np.asarray(x, np.float32).view(np.uint32)
+    assert np.all(u & 0xFFFF == 0)
+    return (u >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("case", ["huge", "tiny", "mixed"])
+def test_sum_of_squares_at_the_range_edges(case):
+    """Finite gradients far from 1: the per-tile sum of squares must not overflow or lose
+    small terms.  'huge': three tiles of 2^60 (each tile's squares sum to 2^133, past the
+    fp32 range; exact in fp64); 'tiny': magnitudes 2^-60 .. 2^-90 on both sides of the
+    pair arithmetic's exact range; 'mixed': both kinds in one tile."""
+    psi, n = 5 * 8192 + 77, 4
+    wl = W.scaled(W.C2, psi, steps=1)
+    gpu = GpuRun(replace(wl, n_ranks=n))
+    orc = OracleRun(replace(wl, n_ranks=n))
+    P = gpu.lay.psi_padded
+    rng = np.random.default_rng(17)
+    vals = np.zeros((n, P), np.float32)
+    if case in ("huge", "mixed"):
+        vals[:, 1000:1000 + 3 * 8192] = np.float32(2.0 ** 60)
+    if case in ("tiny", "mixed"):
+        e = rng.integers(-90, -59, size=(n, psi))
+        sgn = rng.choice([-1.0, 1.0], size=(n, psi))
+        tiny = (sgn * np.ldexp(1.0, e)).astype(np.float32)
+        sel = slice(0, psi) if case == "tiny" else slice(30000, psi)
+        vals[:, sel] = tiny[:, sel]
+    vals[:, psi:] = 0
+    reps_np = [_bf16_bits(vals[k]) for k in range(n)]
+    for k in range(n):
+        gpu.reps[k].copy_(torch.from_numpy(reps_np[k].view(np.int16)))
+    z.zero_step(gpu.lay, gpu.hp, z.ZERO_BF16, gpu.bucket_ptrs(), gpu.g, gpu.partials, gpu.master,
+                gpu.m, gpu.v, gpu.out, gpu.st)
+    st = gpu.state()
+    from oracle import BF16
+    rep = orc.orc.step(orc.lay, orc.hp, BF16, reps_np, orc.g, orc.master, orc.m, orc.v, orc.out,
+                       orc.sc)
+    assert np.isfinite(st.norm) and rep.norm > 0
+    assert_scalars(st, rep)
+    assert_state_close(gpu.arrays(), orc.arrays(), psi, exact_expected=st.clip_coef == rep.clip_coef)
+    gpu.check_guards()
+
+
 def test_bf16_static_scale_overflow_skips_without_backoff():
     wl = W.scaled(W.C2, 30_000, steps=1)
     gpu = GpuRun(wl)

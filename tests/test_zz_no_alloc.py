@@ -63,10 +63,10 @@ def test_static_workspace_matches_zero_step_twice(wl, bucket):
 
 
 def test_static_workspace_rejects_oversized_layout():
-    # 9e9 parameters over 64 ranks: 64 * ceil(140,625,000 / 8192) = 1,098,688 tiles, more
-    # than the array's 2^20 slots; rejected on the host before anything is enqueued
+    # 9e9 parameters over 64 ranks: 64 * (ceil(140,625,000 / 8192) + 1) = 1,098,752 tiles,
+    # more than the array's 2^20 slots; rejected on the host before anything is enqueued
     lay = z.zero_partition(9_000_000_000, 64, 2)
-    assert lay.n_tiles == 1_098_688 > (1 << 20)
+    assert lay.n_tiles == 1_098_752 > (1 << 20)
     with pytest.raises(z.ZeroError) as e:
         z.zero_step_static_workspace(lay, z.hparams(), z.ZERO_BF16, [16] * 64, 16, 16, 16, 16, 16, 16)
     assert e.value.status == z.ZERO_ENOMEM

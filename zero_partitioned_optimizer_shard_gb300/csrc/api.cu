@@ -23,7 +23,7 @@ bool layout_ok(const zero_layout_t* L)
         return false;
     if (L->tile_elems != ZERO_TILE_ELEMS)
         return false;
-    if (L->tiles_per_rank != (L->shard + L->tile_elems - 1) / L->tile_elems ||
+    if (L->tiles_per_rank != tiles_per_rank(L->shard, L->tile_elems) ||
         L->n_tiles != (uint64_t)L->n_ranks * L->tiles_per_rank)
         return false;
     const uint64_t W = L->bucket_elems;
@@ -81,12 +81,8 @@ int reduce_window(const zero_layout_t* L, zero_dtype_t dtype, const void* const*
     a.tiles_per_rank = L->tiles_per_rank;
     a.n_ranks = L->n_ranks;
     a.tile = L->tile_elems;
-    const uint64_t T = L->tile_elems, S = L->shard;
-    const uint64_t r0 = begin / S, r1 = (a.end - 1) / S;
-    const uint64_t u0 = r0 * L->tiles_per_rank + (begin - r0 * S) / T;
-    const uint64_t u1 = r1 * L->tiles_per_rank + (a.end - 1 - r1 * S) / T;
-    a.unit_first = u0;
-    a.unit_count = u1 - u0 + 1;
+    a.unit_first = tile_unit(L, begin);
+    a.unit_count = tile_unit(L, a.end - 1) - a.unit_first + 1;
     return cuda_status(launch_reduce(a, dtype, stream));
 }
 

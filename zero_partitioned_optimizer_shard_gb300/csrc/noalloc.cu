@@ -35,7 +35,8 @@ int fail_cuda(cudaError_t e)
 bool is_aligned16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
 
 /* The same invariants the other device entry points check, restated here so this
- * entry point shares no code path with them. */
+ * entry point's validation shares no code path with them (the tile grid is the
+ * layout's definition, shared). */
 bool layout_valid(const zero_layout_t* L)
 {
     if (!L || L->n_ranks == 0 || L->n_ranks > ZERO_MAX_KERNEL_RANKS || L->psi == 0 ||
@@ -44,7 +45,7 @@ bool layout_valid(const zero_layout_t* L)
     if (L->psi_padded != (uint64_t)L->n_ranks * L->shard || L->psi > L->psi_padded ||
         L->pad != L->psi_padded - L->psi || L->tile_elems != ZERO_TILE_ELEMS)
         return false;
-    if (L->tiles_per_rank != (L->shard + L->tile_elems - 1) / L->tile_elems ||
+    if (L->tiles_per_rank != zero::tiles_per_rank(L->shard, L->tile_elems) ||
         L->n_tiles != (uint64_t)L->n_ranks * L->tiles_per_rank)
         return false;
     const uint64_t W = L->bucket_elems;
@@ -140,10 +141,8 @@ extern "C" int zero_step_static_workspace(const zero_layout_t* layout,
         a.tiles_per_rank = layout->tiles_per_rank;
         a.n_ranks = layout->n_ranks;
         a.tile = layout->tile_elems;
-        const uint64_t S = layout->shard, T = layout->tile_elems;
-        const uint64_t r0 = a.begin / S, r1 = (a.end - 1) / S;
-        a.unit_first = r0 * layout->tiles_per_rank + (a.begin - r0 * S) / T;
-        a.unit_count = r1 * layout->tiles_per_rank + (a.end - 1 - r1 * S) / T - a.unit_first + 1;
+        a.unit_first = zero::tile_unit(layout, a.begin);
+        a.unit_count = zero::tile_unit(layout, a.end - 1) - a.unit_first + 1;
         e = zero::launch_reduce(a, dtype, s);
         if (e != cudaSuccess)
             return fail_cuda(e);

@@ -42,7 +42,7 @@ extern "C" int zero_partition(uint64_t psi, uint32_t n_ranks, uint32_t stage, ui
     L.bucket_elems = W;
     L.n_buckets = (P + W - 1) / W;
     L.tile_elems = ZERO_TILE_ELEMS;
-    L.tiles_per_rank = (S + ZERO_TILE_ELEMS - 1) / ZERO_TILE_ELEMS;
+    L.tiles_per_rank = zero::tiles_per_rank(S, ZERO_TILE_ELEMS);
     L.n_tiles = N * L.tiles_per_rank;
     L.n_ranks = n_ranks;
     L.stage = stage;
@@ -60,6 +60,21 @@ extern "C" int zero_partition(uint64_t psi, uint32_t n_ranks, uint32_t stage, ui
     *out = L;
     return ZERO_OK;
 }
+
+namespace zero {
+
+uint64_t tiles_per_rank(uint64_t S, uint64_t T)
+{
+    return (S + T - 1) / T + 1;  // [a, a+S) meets at most ceil(S/T) + 1 cells of the T grid
+}
+
+uint64_t tile_unit(const zero_layout_t* L, uint64_t i)
+{
+    const uint64_t r = i / L->shard, T = L->tile_elems;
+    return r * L->tiles_per_rank + (i / T - (r * L->shard) / T);
+}
+
+}  // namespace zero
 
 extern "C" size_t zero_workspace_bytes(const zero_layout_t* layout)
 {

@@ -14,9 +14,12 @@
  * combines.
  *
  * GB300 design.  Pure HBM streaming (2N bytes in, 4 out per element, a few flops), so:
- *  - a persistent grid (SM count x resident blocks) walks rank-local tiles of 8192
- *    elements; one block owns a tile, so its partial is written by exactly one block per
- *    launch (deterministic, no atomics on the data path);
+ *  - a persistent grid (SM count x resident blocks) walks tiles of at most 8192
+ *    elements: each shard cut at the flat multiples of 8192, so interior tiles start on
+ *    128-byte lines of every array even when the shard size is not a multiple of 64
+ *    (misaligned warps touched one extra line per load: 4% of the kernel's time at the
+ *    GPT-2 size); one block owns a tile, so its partial is written by exactly one block
+ *    per launch (deterministic, no atomics on the data path);
  *  - every thread moves 8 elements per replica with one 128-bit non-coherent load that
  *    skips L1 (ld.global.nc.L1::no_allocate.v4), all N replica loads issued before the
  *    sum, and writes g with streaming 128-bit stores;
@@ -24,7 +27,8 @@
  *    TwoProduct (FMA) and TwoSum steps, which keeps it at ~2^-48 relative accuracy without
  *    per-element fp64 (GB300's fp64 rate is a small fraction of fp32), then folded into
  *    fp64 once per thread and reduced in a fixed shuffle tree per tile;
- *  - elements whose squares leave the fp32 range are summed in fp64 instead.
+ *  - groups with an element outside the pair arithmetic's exact range (below 2^-74 or
+ *    at least 2^34 in magnitude, or not finite) are summed in fp64 instead.
  */
 #include "zero_internal.h"
 
@@ -94,8 +98,14 @@ __device__ __forceinline__ void add8(float (&s)[8], const uint4& v)
 
 /* Sum of squares of the fp32 gradient, carried as an unevaluated pair hi + lo of fp32
  * values.  TwoProduct: x*x = p + pe exactly (FMA); TwoSum: hi + p = s + err exactly.
- * Exact for every |x| in [2^-50, 2^62) and for zeros; groups holding anything else take
- * the fp64 path below (never in normal training data). */
+ * The values are scaled by 2^24 first (exact) and the tile's total by 2^-48 at the end,
+ * which moves the range where every step is exact and nothing can overflow (1024 squares
+ * per warp before the fp64 fold) to |x| in [2^-74, 2^34), plus zeros: gradients of
+ * ~1e-4 often come within 2^-50 of zero, which unscaled would need the fp64 path.
+ * Power-of-two scaling changes no rounding, so the result is the unscaled pair sum's.
+ * Groups holding anything outside that range take the fp64 path below. */
+constexpr float kSqScale = 16777216.0f;  // 2^24
+constexpr double kSqUnscale = 0x1p-48;
 struct SumSq {
     float hi = 0.0f, lo = 0.0f;
     double wide = 0.0;
@@ -112,8 +122,8 @@ struct SumSq {
     }
 };
 
-/* True when all 8 values are finite and every square is exact in the fp32 pair
- * arithmetic: magnitudes in [2^-50, 2^62) or zero.  Integer compares on the magnitude
+/* True when all 8 values are finite and every scaled square is exact in the fp32 pair
+ * arithmetic: magnitudes in [2^-74, 2^34) or zero.  Integer compares on the magnitude
  * bits, so NaN (above inf) and inf fail the test too. */
 __device__ __forceinline__ bool squares_in_range(const float (&x)[8])
 {
@@ -124,7 +134,7 @@ __device__ __forceinline__ bool squares_in_range(const float (&x)[8])
         mx = max(mx, u);
         mn = min(mn, u == 0u ? 0x3f800000u : u);
     }
-    return mx < 0x5e800000u && mn >= 0x26800000u;  // 2^62 and 2^-50
+    return mx < 0x50800000u && mn >= 0x1a800000u;  // 2^34 and 2^-74
 }
 
 /* fp64 sum of squares of the elements of a group selected by mask; a real call, so the
@@ -167,11 +177,16 @@ __global__ void __launch_bounds__(kBlock) k_reduce(const __grid_constant__ Reduc
         const uint64_t unit = a.unit_first + u;
         const uint64_t r = unit / a.tiles_per_rank;
         const uint64_t j = unit - r * a.tiles_per_rank;
-        const uint64_t shard_lo = r * a.shard;
-        uint64_t lo = shard_lo + j * a.tile;
-        uint64_t hi = lo + a.tile < shard_lo + a.shard ? lo + a.tile : shard_lo + a.shard;
+        // tile j of rank r: the shard cut at the flat multiples of the tile size, so the
+        // 128-bit loads of interior tiles start on 128-byte lines of every array
+        const uint64_t shard_lo = r * a.shard, shard_hi = shard_lo + a.shard;
+        const uint64_t cell = (shard_lo / a.tile + j) * a.tile;
+        uint64_t lo = cell > shard_lo ? cell : shard_lo;
+        uint64_t hi = cell + a.tile < shard_hi ? cell + a.tile : shard_hi;
         lo = lo > a.begin ? lo : a.begin;
         hi = hi < a.end ? hi : a.end;
+        if (lo >= hi)  // a rank's trailing empty slot, or a tile outside the window
+            continue;
 
         SumSq acc;
         for (uint64_t b = (lo & ~7ull) + 8ull * threadIdx.x; b < hi; b += 8ull * kBlock) {
@@ -221,7 +236,7 @@ __global__ void __launch_bounds__(kBlock) k_reduce(const __grid_constant__ Reduc
             if (squares_in_range(sq)) {  // every counted element finite: no overflow
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
-                    acc.add_fast(sq[e]);
+                    acc.add_fast(__fmul_rn(sq[e], kSqScale));
             } else {
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
@@ -255,7 +270,7 @@ __global__ void __launch_bounds__(kBlock) k_reduce(const __grid_constant__ Reduc
                 wide += __shfl_xor_sync(0xffffffffu, wide, o);
         }
         if ((threadIdx.x & 31) == 0)
-            warp_part[threadIdx.x >> 5] = ((double)ph + (double)pl) + wide;
+            warp_part[threadIdx.x >> 5] = ((double)ph + (double)pl) * kSqUnscale + wide;
         __syncthreads();
         if (threadIdx.x == 0) {
             double t = 0.0;

@@ -62,6 +62,13 @@ cudaError_t launch_state_init(const InitArgs& a, cudaStream_t s);
 
 /* Resident blocks per SM times SM count for a kernel, cached per device. */
 bool layout_ok(const zero_layout_t* L);  // the invariants zero_partition establishes
+
+/* Sum-of-squares tiles: each shard [r*S, (r+1)*S) cut at the flat multiples of T, so
+ * every interior tile starts on a 128-byte line of each array whatever S is.  Tile j of
+ * rank r = [r*S, (r+1)*S) intersected with [(c+j)*T, (c+j+1)*T), c = floor(r*S/T);
+ * partial slot r*tiles_per_rank + j (trailing slots of a rank may be empty). */
+uint64_t tiles_per_rank(uint64_t S, uint64_t T);
+uint64_t tile_unit(const zero_layout_t* L, uint64_t i);  // slot of the tile holding flat i
 int sm_count();
 
 /* Make zero_last_cuda_error() report `e` on this thread. */
