@@ -165,121 +165,161 @@ __device__ __forceinline__ bool not_finite(float x)
     return (__float_as_uint(x) & 0x7f800000u) == 0x7f800000u;
 }
 
+/* The tile j of rank r, clipped to the window: [lo, hi), empty for a rank's trailing
+ * slot.  Shards are cut at the flat multiples of the tile size, so the 128-bit loads of
+ * interior tiles start on 128-byte lines of every array. */
+__device__ __forceinline__ void tile_bounds(const ReduceArgs& a, uint64_t unit, uint64_t& lo, uint64_t& hi)
+{
+    constexpr uint64_t T = ZERO_TILE_ELEMS;  // the layout's tile_elems (checked on the host)
+    const uint64_t tpr = a.tiles_per_rank;
+    // 64-bit division is a long instruction sequence; 32 bits cover any layout below
+    // 2^32 tiles (3.5e13 parameters)
+    const uint64_t r = (unit >> 32) == 0 && (tpr >> 32) == 0 ? (uint64_t)((uint32_t)unit / (uint32_t)tpr)
+                                                              : unit / tpr;
+    const uint64_t j = unit - r * tpr;
+    const uint64_t shard_lo = r * a.shard, shard_hi = shard_lo + a.shard;
+    const uint64_t cell = (shard_lo / T + j) * T;
+    lo = cell > shard_lo ? cell : shard_lo;
+    hi = cell + T < shard_hi ? cell + T : shard_hi;
+    lo = lo > a.begin ? lo : a.begin;
+    hi = hi < a.end ? hi : a.end;
+}
+
+/* Elements b .. b+7 once their rank sums s[] are known: unscale, zero the padding, mask
+ * what lies outside the tile [lo, hi), add the squares, flag non-finite values, store g. */
+__device__ __forceinline__ void finish_group(const ReduceArgs& a, float inv, float (&s)[8], uint64_t b,
+                                             uint64_t lo, uint64_t hi, SumSq& acc, bool& bad)
+{
+    const bool full = b >= lo && b + 8 <= hi;  // all 8 elements belong to this tile
+    float gv[8], sq[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        gv[e] = sq[e] = __fmul_rn(s[e], inv);
+    uint32_t in = 0xffu;
+    if (b + 8 > a.psi || !full) {  // padding, or a group cut by the tile/window edge
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const uint64_t i = b + e;
+            if (i >= a.psi)
+                gv[e] = 0.0f;
+            if (!(i >= lo && i < hi))
+                in &= ~(1u << e);
+            sq[e] = (in >> e & 1u) ? gv[e] : 0.0f;
+        }
+    }
+    if (squares_in_range(sq)) {  // every counted element finite: no overflow
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            acc.add_fast(__fmul_rn(sq[e], kSqScale));
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            bad |= (in >> e & 1u) && not_finite(gv[e]);
+        acc.wide += sumsq_wide(gv[0], gv[1], gv[2], gv[3], gv[4], gv[5], gv[6], gv[7], in);
+    }
+    if (full) {
+        __stcs(reinterpret_cast<float4*>(a.g + b), make_float4(gv[0], gv[1], gv[2], gv[3]));
+        __stcs(reinterpret_cast<float4*>(a.g + b + 4), make_float4(gv[4], gv[5], gv[6], gv[7]));
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (in >> e & 1u)
+                a.g[b + e] = gv[e];
+    }
+}
+
+/* One tile straight from the replicas: 8 elements per 128-bit load per replica, all N
+ * loads of a group issued before the ordered sum. */
+template <zero_dtype_t DT, int NR>
+__device__ __forceinline__ void tile_ldg(const ReduceArgs& a, float inv, uint64_t lo, uint64_t hi,
+                                         SumSq& acc, bool& bad)
+{
+    const int N = NR > 0 ? NR : (int)a.n_ranks;
+    for (uint64_t b = (lo & ~7ull) + 8ull * threadIdx.x; b < hi; b += 8ull * kBlock) {
+        float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        const uint64_t off = b - a.begin;  // a multiple of 8: begin is
+        if (b + 8 <= a.end) {
+            // the whole group lies inside the window's buffers: 128-bit loads, even where it
+            // straddles a tile edge (the other tile's elements are masked)
+#pragma unroll 1
+            for (int k0 = 0; k0 < N; k0 += kLoadBatch) {
+                uint4 v[kLoadBatch];
+#pragma unroll
+                for (int kk = 0; kk < kLoadBatch; ++kk)
+                    if (NR > 0 ? (k0 + kk < NR) : (k0 + kk < N))
+                        v[kk] = ld_stream_v4((const uint16_t*)a.rep[k0 + kk] + off);
+#pragma unroll
+                for (int kk = 0; kk < kLoadBatch; ++kk)
+                    if (NR > 0 ? (k0 + kk < NR) : (k0 + kk < N))
+                        add8<DT>(s, v[kk]);
+            }
+        } else {  // the window's last, ragged group: element loads inside [lo, hi) only
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint64_t i = b + e;
+                if (i >= lo && i < hi)
+                    for (int k = 0; k < N; ++k)
+                        s[e] = __fadd_rn(s[e], one16<DT>(ld_stream_u16((const uint16_t*)a.rep[k] + off + e)));
+            }
+        }
+        finish_group(a, inv, s, b, lo, hi, acc, bad);
+    }
+}
+
+/* The tile's partial: a fixed-order pair-arithmetic shuffle tree in fp32, fp64 once per
+ * warp, the warps in order, added to the tile's slot.  One block barrier; the per-warp
+ * values alternate between two buffers (tile parity), so the next tile cannot overwrite
+ * them before thread 0 has read them.  The add is an fp64 atomicAdd whose result is not
+ * used, so thread 0 does not wait for the old value.  Only one block adds to a tile in a
+ * launch, and the windows of a step meet a tile in stream order, so the sum's order, and
+ * its bits, are fixed. */
+__device__ __forceinline__ void tile_done(const ReduceArgs& a, uint64_t unit, const SumSq& acc,
+                                          double (*warp_part)[kBlock / 32], uint32_t& parity)
+{
+    float ph = acc.hi, pl = acc.lo;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float h2 = __shfl_xor_sync(0xffffffffu, ph, o);
+        const float l2 = __shfl_xor_sync(0xffffffffu, pl, o);
+        pair_add(ph, pl, h2, l2);
+    }
+    double wide = acc.wide;
+    if (__any_sync(0xffffffffu, wide != 0.0)) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            wide += __shfl_xor_sync(0xffffffffu, wide, o);
+    }
+    double* wp = warp_part[parity];
+    if ((threadIdx.x & 31) == 0)
+        wp[threadIdx.x >> 5] = ((double)ph + (double)pl) * kSqUnscale + wide;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+#pragma unroll
+        for (int w = 0; w < kBlock / 32; ++w)
+            t += wp[w];
+        atomicAdd(a.partials + unit, t);
+    }
+    parity ^= 1u;
+}
+
+/* The reduce: a persistent grid over the window's tiles, one block per tile at a time. */
 template <zero_dtype_t DT, int NR>
 __global__ void __launch_bounds__(kBlock) k_reduce(const __grid_constant__ ReduceArgs a)
 {
-    const int N = NR > 0 ? NR : (int)a.n_ranks;
     const float inv = a.st->inv_scale;
-    __shared__ double warp_part[kBlock / 32];
+    __shared__ double warp_part[2][kBlock / 32];
+    uint32_t parity = 0;
     bool bad = false;
-
     for (uint64_t u = blockIdx.x; u < a.unit_count; u += gridDim.x) {
         const uint64_t unit = a.unit_first + u;
-        const uint64_t r = unit / a.tiles_per_rank;
-        const uint64_t j = unit - r * a.tiles_per_rank;
-        // tile j of rank r: the shard cut at the flat multiples of the tile size, so the
-        // 128-bit loads of interior tiles start on 128-byte lines of every array
-        const uint64_t shard_lo = r * a.shard, shard_hi = shard_lo + a.shard;
-        const uint64_t cell = (shard_lo / a.tile + j) * a.tile;
-        uint64_t lo = cell > shard_lo ? cell : shard_lo;
-        uint64_t hi = cell + a.tile < shard_hi ? cell + a.tile : shard_hi;
-        lo = lo > a.begin ? lo : a.begin;
-        hi = hi < a.end ? hi : a.end;
+        uint64_t lo, hi;
+        tile_bounds(a, unit, lo, hi);
         if (lo >= hi)  // a rank's trailing empty slot, or a tile outside the window
             continue;
-
         SumSq acc;
-        for (uint64_t b = (lo & ~7ull) + 8ull * threadIdx.x; b < hi; b += 8ull * kBlock) {
-            float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            const bool full = b >= lo && b + 8 <= hi;  // all 8 elements belong to this tile
-            const uint64_t off = b - a.begin;            // a multiple of 8: begin is
-            if (b + 8 <= a.end) {
-                // the whole group lies inside the window's buffers: 128-bit loads, even
-                // where it straddles a tile edge (the other tile's elements are masked)
-#pragma unroll 1
-                for (int k0 = 0; k0 < N; k0 += kLoadBatch) {
-                    uint4 v[kLoadBatch];
-#pragma unroll
-                    for (int kk = 0; kk < kLoadBatch; ++kk)
-                        if (NR > 0 ? (k0 + kk < NR) : (k0 + kk < N))
-                            v[kk] = ld_stream_v4((const uint16_t*)a.rep[k0 + kk] + off);
-#pragma unroll
-                    for (int kk = 0; kk < kLoadBatch; ++kk)
-                        if (NR > 0 ? (k0 + kk < NR) : (k0 + kk < N))
-                            add8<DT>(s, v[kk]);
-                }
-            } else {  // the window's last, ragged group: element loads inside [lo, hi) only
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const uint64_t i = b + e;
-                    if (i >= lo && i < hi)
-                        for (int k = 0; k < N; ++k)
-                            s[e] = __fadd_rn(s[e], one16<DT>(ld_stream_u16((const uint16_t*)a.rep[k] + off + e)));
-                }
-            }
-            float gv[8], sq[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                gv[e] = sq[e] = __fmul_rn(s[e], inv);
-            uint32_t in = 0xffu;
-            if (b + 8 > a.psi || !full) {  // padding, or a group cut by the tile/window edge
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const uint64_t i = b + e;
-                    if (i >= a.psi)
-                        gv[e] = 0.0f;
-                    if (!(i >= lo && i < hi))
-                        in &= ~(1u << e);
-                    sq[e] = (in >> e & 1u) ? gv[e] : 0.0f;
-                }
-            }
-            if (squares_in_range(sq)) {  // every counted element finite: no overflow
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    acc.add_fast(__fmul_rn(sq[e], kSqScale));
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    bad |= (in >> e & 1u) && not_finite(gv[e]);
-                acc.wide += sumsq_wide(gv[0], gv[1], gv[2], gv[3], gv[4], gv[5], gv[6], gv[7], in);
-            }
-            if (full) {
-                __stcs(reinterpret_cast<float4*>(a.g + b), make_float4(gv[0], gv[1], gv[2], gv[3]));
-                __stcs(reinterpret_cast<float4*>(a.g + b + 4), make_float4(gv[4], gv[5], gv[6], gv[7]));
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    if (in >> e & 1u)
-                        a.g[b + e] = gv[e];
-            }
-        }
-
-        // fixed-order reduction of the tile's partial: pair-arithmetic shuffle tree in fp32,
-        // then fp64 once per warp and the warps in order
-        float ph = acc.hi, pl = acc.lo;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float h2 = __shfl_xor_sync(0xffffffffu, ph, o);
-            const float l2 = __shfl_xor_sync(0xffffffffu, pl, o);
-            pair_add(ph, pl, h2, l2);
-        }
-        double wide = acc.wide;
-        if (__any_sync(0xffffffffu, wide != 0.0)) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-                wide += __shfl_xor_sync(0xffffffffu, wide, o);
-        }
-        if ((threadIdx.x & 31) == 0)
-            warp_part[threadIdx.x >> 5] = ((double)ph + (double)pl) * kSqUnscale + wide;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            double t = 0.0;
-#pragma unroll
-            for (int w = 0; w < kBlock / 32; ++w)
-                t += warp_part[w];
-            a.partials[unit] += t;  // windows of one step meet a tile in stream order
-        }
-        __syncthreads();
+        tile_ldg<DT, NR>(a, inv, lo, hi, acc, bad);
+        tile_done(a, unit, acc, warp_part, parity);
     }
     if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0)
         atomicOr(&a.st->overflow, 1u);
