@@ -6,17 +6,20 @@
  *   1. partition      Psi flat parameters into N equal, padded shards (rank r owns
  *                     flat [r*S, (r+1)*S)), with the per-rank model-state ledger
  *   2. reduce-scatter average the N ranks' fp16/bf16 gradient copies into fp32, remove
- *                     the loss scale, flag inf/NaN, and sum g^2 per rank-local tile
+ *                     the loss scale, flag inf/NaN, and sum g^2 per tile of a shard
  *   3. grad norm      global L2 norm of the averaged gradient, clip coefficient,
  *                     loss-scale update and the skip decision, all on the device
  *   4. AdamW + cast   update the fp32 master / momentum / variance of every shard and
  *                     write each shard's bf16 parameters at its own offset r*S of one
- *                     gathered buffer (the layout the parameter all-gather produces)
+ *                     gathered buffer (the layout the parameter all-gather produces);
+ *                     the state may also live in host memory
+ * plus the per-tensor segment map (which rank owns which piece of each model tensor).
  *
  * Sources (web pages on ZeRO):
  *   [ZW] "【论文解读】ZeRO", wkq9411.github.io: sec. 4(1)-(3) the three partitioning stages,
  *        sec. 6(1)-(2) reduce-scatter / all-gather and the 8-parameter, 4-GPU example
- *   [ZM] "ZeRO 显存优化：ZeRO-1、ZeRO-2 与 ZeRO-3", xiangdong0520.pages.dev: sec. 2-3 ledger
+ *   [ZM] "ZeRO 显存优化：ZeRO-1、ZeRO-2 与 ZeRO-3", xiangdong0520.pages.dev: sec. 2-3 ledger,
+ *        sec. 6 optimizer state offloaded to the CPU
  *   [ZS] operatorworld.com ZeRO optimizer-sharding article: AdamW 16-byte ledger (bf16
  *        weights and gradients), stage flows, communication accounting
  *   [ZO] "3、ZeRO技术概述：ZeRO三个阶段原理与对比", 5688vip.com: stage-2 iteration flow,

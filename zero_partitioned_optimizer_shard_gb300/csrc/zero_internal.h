@@ -14,12 +14,12 @@ namespace zero {
 struct ReduceArgs {
     const void* rep[ZERO_MAX_KERNEL_RANKS];  // replica k, pointing at flat `begin`
     float* g;                                // flat fp32 gradient, psi_padded
-    double* partials;                        // one fp64 slot per rank-local tile
+    double* partials;                        // one fp64 slot per tile (shards cut on the flat T grid)
     zero_step_state_t* st;
     uint64_t begin, end;                     // window [begin, end)
     uint64_t psi, shard;
     uint64_t tiles_per_rank;
-    uint64_t unit_first, unit_count;         // rank-local tiles that meet the window
+    uint64_t unit_first, unit_count;         // tile slots that meet the window
     uint32_t n_ranks;
     uint32_t tile;
 };
