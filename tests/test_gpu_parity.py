@@ -189,6 +189,39 @@ def test_sum_of_squares_at_the_range_edges(case):
     gpu.check_guards()
 
 
+@pytest.mark.parametrize("n", [2, 8, 64])
+def test_sharded_step_equals_unsharded_step(n):
+    """The sharding identity of the ZeRO walkthrough (sec. 6(2): each rank updates its
+    own partition, the all-gather reassembles [p0' ... p7']) on the GPU alone: N identical
+    gradient copies average exactly to the copy, so the N-rank sharded step must equal
+    the one-rank step on that copy bit for bit (clipping off, so no norm rounding enters;
+    then with clipping on, within the norm's summation-order rounding)."""
+    psi = 3 * 8192 + 1234
+    for clip in (0.0, 1.0):
+        hp = z.hparams(max_grad_norm=clip)
+        runs = []
+        for ranks in (n, 1):
+            wl = replace(W.scaled(W.C2, psi, steps=2), n_ranks=ranks)
+            gpu = GpuRun(wl, hp=hp)
+            for step in (1, 2):
+                gpu._fill(gpu.reps[0], wl.grad_out, wl.grad_kind, wl.grad_key(step, 0), wl.grad_sigma)
+                for k in range(1, ranks):
+                    gpu.reps[k].copy_(gpu.reps[0])
+                z.zero_step(gpu.lay, gpu.hp, z.ZERO_BF16, gpu.bucket_ptrs(), gpu.g, gpu.partials,
+                            gpu.master, gpu.m, gpu.v, gpu.out, gpu.st)
+            gpu.check_guards()
+            runs.append((gpu.state(), {k: v[:psi] for k, v in gpu.arrays().items()}))
+        (sa, a), (sb, b) = runs
+        assert sa.t == sb.t == 2
+        if clip == 0.0:
+            assert sa.clip_coef == sb.clip_coef == 1.0
+            for k in a:
+                assert np.array_equal(a[k].view(np.uint8), b[k].view(np.uint8)), (n, k)
+        else:
+            assert abs(sa.norm - sb.norm) <= 1e-12 * sb.norm
+            assert_state_close(dict(a, g=b["g"]), b, psi, exact_expected=sa.clip_coef == sb.clip_coef)
+
+
 def test_bf16_static_scale_overflow_skips_without_backoff():
     wl = W.scaled(W.C2, 30_000, steps=1)
     gpu = GpuRun(wl)
