@@ -35,6 +35,9 @@
  *   oracle_step           identity: the sharded step equals the unsharded step on the
  *                         averaged gradient ([ZS]: ZeRO-1 only splits the all-reduce);
  *                         independent of the stage; skip leaves every byte untouched
+ *   oracle_segment_map    hand-worked maps (one is the [ZW] sec. 6(2) example with one
+ *                         tensor per parameter); a numpy run-length derivation; the count
+ *                         (non-empty tensors + boundaries strictly inside a tensor)
  * Parity unpinned: none beyond the readings listed with each function (the AdamW form,
  * the clip epsilon and the scaler policy are chosen readings; their closed forms pin the
  * code to the chosen reading, not the reading to the pages).
