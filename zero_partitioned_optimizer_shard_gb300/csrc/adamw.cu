@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(kBlock, 1) k_adamw(const __grid_constant__ Ada
 {
     extern __shared__ __align__(128) float ring[];  // kStages x {g, master, m, v} x kChunk
     __shared__ __align__(8) uint64_t full[kStages];
+    grid_dependency_wait();
     const zero_step_state_t* st = a.st;
     if (st->skip)
         return;
@@ -229,6 +230,7 @@ constexpr int kHostUnroll = 2;
 template <bool F16>
 __global__ void __launch_bounds__(kBlock) k_adamw_host_state(const __grid_constant__ AdamwArgs a)
 {
+    grid_dependency_wait();
     const zero_step_state_t* st = a.st;
     if (st->skip)
         return;
@@ -325,11 +327,9 @@ cudaError_t launch_adamw(const AdamwArgs& a, cudaStream_t s)
     const uint64_t want = chunks > tail_blocks ? chunks : tail_blocks;
     const uint64_t cap = (uint64_t)sm_count();  // one 192 KiB block per SM
     const unsigned grid = (unsigned)(want < cap ? want : cap);
-    if (a.out_f16)
-        k_adamw<true><<<grid > 0 ? grid : 1, kBlock, kSmemBytes, s>>>(a);
-    else
-        k_adamw<false><<<grid > 0 ? grid : 1, kBlock, kSmemBytes, s>>>(a);
-    return cudaGetLastError();
+    const dim3 g(grid > 0 ? grid : 1), b(kBlock);
+    return a.out_f16 ? launch_pdl(k_adamw<true>, g, b, kSmemBytes, s, a)
+                     : launch_pdl(k_adamw<false>, g, b, kSmemBytes, s, a);
 }
 
 cudaError_t launch_adamw_host_state(const AdamwArgs& a, cudaStream_t s)
@@ -340,11 +340,8 @@ cudaError_t launch_adamw_host_state(const AdamwArgs& a, cudaStream_t s)
     uint64_t want = ((want_threads > tail ? want_threads : tail) + kBlock - 1) / kBlock;
     const uint64_t cap = (uint64_t)sm_count() * 3;  // 80 registers x 256 threads: 3 blocks per SM
     const unsigned grid = (unsigned)(want < cap ? (want > 0 ? want : 1) : cap);
-    if (a.out_f16)
-        k_adamw_host_state<true><<<grid, kBlock, 0, s>>>(a);
-    else
-        k_adamw_host_state<false><<<grid, kBlock, 0, s>>>(a);
-    return cudaGetLastError();
+    return a.out_f16 ? launch_pdl(k_adamw_host_state<true>, dim3(grid), dim3(kBlock), 0, s, a)
+                     : launch_pdl(k_adamw_host_state<false>, dim3(grid), dim3(kBlock), 0, s, a);
 }
 
 }  // namespace zero

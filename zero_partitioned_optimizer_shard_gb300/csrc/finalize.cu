@@ -44,6 +44,7 @@ __global__ void __launch_bounds__(kFinThreads) k_finalize(const __grid_constant_
     __shared__ double red[kFinThreads / 32][kBatch];
     __shared__ double rank_sum[ZERO_MAX_KERNEL_RANKS];
     __shared__ int is_last;
+    grid_dependency_wait();
     const uint32_t N = a.n_ranks;
     const uint64_t tpr = a.tiles_per_rank;
     const uint64_t chunk = (tpr + gridDim.x - 1) / gridDim.x;
@@ -211,8 +212,7 @@ cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s)
 {
     const uint64_t blocks = a.tiles_per_rank < (uint64_t)kFinMaxBlocks ? a.tiles_per_rank
                                                                        : (uint64_t)kFinMaxBlocks;
-    k_finalize<<<(unsigned)(blocks > 0 ? blocks : 1), kFinThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k_finalize, dim3((unsigned)(blocks > 0 ? blocks : 1)), dim3(kFinThreads), 0, s, a);
 }
 
 cudaError_t launch_state_init(const InitArgs& a, cudaStream_t s)

@@ -307,6 +307,7 @@ __device__ __forceinline__ void tile_done(const ReduceArgs& a, uint64_t unit, co
 template <zero_dtype_t DT, int NR>
 __global__ void __launch_bounds__(kBlock) k_reduce(const __grid_constant__ ReduceArgs a)
 {
+    grid_dependency_wait();
     const float inv = a.st->inv_scale;
     __shared__ double warp_part[2][kBlock / 32];
     uint32_t parity = 0;
@@ -341,8 +342,7 @@ cudaError_t launch_t(const ReduceArgs& a, cudaStream_t s)
     const unsigned grid = (unsigned)(a.unit_count < cap ? a.unit_count : cap);
     if (grid == 0)
         return cudaSuccess;
-    k_reduce<DT, NR><<<grid, kBlock, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k_reduce<DT, NR>, dim3(grid), dim3(kBlock), 0, s, a);
 }
 
 template <zero_dtype_t DT>

@@ -53,6 +53,33 @@ struct InitArgs {
     uint32_t dynamic, growth_interval, n_ranks;
 };
 
+/* Programmatic dependent launch (Hopper/Blackwell): the kernel may be launched while the
+ * preceding kernel in the stream is still finishing, so the launch itself overlaps that
+ * kernel's tail.  Every kernel launched this way executes grid_dependency_wait() as its
+ * first instruction, which returns once the preceding grid has completed and its memory
+ * is visible: nothing runs early, so stream order holds whatever the preceding kernel is. */
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 /* Launchers (enqueue only; return the launch's cudaError_t). */
 cudaError_t launch_reduce(const ReduceArgs& a, zero_dtype_t dtype, cudaStream_t s);
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s);
