@@ -13,19 +13,21 @@
  * (cap 2^24).  Everything stays on the device, so a training loop never waits for the
  * host between steps.
  *
- * Block 0 starts with everything that does not need the norm (skip, t, the scaler, the
+ * One extra block runs everything that does not need the norm (skip, t, the scaler, the
  * bias corrections with their two fp64 pow, which GB300's slow fp64 pipe makes the
- * longest chain), split over three warps; that overlaps the other blocks' sums.  The
- * last block then only takes the square root and the clip coefficient.
+ * longest chain), split over three warps, beside the sums.  The last block to arrive
+ * then only takes the square root and the clip coefficient.
  *
- * The sum is spread over up to 128 blocks (GB300's fp64 rate is a few operations per SM
- * per clock, so one block summing every tile partial would take tens of microseconds).
- * Block b sums the fixed chunk b of every rank's tile partials (a fixed tree per block),
- * leaves that chunk's sum in the chunk's first slot and zeroes the rest; the last block
- * to arrive (an atomic counter in the step state, no waiting) adds the chunk sums of
- * each rank in order, then the ranks in order, and runs the scalar logic.  The chunking
- * depends only on N and the tile count, so the result is the same on any GPU.  All
- * partial slots end at zero, ready for the next step's reduce windows.
+ * The sum is spread over up to 128 blocks, one warp per rank in each: block b sums the
+ * fixed chunk b of every rank's tile partials (each lane in order, then a fixed shuffle
+ * tree), leaves that chunk's sum in the chunk's first slot and zeroes the rest; the last
+ * block to arrive (an atomic counter in the step state, no waiting) adds the chunk sums
+ * of each rank in order, then the ranks in order.  GB300's fp64 rate is a few
+ * operations per SM per clock, so the work is shaped to need few of them: one
+ * accumulator per warp (eight per warp measured 7 us at a million parameters, against
+ * about 1.5 us now).  The chunking depends only on N and the tile count, so the result
+ * is the same on any GPU.  All partial slots end at zero, ready for the next step's
+ * reduce windows.
  */
 #include "zero_internal.h"
 
@@ -35,29 +37,25 @@ namespace zero {
 namespace {
 
 constexpr int kFinThreads = 256;
-constexpr int kFinMaxBlocks = 128;
-
-constexpr int kBatch = 8;  // ranks summed together by one block pass
+constexpr int kFinWarps = kFinThreads / 32;
+constexpr int kFinMaxBlocks = 128;  // summing blocks; one more block runs the scalar logic
 
 __global__ void __launch_bounds__(kFinThreads) k_finalize(const __grid_constant__ FinalizeArgs a)
 {
-    __shared__ double red[kFinThreads / 32][kBatch];
     __shared__ double rank_sum[ZERO_MAX_KERNEL_RANKS];
     __shared__ int is_last;
     grid_dependency_wait();
     const uint32_t N = a.n_ranks;
     const uint64_t tpr = a.tiles_per_rank;
-    const uint64_t chunk = (tpr + gridDim.x - 1) / gridDim.x;
-    const uint64_t j0 = (uint64_t)blockIdx.x * chunk;
-    const uint64_t j1 = j0 + chunk < tpr ? j0 + chunk : tpr;
+    const unsigned n_sum = gridDim.x - 1;  // blocks 0 .. n_sum-1 sum; block n_sum: scalars
+    const uint64_t chunk = (tpr + n_sum - 1) / n_sum;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     zero_step_state_t* st = a.st;
 
-    // Block 0 first does everything that does not need the norm, in three warps at once.
-    // It depends only on the overflow flag, which every reduce window has already set;
-    // the fp64 work (two pow) overlaps the other blocks' partial sums.  Block 0's arrival
-    // below publishes it to the last block.
-    if (blockIdx.x == 0) {
+    if (blockIdx.x == n_sum) {
+        // Everything that does not need the norm, in three warps at once, beside the sums
+        // (the two fp64 pow are the longest chain on GB300's slow fp64 pipe).  It depends
+        // only on t and on the overflow flag, which every reduce window has already set.
         __shared__ uint32_t s_t, s_overflow;
         if (threadIdx.x == 0) {
             s_t = st->t;
@@ -95,40 +93,25 @@ __global__ void __launch_bounds__(kFinThreads) k_finalize(const __grid_constant_
             st->loss_scale = L;
             st->inv_scale = (float)(1.0 / ((double)N * (double)L));
         }
-    }
-
-    // this block's chunk of every rank, kBatch ranks at a time: each thread sums its
-    // slots in order, a shuffle tree folds each warp, warps are folded in order
-    for (uint32_t r0 = 0; r0 < N; r0 += kBatch) {
-        double acc[kBatch];
-#pragma unroll
-        for (int q = 0; q < kBatch; ++q)
-            acc[q] = 0.0;
-        for (uint64_t j = j0 + threadIdx.x; j < j1; j += kFinThreads) {
-#pragma unroll
-            for (int q = 0; q < kBatch; ++q)
-                if (r0 + q < N) {
-                    double* p = a.partials + (uint64_t)(r0 + q) * tpr + j;
-                    acc[q] += *p;
-                    *p = 0.0;
-                }
-        }
-#pragma unroll
-        for (int q = 0; q < kBatch; ++q) {
+    } else {
+        // this block's chunk [j0, j1) of every rank's tile partials: one warp per rank,
+        // each lane adds its slots in order, a fixed shuffle tree folds the warp.  The
+        // chunk's sum is left in its first slot; the other slots are zeroed.
+        const uint64_t j0 = (uint64_t)blockIdx.x * chunk;
+        const uint64_t j1 = j0 + chunk < tpr ? j0 + chunk : tpr;
+        for (uint32_t r = w; r < N; r += kFinWarps) {
+            double* p = a.partials + (uint64_t)r * tpr;
+            double acc = 0.0;
+            for (uint64_t j = j0 + lane; j < j1; j += 32) {
+                acc += p[j];
+                p[j] = 0.0;
+            }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1)
-                acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
-            if (lane == 0)
-                red[w][q] = acc[q];
+                acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (lane == 0 && j0 < j1)
+                p[j0] = acc;
         }
-        __syncthreads();
-        if (threadIdx.x < kBatch && r0 + threadIdx.x < N && j0 < j1) {
-            double t = 0.0;
-            for (int ww = 0; ww < kFinThreads / 32; ++ww)
-                t += red[ww][threadIdx.x];
-            a.partials[(uint64_t)(r0 + threadIdx.x) * tpr + j0] = t;
-        }
-        __syncthreads();
     }
     __threadfence();
     __syncthreads();
@@ -141,7 +124,7 @@ __global__ void __launch_bounds__(kFinThreads) k_finalize(const __grid_constant_
 
     // the last block: chunk sums in order per rank (one warp per rank), ranks in order
     const uint64_t n_chunks = (tpr + chunk - 1) / chunk;  // at most kFinMaxBlocks = 4 x 32
-    for (uint32_t r = w; r < N; r += kFinThreads / 32) {
+    for (uint32_t r = w; r < N; r += kFinWarps) {
         double* p = a.partials + (uint64_t)r * tpr;
         double v[kFinMaxBlocks / 32];
 #pragma unroll
@@ -171,7 +154,7 @@ __global__ void __launch_bounds__(kFinThreads) k_finalize(const __grid_constant_
     for (uint32_t r = 0; r < N; ++r)
         total += rank_sum[r];
 
-    // the skip decision and the rest were written by block 0 before it arrived
+    // the skip decision and the rest were written by the scalar block before it arrived
     st->arrivals = 0;
     const double norm = sqrt(total);
     st->sumsq = total;
@@ -210,9 +193,11 @@ __global__ void k_state_init(const __grid_constant__ InitArgs a)
 
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s)
 {
-    const uint64_t blocks = a.tiles_per_rank < (uint64_t)kFinMaxBlocks ? a.tiles_per_rank
-                                                                       : (uint64_t)kFinMaxBlocks;
-    return launch_pdl(k_finalize, dim3((unsigned)(blocks > 0 ? blocks : 1)), dim3(kFinThreads), 0, s, a);
+    uint64_t blocks = a.tiles_per_rank < (uint64_t)kFinMaxBlocks ? a.tiles_per_rank
+                                                                 : (uint64_t)kFinMaxBlocks;
+    if (blocks == 0)
+        blocks = 1;
+    return launch_pdl(k_finalize, dim3((unsigned)blocks + 1), dim3(kFinThreads), 0, s, a);
 }
 
 cudaError_t launch_state_init(const InitArgs& a, cudaStream_t s)
