@@ -296,7 +296,9 @@ def test_checkpoint_resume_bitwise():
 
 
 @pytest.mark.parametrize("psi,n,stage", [(1 << 20, 2, 1), ((1 << 20) + 1, 64, 3), (1 << 22, 16, 2),
-                                         ((1 << 22) + 1, 8, 1), (1 << 21, 4, 3)])
+                                         ((1 << 22) + 1, 8, 1), (1 << 21, 4, 3),
+                                         (3 * (1 << 20) + 5, 3, 2), ((1 << 21) + 7, 7, 2),
+                                         ((1 << 21) + 3, 1, 2)])
 def test_sweep_points_all_elements(psi, n, stage):
     """Bandwidth-sweep points (bf16 ~N(0,1e-3)) small enough for the oracle, every element."""
     _run_pair(W.sweep_point(psi, n, stage, steps=2), 2)
