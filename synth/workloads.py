@@ -136,6 +136,25 @@ def sweep_point(psi: int, n_ranks: int, stage: int, steps: int = 1) -> Workload:
                     synth.NORMAL, 1e-3, 1.0, False, steps, seed=4, random_moments=True)
 
 
+SWEEP_PARITY_POINTS = (
+    [(1 << 20, n, st) for n in (2, 4, 8, 16, 64) for st in (1, 2, 3)]
+    + [((1 << 20) + 1, n, 2) for n in (2, 4, 8, 16, 64)]
+    + [(1 << 24, n, 2) for n in (2, 4, 8, 16, 64)]
+    + [((1 << 24) + 1, n, 2) for n in (2, 4, 8, 16, 64)])
+
+
+def sweep_name(psi: int, n_ranks: int, stage: int) -> str:
+    return f"C4-{psi}-{n_ranks}-{stage}"
+
+
+def by_name(name: str) -> Workload:
+    """C1, C2, C3, C5, or a sweep point "C4-<psi>-<N>-<stage>" (two steps)."""
+    if name.startswith("C4-"):
+        _, psi, n, st = name.split("-")
+        return sweep_point(int(psi), int(n), int(st), steps=2)
+    return globals()[name]
+
+
 def scaled(w: Workload, psi: int, steps: int | None = None, name: str | None = None) -> Workload:
     """The same recipe at another size (small parity cases of a large workload)."""
     from dataclasses import replace

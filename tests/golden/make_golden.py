@@ -10,6 +10,8 @@ step's scalars.  Those scalars are all a full-size parity test needs from the or
 the AdamW update of any sampled element follows from them and its own inputs.
 
 Usage: python tests/golden/make_golden.py C2 [C3 C5 ...]   (uses every host core)
+       python tests/golden/make_golden.py sweep      (every bandwidth-sweep point up to
+                                                      2^24+1 parameters, into golden/sweep/)
 """
 from __future__ import annotations
 
@@ -36,7 +38,7 @@ def _chunk_job(args):
     import oracle
     import synth
     from synth import workloads as W
-    wl = getattr(W, wl_name)
+    wl = W.by_name(wl_name)
     orc = oracle.load()
     lay = orc.partition(wl.psi, wl.n_ranks, wl.stage, 1, 0)
     S = lay.shard
@@ -60,7 +62,7 @@ def _chunk_job(args):
 def run(wl_name: str, procs: int) -> str:
     import oracle
     from synth import workloads as W
-    wl = getattr(W, wl_name)
+    wl = W.by_name(wl_name)
     orc = oracle.load()
     lay = orc.partition(wl.psi, wl.n_ranks, wl.stage, 1, 0)
     S = lay.shard
@@ -92,7 +94,8 @@ def run(wl_name: str, procs: int) -> str:
                          f"{norm.hex()} {float(np.float32(c)).hex()} {sc.loss_scale!r}")
             print(f"[{wl_name}] step {step}: L={L} ov={overflow} norm={norm:.9g} c={c:.9g} "
                   f"t={sc.t} ({time.time() - t0:.0f}s)", flush=True)
-    path = os.path.join(ROOT, "tests", "golden", f"{wl_name}_steps.txt")
+    path = golden_path(wl_name)
+    os.makedirs(os.path.dirname(path), exist_ok=True)
     with open(path, "w", encoding="utf-8") as f:
         f.write(f"# Oracle per-step results for workload {wl_name}: {wl.name}\n")
         f.write("# Written by tests/golden/make_golden.py (CPU oracle + seeded generator only).\n")
@@ -104,9 +107,14 @@ def run(wl_name: str, procs: int) -> str:
     return path
 
 
+def golden_path(wl_name: str) -> str:
+    sub = ("sweep",) if wl_name.startswith("C4-") else ()
+    return os.path.join(ROOT, "tests", "golden", *sub, f"{wl_name}_steps.txt")
+
+
 def load(wl_name: str):
     """Rows of a golden file as dicts (used by the full-size parity tests)."""
-    path = os.path.join(ROOT, "tests", "golden", f"{wl_name}_steps.txt")
+    path = golden_path(wl_name)
     rows = []
     with open(path, encoding="utf-8") as f:
         for line in f:
@@ -122,4 +130,9 @@ def load(wl_name: str):
 if __name__ == "__main__":
     procs = int(os.environ.get("GOLDEN_PROCS", os.cpu_count() or 1))
     for name in sys.argv[1:]:
-        print(run(name, procs))
+        if name == "sweep":
+            from synth import workloads as W
+            for point in W.SWEEP_PARITY_POINTS:
+                print(run(W.sweep_name(*point), procs))
+        else:
+            print(run(name, procs))

@@ -1,4 +1,5 @@
-"""Full-size workloads on the GPU vs the oracle (needs a GB300 and ~130 GB of HBM for C3).
+"""Full-size workloads and sweep points on the GPU vs the oracle (needs a GB300 and ~130 GB
+of HBM for C3).
 
 The GPU runs the whole workload through the C ABI exactly as the benchmark launches it.
 The oracle's per-step scalars (norm, clip coefficient, overflow, skip, t, loss scale) come
@@ -127,7 +128,7 @@ def _compare(gpu, so, idx, step):
 
 
 def _run(name):
-    wl = getattr(W, name)
+    wl = W.by_name(name)
     rows = golden.load(name)
     assert len(rows) == wl.steps
     dev = torch.device("cuda:0")
@@ -202,7 +203,7 @@ def _run(name):
 
 
 def _need(name):
-    path = os.path.join(os.path.dirname(__file__), "golden", f"{name}_steps.txt")
+    path = golden.golden_path(name)
     if not os.path.exists(path):
         pytest.skip(f"golden file for {name} not generated")
 
@@ -226,3 +227,14 @@ def test_c5_fp16_stress_full_size_50_steps():
     assert sum(r["skipped"] for r in rows) >= 7  # injections, plus natural fp16 overflow
     assert rows[0]["loss_scale"] == 65536.0 and min(r["clip_coef"] for r in rows) < 1.0
     _run("C5")
+
+
+@pytest.mark.parametrize("point", W.SWEEP_PARITY_POINTS, ids=lambda p: W.sweep_name(*p))
+def test_sweep_point_vs_golden(point):
+    """Every bandwidth-sweep point up to 2^24+1 parameters (N = 2 .. 64; stages 1-3 at
+    2^20): the norm and scalars against the oracle's golden file, elements on windows at
+    every shard's start, middle and end and at random places, two steps."""
+    name = W.sweep_name(*point)
+    _need(name)
+    _run(name)
+
