@@ -143,15 +143,26 @@ SWEEP_PARITY_POINTS = (
     + [((1 << 24) + 1, n, 2) for n in (2, 4, 8, 16, 64)])
 
 
+# above 2^24 the sweep points are checked by sampling: a subset of N, elements on windows
+SWEEP_SAMPLED_POINTS = [(psi, n, 2) for k in (27, 29, 31) for psi in (1 << k, (1 << k) + 1)
+                        for n in (2, 8, 64)]
+
+
 def sweep_name(psi: int, n_ranks: int, stage: int) -> str:
     return f"C4-{psi}-{n_ranks}-{stage}"
 
 
 def by_name(name: str) -> Workload:
-    """C1, C2, C3, C5, or a sweep point "C4-<psi>-<N>-<stage>" (two steps)."""
+    """C1, C2, C3, C5, or a sweep point "C4-<psi>-<N>-<stage>" (two steps; 2^27-element
+    buckets when the N gradient copies would not fit beside the state in ~200 GB)."""
     if name.startswith("C4-"):
         _, psi, n, st = name.split("-")
-        return sweep_point(int(psi), int(n), int(st), steps=2)
+        from dataclasses import replace
+        wl = sweep_point(int(psi), int(n), int(st), steps=2)
+        P = -(-wl.psi // wl.n_ranks) * wl.n_ranks
+        if wl.n_ranks * P * 2 + 18 * P > 200e9:
+            wl = replace(wl, bucket_elems=1 << 27)
+        return wl
     return globals()[name]
 
 

@@ -12,6 +12,8 @@ the AdamW update of any sampled element follows from them and its own inputs.
 Usage: python tests/golden/make_golden.py C2 [C3 C5 ...]   (uses every host core)
        python tests/golden/make_golden.py sweep      (every bandwidth-sweep point up to
                                                       2^24+1 parameters, into golden/sweep/)
+       python tests/golden/make_golden.py sweep-sampled   (2^27, 2^29, 2^31 and +1 at
+                                                      N = 2, 8, 64)
 """
 from __future__ import annotations
 
@@ -130,9 +132,10 @@ def load(wl_name: str):
 if __name__ == "__main__":
     procs = int(os.environ.get("GOLDEN_PROCS", os.cpu_count() or 1))
     for name in sys.argv[1:]:
-        if name == "sweep":
+        if name in ("sweep", "sweep-sampled"):
             from synth import workloads as W
-            for point in W.SWEEP_PARITY_POINTS:
+            points = W.SWEEP_PARITY_POINTS if name == "sweep" else W.SWEEP_SAMPLED_POINTS
+            for point in points:
                 print(run(W.sweep_name(*point), procs))
         else:
             print(run(name, procs))

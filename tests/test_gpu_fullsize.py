@@ -238,3 +238,18 @@ def test_sweep_point_vs_golden(point):
     _need(name)
     _run(name)
 
+
+@pytest.mark.parametrize("point", W.SWEEP_SAMPLED_POINTS, ids=lambda p: W.sweep_name(*p))
+def test_sweep_point_sampled_vs_golden(point):
+    """Sweep points above 2^24 (2^27, 2^29, 2^31 and +1; N = 2, 8, 64; the largest in
+    2^27-element buckets): scalars against the golden file, elements on sampled windows."""
+    name = W.sweep_name(*point)
+    _need(name)
+    wl = W.by_name(name)
+    P = -(-wl.psi // wl.n_ranks) * wl.n_ranks
+    need = 18 * P + 2 * wl.n_ranks * (wl.bucket_elems or P)
+    free, _ = torch.cuda.mem_get_info()
+    if free < need * 1.1:
+        pytest.skip(f"{name} needs ~{need / 1e9:.0f} GB of free HBM, {free / 1e9:.0f} GB free")
+    _run(name)
+
