@@ -315,29 +315,36 @@ def test_stages_share_arithmetic():
             assert np.array_equal(o[k].view(np.uint8), outs[0][k].view(np.uint8))
 
 
-def test_step_host_equals_device_path():
+@pytest.mark.parametrize("recipe,steps", [("C2", 2), ("C5", 8)])
+def test_step_host_equals_device_path(recipe, steps):
     """zero_step_host (gradients in pinned host memory, bucketed H2D ring) gives the same
-    bits as zero_step on device-resident gradients."""
-    wl = W.scaled(W.C2, 3 * 65536 + 40, steps=2)
+    bits as zero_step on device-resident gradients; with the fp16 dynamic-scale recipe
+    the injected inf at step 7 is skipped the same way."""
+    wl = W.scaled(getattr(W, recipe), 3 * 65536 + 40, steps=steps)
+    dt = z.ZERO_F16 if wl.grad_dtype == "f16" else z.ZERO_BF16
     dev = GpuRun(wl, bucket_elems=65536)
     host = GpuRun(wl, bucket_elems=65536)
     P = host.lay.psi_padded
     staging = torch.empty(2 * wl.n_ranks * 65536, dtype=torch.int16, device="cuda")
     copy_stream = torch.cuda.Stream()
     hstate = torch.empty(z.STATE_BYTES, dtype=torch.uint8).pin_memory()
-    for s in (1, 2):
+    skipped = 0
+    for s in range(1, steps + 1):
         dev.step(s)
         host.gen_grads(s)
         hreps = [r.cpu().pin_memory() for r in host.reps]
         for r in host.reps:
             r.fill_(0x7F7F)  # the device copies must not be read
-        z.zero_step_host(host.lay, host.hp, z.ZERO_BF16, hreps, staging, staging.numel() * 2,
+        z.zero_step_host(host.lay, host.hp, dt, hreps, staging, staging.numel() * 2,
                          host.g, host.partials, host.master, host.m, host.v, host.out, host.st,
                          hstate, None, copy_stream)
         torch.cuda.synchronize()
         hs = z.StepState.from_buffer_copy(hstate.numpy().tobytes())
         ds = dev.state()
-        assert hs.norm == ds.norm and hs.t == ds.t == s
+        assert (hs.skip, hs.t, hs.loss_scale) == (ds.skip, ds.t, ds.loss_scale)
+        assert hs.norm == ds.norm or (hs.skip and ds.skip)
+        skipped += hs.skip
+    assert hs.t == steps - skipped and skipped >= (1 if recipe == "C5" else 0)
     x, y = dev.arrays(), host.arrays()
     for k in x:
         assert np.array_equal(x[k].view(np.uint8), y[k].view(np.uint8)), k
