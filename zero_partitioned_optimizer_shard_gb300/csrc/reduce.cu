@@ -18,8 +18,8 @@
  *    elements: each shard cut at the flat multiples of 8192, so interior tiles start on
  *    128-byte lines of every array even when the shard size is not a multiple of 64
  *    (misaligned warps touched one extra line per load: 4% of the kernel's time at the
- *    GPT-2 size); one block owns a tile, so its partial is written by exactly one block
- *    per launch (deterministic, no atomics on the data path);
+ *    GPT-2 size); one block owns a tile, so its partial gets exactly one add per launch
+ *    (deterministic; the add is an fp64 atomicAdd only so that it need not wait);
  *  - every thread moves 8 elements per replica with one 128-bit non-coherent load that
  *    skips L1 (ld.global.nc.L1::no_allocate.v4), all N replica loads issued before the
  *    sum, and writes g with streaming 128-bit stores;
@@ -28,7 +28,9 @@
  *    per-element fp64 (GB300's fp64 rate is a small fraction of fp32), then folded into
  *    fp64 once per thread and reduced in a fixed shuffle tree per tile;
  *  - groups with an element outside the pair arithmetic's exact range (below 2^-74 or
- *    at least 2^34 in magnitude, or not finite) are summed in fp64 instead.
+ *    at least 2^34 in magnitude, or not finite) are summed in fp64 instead;
+ *  - launched with programmatic dependent launch (the kernel waits for the preceding grid
+ *    first thing), so its launch overlaps the previous kernel's tail.
  */
 #include "zero_internal.h"
 
