@@ -113,14 +113,19 @@ __global__ void __launch_bounds__(kFinThreads) k_finalize(const __grid_constant_
                 p[j0] = acc;
         }
     }
-    __threadfence();
+    // arrival: the block's writes are ordered before the count by the barrier and one
+    // release fence of thread 0 (fences in every thread stalled the kernel on membar);
+    // the last block to arrive acquires before reading the other blocks' chunk sums
     __syncthreads();
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0) {
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
         is_last = atomicAdd(&a.st->arrivals, 1u) == gridDim.x - 1;
+        if (is_last)
+            asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    }
     __syncthreads();
     if (!is_last)
         return;
-    __threadfence();
 
     // the last block: chunk sums in order per rank (one warp per rank), ranks in order
     const uint64_t n_chunks = (tpr + chunk - 1) / chunk;  // at most kFinMaxBlocks = 4 x 32
