@@ -439,9 +439,14 @@ def run_sweep(args):
                     z.zero_step_state_init(lay, 1.0, False, 1000, st, partials, stream)
                     ptrs = [reps[kk].data_ptr() for b in range(lay.n_buckets) for kk in range(N)]
                     hp = z.hparams()
+                    # N = 2 with resident copies: re-read the copies in AdamW (26 + 4N = 34
+                    # bytes per parameter) instead of writing and re-reading g (34 + 2N = 38)
+                    reread = N == 2 and not bucketed and not args.sweep_materialise
+                    g_arg = None if reread else bufs["g"]
+                    moved = 26 + 4 * N if reread else 34 + 2 * N
 
                     def step():
-                        z.zero_step(lay, hp, z.ZERO_BF16, ptrs, bufs["g"], partials, bufs["master"],
+                        z.zero_step(lay, hp, z.ZERO_BF16, ptrs, g_arg, partials, bufs["master"],
                                     bufs["m"], bufs["v"], out, st, stream)
 
                     for _ in range(3):
@@ -469,11 +474,13 @@ def run_sweep(args):
                     print(json.dumps({
                         "sweep": True, "psi": psi, "n_ranks": N, "stage": stage,
                         "mode": "bucketed 2^27" if bucketed else "resident", "steps": steps,
+                        "schedule": "re-read copies" if reread else "materialise g",
                         "launch": "cuda graph replay" if args.graph else "direct",
                         "ms_per_step": ms, "params_per_s": psi / (ms / 1e3),
                         "gbs_at_26p2n": (26 + 2 * N) * P / (ms / 1e3) / 1e9,
-                        "gbs_moved_34p2n": (34 + 2 * N) * P / (ms / 1e3) / 1e9,
-                        "l2": "L2-resident regime" if (34 + 2 * N) * P < 129e6 else "HBM"}), flush=True)
+                        "bytes_moved_per_param": moved,
+                        "gbs_moved": moved * P / (ms / 1e3) / 1e9,
+                        "l2": "L2-resident regime" if moved * P < 129e6 else "HBM"}), flush=True)
                     del reps, bufs, out, partials, st, graph
                     torch.cuda.empty_cache()
     return 0
@@ -716,6 +723,8 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="bandwidth sweep over psi and N (one JSON line per point)")
     ap.add_argument("--sweep-k", default="20,24,27,29,30,31")
+    ap.add_argument("--sweep-materialise", action="store_true",
+                    help="sweep: write and re-read g at N = 2 too (default: re-read the copies)")
     ap.add_argument("--graph", action="store_true", help="sweep: replay each step from a CUDA graph")
     ap.add_argument("--producer-blocks", type=int, default=2,
                     help="overlap: generator blocks per SM for the synthetic backward")

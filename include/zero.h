@@ -59,7 +59,8 @@ typedef struct CUstream_st* zero_stream_t;
 #define ZERO_EALIGN (-2)   /* pointer or window not aligned as required */
 #define ZERO_ENOMEM (-3)   /* caller-provided buffer too small */
 #define ZERO_ECUDA (-4)    /* CUDA launch or copy failed; see zero_last_cuda_error() */
-#define ZERO_ETIMEOUT (-5) /* reserved for bounded device waits (none wait today) */
+#define ZERO_ETIMEOUT (-5) /* reserved; a device wait that gives up records 1 in the step
+                              state's error word instead */
 
 typedef enum zero_dtype { ZERO_F16 = 1, ZERO_BF16 = 2 } zero_dtype_t;
 
@@ -122,10 +123,11 @@ typedef struct zero_step_state {
     uint32_t n_ranks;
     uint32_t n_steps;       /* finalised steps, applied or skipped */
     uint32_t n_skipped;
-    uint32_t error;         /* device error word, 0 = none (reserved) */
+    uint32_t error;         /* device error word: 0 = none; 1 = a bounded wait gave up */
     uint32_t arrivals;      /* internal to zero_grad_norm: its blocks that have finished
                                (0 between steps; keep it 0 when writing a state) */
-    uint32_t reserved[11];
+    float inv_scale_used;   /* the inv_scale the last finalised step's reduce used */
+    uint32_t reserved[10];
 } zero_step_state_t;        /* 128 bytes */
 
 /* -------------------------------------------------------------------------------------
@@ -288,6 +290,13 @@ int zero_adamw_cast_gather_host_state(const zero_layout_t* layout,
  *              replicas[b*N + k] holds rank k's gradient for flat
  *              [b*W, min((b+1)*W, psi_padded)).  With n_buckets = 1 these are simply
  *              the N full gradient copies.
+ *   g          as in zero_reduce_shard_unscale, or NULL when N = 2 and n_buckets = 1:
+ *              the re-reading schedule.  Clipping needs the global norm before any
+ *              update, so an exact step either writes the fp32 g and reads it back
+ *              (34 + 2N bytes per parameter) or reads the N copies twice (26 + 4N); at
+ *              N = 2 the second moves 34 instead of 38 B.  The reduce then stores no g
+ *              and AdamW forms each g[i] again from the two copies with the same
+ *              arithmetic (same bits).  ZERO_EINVAL for NULL g with any other layout.
  *   other arguments as in the three calls above.  3 + n_buckets - 1 kernel launches.
  * ------------------------------------------------------------------------------------- */
 int zero_step(const zero_layout_t* layout, const zero_adamw_hparams_t* hp, zero_dtype_t dtype,

@@ -151,6 +151,14 @@ def test_norm_adamw_step_rejections(lib):
     reps = (C.c_void_p * 4)(A, A, A, A)
     # a bad bucket pointer anywhere rejects the whole step before any launch
     assert lib.zero_step(C.byref(lay), C.byref(hp), z.ZERO_BF16, reps, A, A, A, A, A, A + 1, A, None) == z.ZERO_EALIGN
+    # g = NULL (the re-reading schedule) only for N = 2 with one window
+    assert lib.zero_step(C.byref(lay), C.byref(hp), z.ZERO_BF16, reps, None, A, A, A, A, A, A, None) == z.ZERO_EINVAL
+    lay2b = z.zero_partition(1 << 20, 2, 2, 1, 1 << 16)
+    reps2 = (C.c_void_p * (2 * lay2b.n_buckets))(*([A] * (2 * lay2b.n_buckets)))
+    assert lib.zero_step(C.byref(lay2b), C.byref(hp), z.ZERO_BF16, reps2, None, A, A, A, A, A, A, None) == z.ZERO_EINVAL
+    lay2 = z.zero_partition(1000, 2)
+    reps1 = (C.c_void_p * 2)(A, A)
+    assert lib.zero_step(C.byref(lay2), C.byref(hp), z.ZERO_BF16, reps1, None, A, A, A, A, A + 2, A, None) == z.ZERO_EALIGN
     reps0 = (C.c_void_p * 4)(A, 0, A, A)
     assert lib.zero_step(C.byref(lay), C.byref(hp), z.ZERO_BF16, reps0, A, A, A, A, A, A, A, None) == z.ZERO_EINVAL
     assert lib.zero_step_state_init(C.byref(lay), 0.0, 1, 1000, A, A, None) == z.ZERO_EINVAL

@@ -55,7 +55,7 @@ class StepState(C.Structure):
         ("t", C.c_uint32), ("good_steps", C.c_uint32), ("growth_interval", C.c_uint32),
         ("dynamic", C.c_uint32), ("n_ranks", C.c_uint32), ("n_steps", C.c_uint32),
         ("n_skipped", C.c_uint32), ("error", C.c_uint32), ("arrivals", C.c_uint32),
-        ("reserved", C.c_uint32 * 11),
+        ("inv_scale_used", C.c_float), ("reserved", C.c_uint32 * 10),
     ]
 
 

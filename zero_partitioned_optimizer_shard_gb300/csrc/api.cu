@@ -88,18 +88,18 @@ int reduce_window(const zero_layout_t* L, zero_dtype_t dtype, const void* const*
 
 int check_reduce_args(const zero_layout_t* L, zero_dtype_t dtype, const void* const* replicas,
                       uint64_t begin, uint64_t count, const float* g, const double* partials,
-                      const zero_step_state_t* st)
+                      const zero_step_state_t* st, bool need_g = true)
 {
     if (!kernel_layout_ok(L) || (dtype != ZERO_F16 && dtype != ZERO_BF16) || !replicas)
         return ZERO_EINVAL;
     if (count == 0 || begin >= L->psi_padded || count > L->psi_padded - begin)
         return ZERO_EINVAL;
-    if (!g || !partials || !st)
+    if ((need_g && !g) || !partials || !st)
         return ZERO_EINVAL;
     for (uint32_t k = 0; k < L->n_ranks; ++k)
         if (!replicas[k])
             return ZERO_EINVAL;
-    if (begin % 8 != 0 || !aligned16(g) || !aligned16(partials) || !aligned16(st))
+    if (begin % 8 != 0 || (need_g && !aligned16(g)) || !aligned16(partials) || !aligned16(st))
         return ZERO_EALIGN;
     for (uint32_t k = 0; k < L->n_ranks; ++k)
         if (!aligned16(replicas[k]))
@@ -109,11 +109,12 @@ int check_reduce_args(const zero_layout_t* L, zero_dtype_t dtype, const void* co
 
 int check_adamw_args(const zero_layout_t* L, const zero_adamw_hparams_t* hp, const float* g,
                      const float* master, const float* m, const float* v, const uint16_t* params,
-                     const zero_step_state_t* st)
+                     const zero_step_state_t* st, bool need_g = true)
 {
-    if (!kernel_layout_ok(L) || !hparams_ok(hp) || !g || !master || !m || !v || !params || !st)
+    if (!kernel_layout_ok(L) || !hparams_ok(hp) || (need_g && !g) || !master || !m || !v ||
+        !params || !st)
         return ZERO_EINVAL;
-    if (!aligned16(g) || !aligned16(master) || !aligned16(m) || !aligned16(v) ||
+    if ((need_g && !aligned16(g)) || !aligned16(master) || !aligned16(m) || !aligned16(v) ||
         !aligned16(params) || !aligned16(st))
         return ZERO_EALIGN;
     return ZERO_OK;
@@ -150,6 +151,31 @@ int adamw(const zero_layout_t* L, const zero_adamw_hparams_t* hp, const float* g
     a.eps = hp->eps;
     a.out_f16 = hp->params_dtype == ZERO_F16 ? 1u : 0u;
     return cuda_status(host_state ? launch_adamw_host_state(a, stream) : launch_adamw(a, stream));
+}
+
+/* AdamW for the re-reading schedule: g formed again from the two gradient copies. */
+int adamw_rereduce(const zero_layout_t* L, const zero_adamw_hparams_t* hp, zero_dtype_t dtype,
+                   const void* rep0, const void* rep1, float* master, float* m, float* v,
+                   uint16_t* params, const zero_step_state_t* st, cudaStream_t stream)
+{
+    AdamwArgs a;
+    memset(&a, 0, sizeof a);
+    a.master = master;
+    a.m = m;
+    a.v = v;
+    a.out = params;
+    a.st = st;
+    a.err = const_cast<uint32_t*>(&st->error);
+    a.psi = L->psi;
+    a.psi_padded = L->psi_padded;
+    a.beta1 = hp->beta1;
+    a.beta2 = hp->beta2;
+    a.eps = hp->eps;
+    a.out_f16 = hp->params_dtype == ZERO_F16 ? 1u : 0u;
+    a.rep0 = static_cast<const uint16_t*>(rep0);
+    a.rep1 = static_cast<const uint16_t*>(rep1);
+    a.grad_f16 = dtype == ZERO_F16 ? 1u : 0u;
+    return cuda_status(launch_adamw_rereduce(a, stream));
 }
 
 /* The device address of `bytes` of page-locked host memory at p (cudaHostAlloc or
@@ -299,14 +325,19 @@ extern "C" int zero_step(const zero_layout_t* layout, const zero_adamw_hparams_t
 {
     if (!kernel_layout_ok(layout) || !replicas)
         return ZERO_EINVAL;
+    // g == NULL: the re-reading schedule (N = 2, one window over resident copies)
+    const bool reread = g == nullptr;
+    if (reread && (layout->n_ranks != 2 || layout->n_buckets != 1))
+        return ZERO_EINVAL;
     const uint64_t W = layout->bucket_elems, P = layout->psi_padded, N = layout->n_ranks;
     for (uint64_t b = 0; b < layout->n_buckets; ++b) {
         const uint64_t begin = b * W, count = begin + W < P ? W : P - begin;
-        int rc = check_reduce_args(layout, dtype, replicas + b * N, begin, count, g, partials, st);
+        int rc = check_reduce_args(layout, dtype, replicas + b * N, begin, count, g, partials, st,
+                                   !reread);
         if (rc != ZERO_OK)
             return rc;
     }
-    int rc = check_adamw_args(layout, hp, g, master, m, v, params, st);
+    int rc = check_adamw_args(layout, hp, g, master, m, v, params, st, !reread);
     if (rc != ZERO_OK)
         return rc;
     if (!aligned16(partials))
@@ -321,6 +352,9 @@ extern "C" int zero_step(const zero_layout_t* layout, const zero_adamw_hparams_t
     rc = grad_norm(layout, hp, partials, st, s);
     if (rc != ZERO_OK)
         return rc;
+    if (reread)
+        return adamw_rereduce(layout, hp, dtype, replicas[0], replicas[1], master, m, v, params,
+                              st, s);
     return adamw(layout, hp, g, master, m, v, params, st, s);
 }
 

@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(kFinThreads) k_finalize(const __grid_constant_
         if (lane == 0 && w == 2 && !s_overflow)
             st->rbc2 = (float)sqrt(1.0 - pow((double)a.hp.beta2, (double)t));
         if (lane == 0 && w == 3) {
+            st->inv_scale_used = st->inv_scale;  // this step's unscale, for a re-reading AdamW
             float L = st->loss_scale;
             if (s_overflow) {
                 st->skip = 1;

@@ -219,7 +219,9 @@ __device__ __forceinline__ void finish_group(const ReduceArgs& a, float inv, flo
             bad |= (in >> e & 1u) && not_finite(gv[e]);
         acc.wide += sumsq_wide(gv[0], gv[1], gv[2], gv[3], gv[4], gv[5], gv[6], gv[7], in);
     }
-    if (full) {
+    if (!a.g) {
+        // no g: the AdamW pass re-reads the gradient copies instead (small N)
+    } else if (full) {
         __stcs(reinterpret_cast<float4*>(a.g + b), make_float4(gv[0], gv[1], gv[2], gv[3]));
         __stcs(reinterpret_cast<float4*>(a.g + b + 4), make_float4(gv[4], gv[5], gv[6], gv[7]));
     } else {

@@ -43,6 +43,10 @@ struct AdamwArgs {
     uint64_t psi, psi_padded;
     float beta1, beta2, eps;
     uint32_t out_f16;                        // gathered parameters as fp16 instead of bf16
+    // re-reading schedule (N = 2, g not materialised): the two gradient copies instead of g
+    const uint16_t* rep0;
+    const uint16_t* rep1;
+    uint32_t grad_f16;                       // copies are fp16 (else bf16)
 };
 
 struct InitArgs {
@@ -84,7 +88,8 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
 cudaError_t launch_reduce(const ReduceArgs& a, zero_dtype_t dtype, cudaStream_t s);
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s);
 cudaError_t launch_adamw(const AdamwArgs& a, cudaStream_t s);
-cudaError_t launch_adamw_host_state(const AdamwArgs& a, cudaStream_t s);  // master/m/v in pinned host memory
+cudaError_t launch_adamw_host_state(const AdamwArgs& a, cudaStream_t s);
+cudaError_t launch_adamw_rereduce(const AdamwArgs& a, cudaStream_t s);  // g from rep0 + rep1  // master/m/v in pinned host memory
 cudaError_t launch_state_init(const InitArgs& a, cudaStream_t s);
 
 /* Resident blocks per SM times SM count for a kernel, cached per device. */
