@@ -342,12 +342,15 @@ def _traffic_from_profile():
     kernel source has changed since those counters were taken."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "k_adamw_traffic.json")
-    src = os.path.join(ROOT, "zero_partitioned_optimizer_shard_gb300", "csrc", "adamw.cu")
+    csrc = os.path.join(ROOT, "zero_partitioned_optimizer_shard_gb300", "csrc")
     try:
         with open(path) as f:
             rec = json.load(f)
-        with open(src, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
+        h = hashlib.sha256()
+        for name in ("adamw.cu", "adamw_elem.cuh"):  # k_adamw's whole source
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+        sha = h.hexdigest()
         if not sha.startswith(rec["source_sha256_prefix"]):
             return None
         return rec["traffic_bytes_per_launch_full_size"]

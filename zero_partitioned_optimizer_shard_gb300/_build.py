@@ -10,8 +10,10 @@ CSRC = os.path.join(PKG, "csrc")
 ROOT = os.path.dirname(PKG)
 OBJ = os.path.join(ROOT, "_build", "zero_shard")
 LIB = os.path.join(PKG, "libzero_shard.so")
-SOURCES = ["partition.cu", "reduce.cu", "finalize.cu", "adamw.cu", "api.cu", "noalloc.cu"]
-HEADERS = [os.path.join(CSRC, "zero_internal.h"), os.path.join(ROOT, "include", "zero.h")]
+SOURCES = ["partition.cu", "reduce.cu", "finalize.cu", "adamw.cu", "adamw_variants.cu", "api.cu",
+           "noalloc.cu"]
+HEADERS = [os.path.join(CSRC, "zero_internal.h"), os.path.join(CSRC, "adamw_elem.cuh"),
+           os.path.join(ROOT, "include", "zero.h")]
 
 ARCH = os.environ.get("ZERO_CUDA_ARCH", "103a")
 NVCC_FLAGS = [

@@ -1,0 +1,81 @@
+/*
+ * adamw_elem.cuh -- the AdamW element update and the bulk-copy ring helpers shared by the
+ * AdamW kernels (adamw.cu: state in HBM; adamw_variants.cu: the re-reading schedule and
+ * the state in host memory), so every variant computes the same bits.
+ *
+ * Per element, in fp32 and in this order (the _rn intrinsics forbid FMA contraction, so
+ * the result is the correctly rounded value of each written operation):
+ *   gc = c*g;  m = b1*m + (1-b1)*gc;  v = b2*v + (1-b2)*(gc*gc)
+ *   p  = p*decay - step_size * (m / (sqrt(v)/rbc2 + eps));  out = bf16_rne(p) (or fp16)
+ */
+#pragma once
+
+#include "zero_internal.h"
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace zero {
+namespace {
+
+constexpr int kBlock = 256;
+
+struct Scalars {
+    float c, step, rbc2, decay, b1, b2, omb1, omb2, eps;
+};
+
+__device__ __forceinline__ float adamw_one(float g, float& p, float& m, float& v, const Scalars& s)
+{
+    const float gc = __fmul_rn(s.c, g);
+    m = __fadd_rn(__fmul_rn(s.b1, m), __fmul_rn(s.omb1, gc));
+    v = __fadd_rn(__fmul_rn(s.b2, v), __fmul_rn(s.omb2, __fmul_rn(gc, gc)));
+    const float denom = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), s.rbc2), s.eps);
+    p = __fsub_rn(__fmul_rn(p, s.decay), __fmul_rn(s.step, __fdiv_rn(m, denom)));
+    return p;
+}
+
+/* Two gathered parameters, rounded to nearest even, in one 32-bit word (lo first). */
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi)
+{
+    if (F16) {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <bool F16>
+__device__ __forceinline__ uint16_t pack1(float x)
+{
+    return F16 ? __half_as_ushort(__float2half_rn(x)) : __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+/* Wait for phase `parity` of an mbarrier, at most ~2 s (4e9 cycles); 0 on timeout. */
+__device__ __forceinline__ uint32_t wait_parity_bounded(uint32_t bar, uint32_t parity)
+{
+    const long long t0 = clock64();
+    uint32_t ok = 0;
+    while (true) {
+        asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; "
+                     "selp.u32 %0, 1, 0, p; }"
+                     : "=r"(ok)
+                     : "r"(bar), "r"(parity)
+                     : "memory");
+        if (ok || clock64() - t0 > 4000000000LL)
+            return ok;
+    }
+}
+
+constexpr int kChunk = 4096;  // elements per bulk-copied chunk of each array
+constexpr int kStages = 3;
+constexpr size_t kSmemBytes = (size_t)kStages * 4 * kChunk * sizeof(float);  // 192 KiB
+
+}  // namespace
+}  // namespace zero
