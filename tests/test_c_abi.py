@@ -1,9 +1,13 @@
-"""The boundary is a C ABI: a plain C program (tests/c_abi_host.c) compiled with gcc against
-include/zero.h and linked with libzero_shard.so calls the host-only entry points.  No GPU
-is touched."""
+"""The boundary is a C ABI: plain C programs compiled with gcc against include/zero.h and
+linked with libzero_shard.so.  tests/c_abi_host.c calls the host-only entry points (no
+GPU); tests/c_abi_step.c (GPU test) runs two steps with CUDA-runtime buffers and checks
+them against the C oracle on the same inputs, with no PyTorch or Python in the loop."""
 import os
 import subprocess
 
+import pytest
+
+import oracle
 from zero_partitioned_optimizer_shard_gb300 import _build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -19,3 +23,30 @@ def test_c_program_links_and_runs(tmp_path):
     r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.strip().endswith("ok")
+
+
+def _cuda_home():
+    for p in (os.environ.get("CUDA_HOME", ""), "/usr/local/cuda"):
+        if p and os.path.exists(os.path.join(p, "include", "cuda_runtime.h")):
+            return p
+    pytest.skip("CUDA toolkit headers not found")
+
+
+@pytest.mark.gpu
+def test_c_program_runs_a_step_against_the_c_oracle(tmp_path):
+    lib = _build.build()
+    olib = oracle.build()
+    cuda = _cuda_home()
+    exe = str(tmp_path / "c_abi_step")
+    subprocess.run(["gcc", "-std=c11", "-O2", "-Wall", "-Werror", "-ffp-contract=off",
+                    "-I", os.path.join(ROOT, "include"), "-I", os.path.join(ROOT, "oracle"),
+                    "-I", os.path.join(cuda, "include"),
+                    os.path.join(ROOT, "tests", "c_abi_step.c"), "-o", exe,
+                    "-L", os.path.dirname(lib), "-lzero_shard", f"-Wl,-rpath,{os.path.dirname(lib)}",
+                    olib, f"-Wl,-rpath,{os.path.dirname(olib)}",
+                    "-L", os.path.join(cuda, "lib64"), "-lcudart",
+                    f"-Wl,-rpath,{os.path.join(cuda, 'lib64')}", "-lm"], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.strip().endswith("ok"), r.stdout
+
