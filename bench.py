@@ -110,16 +110,17 @@ class ClockSampler:
                 "samples": len(rows), "reasons": reasons}
 
 
-def cpu_oracle_baseline(steps: int = 1, psi_sample: int = 1 << 24):
-    """Time the CPU oracle (as it stands, single-threaded) on a bounded sample of the
-    GPT-2 workload: the same recipe at psi_sample parameters, N = 8; params/s."""
+def cpu_oracle_baseline(steps: int = 1, psi_sample: int = 1 << 24, base=None):
+    """Time the CPU oracle (as it stands, single-threaded) on a bounded sample of a
+    workload (default the GPT-2 one): the same recipe at psi_sample parameters, N = 8;
+    params/s."""
     import numpy as np
 
     import oracle
     import synth
     from synth import workloads as W
 
-    wl = W.scaled(W.C2, psi_sample, steps=steps)
+    wl = W.scaled(W.C2 if base is None else base, psi_sample, steps=steps)
     orc = oracle.load()
     lay = orc.partition(wl.psi, wl.n_ranks, wl.stage)
     P = lay.psi_padded
@@ -144,12 +145,14 @@ def run_reference(args):
     ws, rank, _ = _dist()
     if rank != 0:
         return 0
+    from synth import workloads as W
+    base = W.C3 if args.workload == "llama-7b" else W.C2
     sample = 1 << 22
     for _ in range(args.warmup):
-        cpu_oracle_baseline(1, sample)
+        cpu_oracle_baseline(1, sample, base)
     total = 0.0
     for _ in range(args.steps):
-        _, dt, wl = cpu_oracle_baseline(1, sample)
+        _, dt, wl = cpu_oracle_baseline(1, sample, base)
         total += dt
     value = sample * args.steps / total
     line = {
@@ -157,9 +160,10 @@ def run_reference(args):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": _config(),
+        "config": _config(base=base),
         "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
-                         "sample": f"each step: the GPT-2-1.5B recipe at psi={sample} "
+                         "sample": f"each step: the {'Llama-7B' if base is W.C3 else 'GPT-2-1.5B'} "
+                                   f"recipe at psi={sample} "
                                    f"(N=8 bf16 copies, random fp32 state), one oracle step"},
         "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -168,17 +172,26 @@ def run_reference(args):
     return 0
 
 
-def _config(extra=None, psi=None):
+def _config(extra=None, psi=None, base=None):
     from synth import workloads as W
-    psi = W.C2.psi if psi is None else psi
-    name = ("GPT-2-1.5B-shaped flat buffer, psi=1,557,611,200" if psi == W.C2.psi else
-            f"GPT-2-1.5B recipe at a reduced psi={psi:,} (profiling case, not the headline)")
-    c = {"workload": name + ", N=8 simulated ranks, ZeRO-2, bf16 gradient copies ~N(0,1e-4), "
+    base = W.C2 if base is None else base
+    psi = base.psi if psi is None else psi
+    if base is W.C3:
+        name = ("Llama-7B-shaped flat buffer, psi=6,738,415,616, N=8 simulated ranks, ZeRO-3, "
+                "gradients in 2^27-element buckets of 8 bf16 copies (51 buckets, each reduced "
+                "by its own launch)")
+    else:
+        name = ("GPT-2-1.5B-shaped flat buffer, psi=1,557,611,200" if psi == W.C2.psi else
+                f"GPT-2-1.5B recipe at a reduced psi={psi:,} (profiling case, not the headline)")
+        name += ", N=8 simulated ranks, ZeRO-2"
+    c = {"workload": name + ", bf16 gradient copies ~N(0,1e-4), "
                      "fp32 master/m/v random-init, AdamW lr 1e-3 betas 0.9/0.999 eps 1e-8 "
                      "wd 0.01 clip 1.0",
-         "psi": psi, "n_ranks": W.C2.n_ranks, "stage": W.C2.stage, "grad_dtype": "bf16",
+         "psi": psi, "n_ranks": base.n_ranks, "stage": base.stage, "grad_dtype": "bf16",
          "l2": f"inputs larger than L2 ({(42 * psi) / 1e9:.1f} GB working set vs 129 MB L2); "
                "no flush needed"}
+    if base.bucket_elems:
+        c["bucket_elems"] = base.bucket_elems
     if extra:
         c.update(extra)
     return c
@@ -197,9 +210,11 @@ def run_ours(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wl = W.C2 if args.psi in (None, W.C2.psi) else W.scaled(W.C2, args.psi)
-    lay = z.zero_partition(wl.psi, wl.n_ranks, wl.stage)
+    base = W.C3 if args.workload == "llama-7b" else W.C2
+    wl = base if args.psi in (None, base.psi) else W.scaled(base, args.psi)
+    lay = z.zero_partition(wl.psi, wl.n_ranks, wl.stage, 1, wl.bucket_elems)
     P, N = lay.psi_padded, lay.n_ranks
+    Wb, nb = lay.bucket_elems, lay.n_buckets
     hp = z.hparams(**wl.hp.__dict__)
     stream = torch.cuda.current_stream(dev)
     s = stream.cuda_stream
@@ -222,9 +237,14 @@ def run_ours(args):
     st = torch.empty(z.STATE_BYTES, dtype=torch.uint8, device=dev)
     z.zero_step_state_init(lay, 1.0, False, 1000, st, partials, stream)
     rep_ptrs = [r.data_ptr() for r in reps]
+    # one window per bucket: every bucket's N copies stay resident, each reduced by its own
+    # launch (a single window over the whole buffer when the workload is not bucketed)
+    windows = [(b * Wb, min(Wb, P - b * Wb), [p + 2 * b * Wb for p in rep_ptrs]) for b in range(nb)]
 
     def step(ev=None):
-        z.zero_reduce_shard_unscale(lay, z.ZERO_BF16, rep_ptrs, 0, P, g, partials, st, stream)
+        for begin, count, ptrs in windows:
+            z.zero_reduce_shard_unscale(lay, z.ZERO_BF16, ptrs, begin, count, g, partials, st,
+                                        stream)
         if ev:
             ev[0].record(stream)
         z.zero_grad_norm(lay, hp, partials, st, stream)
@@ -272,7 +292,12 @@ def run_ours(args):
 
     # --- end to end through zero_step_host: gradients from pinned host memory -----------
     e2e = None
-    if not args.no_e2e:
+    if nb > 1:
+        e2e = {"value": None, "unit": "params/s", "h2d_bytes_per_step": N * P * 2,
+               "d2h_bytes_per_step": z.STATE_BYTES,
+               "note": "not measured for the bucketed buffer: its gradient copies "
+                       f"({N * P * 2 / 1e9:.0f} GB) would all have to be pinned in host memory"}
+    elif not args.no_e2e:
         e2e = _e2e(args, z, torch, dev, wl, hp, reps, g, partials, master, m, v, out, st, stream)
 
     peak, peak_kind = _peaks()
@@ -296,7 +321,7 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": _config({"parallelism": f"{ws} independent replica(s) of the simulated "
                                           f"{N}-rank step" if ws > 1 else "1 GPU, 8 simulated ranks"},
-                          psi=wl.psi),
+                          psi=wl.psi, base=base),
         "hbm": {
             "gbs_at_26p2n_bytes": bytes_26 / (ms / 1e3) / 1e9,
             "pct_of_8tbs": 100 * bytes_26 / (ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
@@ -310,24 +335,28 @@ def run_ours(args):
             "kernel": "k_adamw (fused AdamW + bf16 cast + gathered write)",
             "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
             "peak_kind": peak_kind + ", burst figure of a kernel timed alone",
-            "traffic": _traffic_from_profile(), "bytes_per_launch": ADAMW_BYTES * P,
+            "traffic": _traffic_from_profile(P), "bytes_per_launch": ADAMW_BYTES * P,
             "avg_launch_ms": adamw_avg,
         },
         "kernels": {
             "k_reduce": {"avg_ms": reduce_avg, "bytes_per_launch": red_bytes,
+                         "gbs": red_bytes / (reduce_avg / 1e3) / 1e9} if nb == 1 else
+                        {"launches_per_step": nb, "avg_ms_all_buckets": reduce_avg,
+                         "bytes_all_buckets": red_bytes,
                          "gbs": red_bytes / (reduce_avg / 1e3) / 1e9},
             "k_finalize": {"avg_ms": statistics.mean(norm_ms)},
             "k_adamw": {"avg_ms": adamw_avg, "bytes_per_launch": ADAMW_BYTES * P, "gbs": ach},
         },
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (nb + 2) * args.steps,
         "clocks": clk,
         "e2e": e2e,
         "final_state": {"t": stt.t, "norm": stt.norm, "clip_coef": stt.clip_coef},
     }
     if rank == 0 and not args.no_cpu_baseline:
-        v, dt, swl = cpu_oracle_baseline(6, 1 << 26)
+        v, dt, swl = cpu_oracle_baseline(6, 1 << 26, base)
         line["cpu_baseline"] = {"value": v, "unit": "params/s", "cores": 1, "kind": "oracle",
-                                "sample": f"6 oracle steps of the GPT-2-1.5B recipe at psi={swl.psi} "
+                                "sample": f"6 oracle steps of the {'Llama-7B' if base is W.C3 else 'GPT-2-1.5B'} "
+                                          f"recipe at psi={swl.psi} "
                                           f"(N=8 bf16 copies, random fp32 state), {dt:.1f} s "
                                           f"single-threaded"}
     if rank == 0:
@@ -337,9 +366,10 @@ def run_ours(args):
     return 0
 
 
-def _traffic_from_profile():
-    """DRAM bytes per k_adamw launch from the committed ncu summary, or None when the
-    kernel source has changed since those counters were taken."""
+def _traffic_from_profile(psi_padded):
+    """DRAM bytes per k_adamw launch over psi_padded parameters, scaled from the committed
+    ncu capture (traffic is proportional to the parameters), or None when the kernel
+    source has changed since those counters were taken."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "k_adamw_traffic.json")
     csrc = os.path.join(ROOT, "zero_partitioned_optimizer_shard_gb300", "csrc")
@@ -353,7 +383,7 @@ def _traffic_from_profile():
         sha = h.hexdigest()
         if not sha.startswith(rec["source_sha256_prefix"]):
             return None
-        return rec["traffic_bytes_per_launch_full_size"]
+        return round(rec["traffic_bytes_per_launch_small"] * psi_padded / rec["small_psi"])
     except Exception:
         return None
 
@@ -649,9 +679,11 @@ def run_offload(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     link = _link_bandwidth(torch, dev)
-    wl = W.C2 if args.psi in (None, W.C2.psi) else W.scaled(W.C2, args.psi)
-    lay = z.zero_partition(wl.psi, wl.n_ranks, wl.stage)
+    base = W.C3 if args.workload == "llama-7b" else W.C2
+    wl = base if args.psi in (None, base.psi) else W.scaled(base, args.psi)
+    lay = z.zero_partition(wl.psi, wl.n_ranks, wl.stage, 1, wl.bucket_elems)
     P, N = lay.psi_padded, lay.n_ranks
+    Wb, nb = lay.bucket_elems, lay.n_buckets
     hp = z.hparams(**wl.hp.__dict__)
     stream = torch.cuda.current_stream(dev)
     s = stream.cuda_stream
@@ -738,6 +770,9 @@ def main():
                     help="optimizer state (master/m/v) in pinned host memory, updated over "
                          "the CPU-GPU link")
     ap.add_argument("--sweep-n", default="2,4,8,16,64")
+    ap.add_argument("--workload", default="gpt2-1.5b", choices=["gpt2-1.5b", "llama-7b"],
+                    help="gpt2-1.5b: psi=1,557,611,200, N=8, ZeRO-2 (the headline); llama-7b: "
+                         "psi=6,738,415,616, N=8, ZeRO-3, 51 gradient buckets of 2^27 elements")
     ap.add_argument("--psi", type=int, default=None,
                     help="profiling only: the same recipe at another size (default: the "
                          "GPT-2-1.5B buffer)")

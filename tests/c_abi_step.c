@@ -35,22 +35,23 @@ int main(void)
     zero_layout_t L;
     ZK(zero_partition(psi, (uint32_t)N, 2, 1, 0, &L));
     const uint64_t P = L.psi_padded;
+    const uint64_t R = (P + 7) & ~7ull;  /* array stride: every copy and state array starts 16-byte aligned */
 
     /* host inputs: N bf16 gradient copies (pads 0), fp32 master / m / v */
-    uint16_t* reps = calloc(N * P, 2);
-    float* st3 = calloc(3 * P, 4);
+    uint16_t* reps = calloc(N * R, 2);
+    float* st3 = calloc(3 * R, 4);
     for (uint64_t k = 0; k < N; ++k)
         for (uint64_t i = 0; i < psi; ++i) {
             float x = uniform(k * 1000003ull + i, 1e-3);
             uint32_t u;
             memcpy(&u, &x, 4);
-            reps[k * P + i] = (uint16_t)(u >> 16);  /* truncate to bf16 */
+            reps[k * R + i] = (uint16_t)(u >> 16);  /* truncate to bf16 */
         }
     for (uint64_t i = 0; i < psi; ++i) {
         st3[i] = uniform(7ull << 40 | i, 0.02);
-        st3[P + i] = uniform(8ull << 40 | i, 1e-4);
+        st3[R + i] = uniform(8ull << 40 | i, 1e-4);
         float s = uniform(9ull << 40 | i, 1e-4);
-        st3[2 * P + i] = s * s;
+        st3[2 * R + i] = s * s;
     }
 
     /* device buffers through the CUDA runtime */
@@ -59,29 +60,29 @@ int main(void)
     uint16_t* d_out;
     double* d_part;
     zero_step_state_t* d_st;
-    CK(cudaMalloc(&d_reps, N * P * 2));
+    CK(cudaMalloc(&d_reps, N * R * 2));
     CK(cudaMalloc((void**)&d_g, P * 4));
-    CK(cudaMalloc((void**)&d_state, 3 * P * 4));
+    CK(cudaMalloc((void**)&d_state, 3 * R * 4));
     CK(cudaMalloc((void**)&d_out, P * 2));
     CK(cudaMalloc((void**)&d_part, zero_workspace_bytes(&L)));
     CK(cudaMalloc((void**)&d_st, sizeof(zero_step_state_t)));
-    CK(cudaMemcpy(d_reps, reps, N * P * 2, cudaMemcpyHostToDevice));
-    CK(cudaMemcpy(d_state, st3, 3 * P * 4, cudaMemcpyHostToDevice));
+    CK(cudaMemcpy(d_reps, reps, N * R * 2, cudaMemcpyHostToDevice));
+    CK(cudaMemcpy(d_state, st3, 3 * R * 4, cudaMemcpyHostToDevice));
     const void* rp[4];
     for (uint64_t k = 0; k < N; ++k)
-        rp[k] = (const char*)d_reps + k * P * 2;
+        rp[k] = (const char*)d_reps + k * R * 2;
     zero_adamw_hparams_t hp = {1e-3f, 0.9f, 0.999f, 1e-8f, 0.01f, 1.0f, 0};
     ZK(zero_step_state_init(&L, 1.0f, 0, 1000, d_st, d_part, NULL));
     for (int step = 0; step < 2; ++step)
-        ZK(zero_step(&L, &hp, ZERO_BF16, rp, d_g, d_part, d_state, d_state + P, d_state + 2 * P,
+        ZK(zero_step(&L, &hp, ZERO_BF16, rp, d_g, d_part, d_state, d_state + R, d_state + 2 * R,
                      d_out, d_st, NULL));
     zero_step_state_t s;
     ZK(zero_step_state_read(d_st, &s, NULL));
     float* g = malloc(P * 4);
-    float* state = malloc(3 * P * 4);
+    float* state = malloc(3 * R * 4);
     uint16_t* out = malloc(P * 2);
     CK(cudaMemcpy(g, d_g, P * 4, cudaMemcpyDeviceToHost));
-    CK(cudaMemcpy(state, d_state, 3 * P * 4, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(state, d_state, 3 * R * 4, cudaMemcpyDeviceToHost));
     CK(cudaMemcpy(out, d_out, P * 2, cudaMemcpyDeviceToHost));
 
     /* the oracle, two steps on the same inputs */
@@ -93,11 +94,11 @@ int main(void)
     oracle_report_t rep;
     const uint16_t* orp[4];
     for (uint64_t k = 0; k < N; ++k)
-        orp[k] = reps + k * P;
+        orp[k] = reps + k * R;
     float* og = calloc(P, 4);
     uint16_t* oout = calloc(P, 2);
     for (int step = 0; step < 2; ++step)
-        if (oracle_step(&ol, &ohp, ORACLE_BF16, orp, og, st3, st3 + P, st3 + 2 * P, oout, &sc, &rep) != 0)
+        if (oracle_step(&ol, &ohp, ORACLE_BF16, orp, og, st3, st3 + R, st3 + 2 * R, oout, &sc, &rep) != 0)
             return 1;
 
     if (s.t != rep.t || s.skip != rep.skipped || fabs(s.norm - rep.norm) > 1e-5 * rep.norm) {
@@ -109,7 +110,7 @@ int main(void)
         if (memcmp(&g[i], &og[i], 4) != 0)
             ++bad;
         for (int a = 0; a < 3; ++a) {
-            const float x = state[a * P + i], y = st3[a * P + i];
+            const float x = state[a * R + i], y = st3[a * R + i];
             if (memcmp(&x, &y, 4) == 0)
                 ++exact;
             else if (!(fabs((double)x - y) <= 1e-5 * fabs((double)y) + 1e-30))
