@@ -31,6 +31,8 @@ METRIC = "params updated/s and achieved HBM GB/s (% of ~8 TB/s) for the fused sh
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 ADAMW_BYTES = 30   # per parameter: g, master, m, v read (16); master, m, v, bf16 written (14)
+L2_FLUSH_BELOW = 4 * 129e6   # working sets below this are timed with L2 flushed between steps
+L2_FLUSH_BYTES = 512 << 20
 
 
 def _peaks():
@@ -120,23 +122,28 @@ def cpu_oracle_baseline(steps: int = 1, psi_sample: int = 1 << 24, base=None):
     import synth
     from synth import workloads as W
 
-    wl = W.scaled(W.C2 if base is None else base, psi_sample, steps=steps)
+    base = W.C2 if base is None else base
+    wl = base if psi_sample == base.psi else W.scaled(base, psi_sample, steps=steps)
     orc = oracle.load()
     lay = orc.partition(wl.psi, wl.n_ranks, wl.stage)
     P = lay.psi_padded
     hp = oracle.hparams(**wl.hp.__dict__)
     reps = [synth.fill_host(wl.grad_out, wl.grad_kind, wl.grad_key(1, k), 0, P, wl.psi,
-                            wl.grad_sigma) for k in range(wl.n_ranks)]
-    st = [synth.fill_host(synth.OUT_F32, kind, wl.state_key(role), 0, P, wl.psi, sig)
-          for role, kind, sig in ((synth.ROLE_MASTER, synth.NORMAL, wl.master_sigma),
-                                  (synth.ROLE_MOM, synth.NORMAL, wl.mom_sigma),
-                                  (synth.ROLE_VAR, synth.NORMAL_SQ, wl.mom_sigma))]
+                            wl.grad_sigma, wl.loss_scale) for k in range(wl.n_ranks)]
+    st = [synth.fill_host(synth.OUT_F32, synth.NORMAL, wl.state_key(synth.ROLE_MASTER), 0, P,
+                          wl.psi, wl.master_sigma)]
+    if wl.random_moments:
+        st += [synth.fill_host(synth.OUT_F32, kind, wl.state_key(role), 0, P, wl.psi, wl.mom_sigma)
+               for role, kind in ((synth.ROLE_MOM, synth.NORMAL), (synth.ROLE_VAR, synth.NORMAL_SQ))]
+    else:
+        st += [np.zeros(P, np.float32), np.zeros(P, np.float32)]
     g = np.zeros(P, np.float32)
     out = np.zeros(P, np.uint16)
-    sc = oracle.scaler(1.0, False, 1000)
+    sc = oracle.scaler(wl.loss_scale, wl.dynamic, wl.growth_interval)
+    dt_ = oracle.F16 if wl.grad_dtype == "f16" else oracle.BF16
     t0 = time.perf_counter()
     for _ in range(steps):
-        orc.step(lay, hp, oracle.BF16, reps, g, *st, out, sc)
+        orc.step(lay, hp, dt_, reps, g, *st, out, sc)
     dt = time.perf_counter() - t0
     return wl.psi * steps / dt, dt, wl
 
@@ -145,9 +152,8 @@ def run_reference(args):
     ws, rank, _ = _dist()
     if rank != 0:
         return 0
-    from synth import workloads as W
-    base = W.C3 if args.workload == "llama-7b" else W.C2
-    sample = 1 << 22
+    base = _base_workload(args.workload)
+    sample = min(1 << 22, base.psi)
     for _ in range(args.warmup):
         cpu_oracle_baseline(1, sample, base)
     total = 0.0
@@ -162,14 +168,24 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": _config(base=base),
         "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
-                         "sample": f"each step: the {'Llama-7B' if base is W.C3 else 'GPT-2-1.5B'} "
+                         "sample": f"each step: the {_recipe_name(base)} "
                                    f"recipe at psi={sample} "
-                                   f"(N=8 bf16 copies, random fp32 state), one oracle step"},
+                                   f"(N={base.n_ranks} {base.grad_dtype} copies), one oracle step"},
         "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def _base_workload(name):
+    from synth import workloads as W
+    return {"gpt2-1.5b": W.C2, "llama-7b": W.C3, "c1": W.C1}[name]
+
+
+def _recipe_name(base):
+    from synth import workloads as W
+    return {id(W.C2): "GPT-2-1.5B", id(W.C3): "Llama-7B", id(W.C1): "odd-size fp16"}[id(base)]
 
 
 def _config(extra=None, psi=None, base=None):
@@ -180,16 +196,24 @@ def _config(extra=None, psi=None, base=None):
         name = ("Llama-7B-shaped flat buffer, psi=6,738,415,616, N=8 simulated ranks, ZeRO-3, "
                 "gradients in 2^27-element buckets of 8 bf16 copies (51 buckets, each reduced "
                 "by its own launch)")
+    elif base is W.C1:
+        name = ("odd-size fp16 buffer, psi=1,000,003 (last shard padded), N=4 simulated ranks, "
+                "ZeRO-2, fp16 gradient copies fp16(N(0,1e-3)*1024), dynamic loss scale 1024, "
+                "fp32 master ~N(0,0.02), m = v = 0")
     else:
         name = ("GPT-2-1.5B-shaped flat buffer, psi=1,557,611,200" if psi == W.C2.psi else
                 f"GPT-2-1.5B recipe at a reduced psi={psi:,} (profiling case, not the headline)")
         name += ", N=8 simulated ranks, ZeRO-2"
-    c = {"workload": name + ", bf16 gradient copies ~N(0,1e-4), "
-                     "fp32 master/m/v random-init, AdamW lr 1e-3 betas 0.9/0.999 eps 1e-8 "
-                     "wd 0.01 clip 1.0",
-         "psi": psi, "n_ranks": base.n_ranks, "stage": base.stage, "grad_dtype": "bf16",
-         "l2": f"inputs larger than L2 ({(42 * psi) / 1e9:.1f} GB working set vs 129 MB L2); "
-               "no flush needed"}
+    if base is not W.C1:
+        name += ", bf16 gradient copies ~N(0,1e-4), fp32 master/m/v random-init"
+    ws_bytes = (34 + 2 * base.n_ranks) * psi
+    c = {"workload": name + ", AdamW lr 1e-3 betas 0.9/0.999 eps 1e-8 wd 0.01 clip 1.0",
+         "psi": psi, "n_ranks": base.n_ranks, "stage": base.stage, "grad_dtype": base.grad_dtype,
+         "l2": (f"inputs larger than L2 ({ws_bytes / 1e9:.1f} GB working set vs 129 MB L2); "
+                "no flush needed") if ws_bytes > L2_FLUSH_BELOW else
+               (f"L2 flushed before every step (a {L2_FLUSH_BYTES >> 20} MiB write, outside the "
+                f"timed events): the {ws_bytes / 1e6:.0f} MB working set would otherwise stay "
+                "in the 129 MB L2")}
     if base.bucket_elems:
         c["bucket_elems"] = base.bucket_elems
     if extra:
@@ -210,8 +234,9 @@ def run_ours(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    base = W.C3 if args.workload == "llama-7b" else W.C2
+    base = _base_workload(args.workload)
     wl = base if args.psi in (None, base.psi) else W.scaled(base, args.psi)
+    gdt = z.ZERO_F16 if wl.grad_dtype == "f16" else z.ZERO_BF16
     lay = z.zero_partition(wl.psi, wl.n_ranks, wl.stage, 1, wl.bucket_elems)
     P, N = lay.psi_padded, lay.n_ranks
     Wb, nb = lay.bucket_elems, lay.n_buckets
@@ -222,37 +247,44 @@ def run_ours(args):
     reps = [torch.empty(P, dtype=torch.int16, device=dev) for _ in range(N)]
     for k, r in enumerate(reps):
         synth.fill_dev(r.data_ptr(), wl.grad_out, wl.grad_kind, wl.grad_key(1, k), 0, P, wl.psi,
-                       wl.grad_sigma, 1.0, s)
+                       wl.grad_sigma, wl.loss_scale, s)
     master = torch.empty(P, dtype=torch.float32, device=dev)
-    m = torch.empty(P, dtype=torch.float32, device=dev)
-    v = torch.empty(P, dtype=torch.float32, device=dev)
-    for t_, role, kind, sig in ((master, synth.ROLE_MASTER, synth.NORMAL, wl.master_sigma),
-                                (m, synth.ROLE_MOM, synth.NORMAL, wl.mom_sigma),
-                                (v, synth.ROLE_VAR, synth.NORMAL_SQ, wl.mom_sigma)):
+    m = torch.zeros(P, dtype=torch.float32, device=dev)
+    v = torch.zeros(P, dtype=torch.float32, device=dev)
+    fills = [(master, synth.ROLE_MASTER, synth.NORMAL, wl.master_sigma)]
+    if wl.random_moments:
+        fills += [(m, synth.ROLE_MOM, synth.NORMAL, wl.mom_sigma),
+                  (v, synth.ROLE_VAR, synth.NORMAL_SQ, wl.mom_sigma)]
+    for t_, role, kind, sig in fills:
         synth.fill_dev(t_.data_ptr(), synth.OUT_F32, kind, wl.state_key(role), 0, P, wl.psi, sig,
                        1.0, s)
     g = torch.empty(P, dtype=torch.float32, device=dev)
     out = torch.empty(P, dtype=torch.int16, device=dev)
     partials = torch.empty(lay.n_tiles, dtype=torch.float64, device=dev)
     st = torch.empty(z.STATE_BYTES, dtype=torch.uint8, device=dev)
-    z.zero_step_state_init(lay, 1.0, False, 1000, st, partials, stream)
+    z.zero_step_state_init(lay, wl.loss_scale, wl.dynamic, wl.growth_interval, st, partials, stream)
     rep_ptrs = [r.data_ptr() for r in reps]
+    flush = None
+    if (34 + 2 * N) * P <= L2_FLUSH_BELOW:
+        flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     # one window per bucket: every bucket's N copies stay resident, each reduced by its own
     # launch (a single window over the whole buffer when the workload is not bucketed)
     windows = [(b * Wb, min(Wb, P - b * Wb), [p + 2 * b * Wb for p in rep_ptrs]) for b in range(nb)]
 
-    def step(ev=None):
+    bucket_ptrs = [p for _, _, ptrs in windows for p in ptrs]
+    launches = z.zero_step_launches(lay, gdt)  # 1: the single-launch step; else nb + 2
+
+    def step():  # the public call: zero_step over every bucket, the norm and AdamW
+        z.zero_step(lay, hp, gdt, bucket_ptrs, g, partials, master, m, v, out, st, stream)
+
+    def step_split(ev):  # the same launches one by one, with an event after each part
         for begin, count, ptrs in windows:
-            z.zero_reduce_shard_unscale(lay, z.ZERO_BF16, ptrs, begin, count, g, partials, st,
-                                        stream)
-        if ev:
-            ev[0].record(stream)
+            z.zero_reduce_shard_unscale(lay, gdt, ptrs, begin, count, g, partials, st, stream)
+        ev[1].record(stream)
         z.zero_grad_norm(lay, hp, partials, st, stream)
-        if ev:
-            ev[1].record(stream)
+        ev[2].record(stream)
         z.zero_adamw_cast_gather(lay, hp, g, master, m, v, out, st, stream)
-        if ev:
-            ev[2].record(stream)
+        ev[3].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -260,7 +292,7 @@ def run_ours(args):
 
     clocks = ClockSampler(local)
     clocks.start()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -268,27 +300,41 @@ def run_ours(args):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
-    prev = t_start
-    reduce_ms, norm_ms, adamw_ms = [], [], []
     for i in range(args.steps):
-        step(evs[i])
+        if flush is not None:
+            flush.fill_(float(i))  # evicts the step's working set from L2; not timed
+            evs[i][0].record(stream)
+        step()
+        if flush is not None:
+            evs[i][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     clocks.mark(False)
     elapsed_ms = t_start.elapsed_time(t_end)
-    for i in range(args.steps):
-        reduce_ms.append(prev.elapsed_time(evs[i][0]))
-        norm_ms.append(evs[i][0].elapsed_time(evs[i][1]))
-        adamw_ms.append(evs[i][1].elapsed_time(evs[i][2]))
-        prev = evs[i][2]
+    if flush is not None:  # the flushes between steps are not part of the step
+        elapsed_ms = sum(e[0].elapsed_time(e[1]) for e in evs)
     if ws > 1:
         tt = torch.tensor([elapsed_ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         elapsed_ms = float(tt.item())
         dist.barrier()
     clk = clocks.stop()
+
+    # --- per-kernel breakdown: the same launches made one by one, an event after each --
+    n_split = min(args.steps, 20)
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_split)]
+    for i in range(n_split):
+        if flush is not None:
+            flush.fill_(float(i))
+        sev[i][0].record(stream)
+        step_split(sev[i])
+    torch.cuda.synchronize(dev)
+    reduce_ms = [e[0].elapsed_time(e[1]) for e in sev]
+    norm_ms = [e[1].elapsed_time(e[2]) for e in sev]
+    adamw_ms = [e[2].elapsed_time(e[3]) for e in sev]
     stt = z.zero_step_state_read(st, stream)
-    assert stt.t == args.warmup + args.steps and stt.skip == 0 and stt.norm == stt.norm
+    assert stt.t == args.warmup + args.steps + n_split and stt.skip == 0 and stt.norm == stt.norm
+    assert stt.error == 0
 
     # --- end to end through zero_step_host: gradients from pinned host memory -----------
     e2e = None
@@ -302,43 +348,56 @@ def run_ours(args):
 
     peak, peak_kind = _peaks()
     ms = elapsed_ms / args.steps
-    per_step = sorted(a + b + c for a, b, c in zip(reduce_ms, norm_ms, adamw_ms))
-
-    def pct(q):  # nearest-rank percentile of the per-step event times
-        return per_step[min(len(per_step) - 1, max(0, round(q / 100 * len(per_step)) - 1))]
+    if flush is not None:
+        per_step = sorted(e[0].elapsed_time(e[1]) for e in evs)
+        spread = {"p10": _pct(per_step, 10), "p50": _pct(per_step, 50), "p90": _pct(per_step, 90)}
+    else:
+        spread = None  # back-to-back steps: no event between them to keep launches overlapped
     params_per_s = wl.psi * args.steps * ws / (elapsed_ms / 1e3)
     bytes_26 = (26 + 2 * N) * P
-    bytes_mat = (34 + 2 * N) * P
+    moved = (30 + 2 * N) if launches == 1 else (34 + 2 * N)  # g written; re-read if split
     adamw_avg = statistics.mean(adamw_ms)
     reduce_avg = statistics.mean(reduce_ms)
     ach = ADAMW_BYTES * P / (adamw_avg / 1e3) / 1e9
     red_bytes = (2 * N + 4) * P
+    if launches == 1:
+        fused_bytes = (30 + 2 * N) * P
+        ach_f = fused_bytes / (ms / 1e3) / 1e9
+        roof = {"kernel": "k_step_fused (the whole step in one cooperative launch)",
+                "bound": "hbm", "achieved": ach_f, "peak": peak, "unit": "GB/s",
+                "frac": ach_f / peak, "peak_kind": peak_kind + ", burst figure of a kernel "
+                "timed alone", "traffic": None, "bytes_per_launch": fused_bytes,
+                "avg_launch_ms": ms,
+                "note": "latency-bound size: one launch per step, timed as the step"}
+    else:
+        roof = {"kernel": "k_adamw (fused AdamW + bf16 cast + gathered write)",
+                "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+                "peak_kind": peak_kind + ", burst figure of a kernel timed alone",
+                "traffic": _traffic_from_profile(P), "bytes_per_launch": ADAMW_BYTES * P,
+                "avg_launch_ms": adamw_avg}
     line = {
         "metric": METRIC, "value": params_per_s, "unit": "params/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-        "ms_per_step_spread": {"p10": pct(10), "p50": pct(50), "p90": pct(90)},
+        "ms_per_step_spread": spread,
         "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": _config({"parallelism": f"{ws} independent replica(s) of the simulated "
-                                          f"{N}-rank step" if ws > 1 else "1 GPU, 8 simulated ranks"},
+                                          f"{N}-rank step" if ws > 1 else f"1 GPU, {N} simulated ranks"},
                           psi=wl.psi, base=base),
         "hbm": {
             "gbs_at_26p2n_bytes": bytes_26 / (ms / 1e3) / 1e9,
             "pct_of_8tbs": 100 * bytes_26 / (ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
             "pct_of_measured_peak": 100 * bytes_26 / (ms / 1e3) / 1e9 / peak,
-            "gbs_at_34p2n_bytes_moved": bytes_mat / (ms / 1e3) / 1e9,
+            "bytes_per_param_moved": moved,
+            "gbs_moved": moved * P / (ms / 1e3) / 1e9,
             "note": "(26+2N) B/param is the headline roofline; an exact step must also write "
                     "and re-read the fp32 gradient (34+2N) because clipping needs the global "
-                    "norm before any update",
+                    "norm before any update; the single-launch step of small layouts keeps g "
+                    "on chip (30+2N: g is written for the caller but not read back)",
         },
-        "roofline": {
-            "kernel": "k_adamw (fused AdamW + bf16 cast + gathered write)",
-            "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-            "peak_kind": peak_kind + ", burst figure of a kernel timed alone",
-            "traffic": _traffic_from_profile(P), "bytes_per_launch": ADAMW_BYTES * P,
-            "avg_launch_ms": adamw_avg,
-        },
+        "roofline": roof,
         "kernels": {
+            "timing": f"{n_split} extra steps made of the separate calls, an event after each",
             "k_reduce": {"avg_ms": reduce_avg, "bytes_per_launch": red_bytes,
                          "gbs": red_bytes / (reduce_avg / 1e3) / 1e9} if nb == 1 else
                         {"launches_per_step": nb, "avg_ms_all_buckets": reduce_avg,
@@ -347,23 +406,30 @@ def run_ours(args):
             "k_finalize": {"avg_ms": statistics.mean(norm_ms)},
             "k_adamw": {"avg_ms": adamw_avg, "bytes_per_launch": ADAMW_BYTES * P, "gbs": ach},
         },
-        "gpu_launches": (nb + 2) * args.steps,
+        "launches_per_step": launches,
+        "gpu_launches": launches * args.steps,
         "clocks": clk,
         "e2e": e2e,
         "final_state": {"t": stt.t, "norm": stt.norm, "clip_coef": stt.clip_coef},
     }
     if rank == 0 and not args.no_cpu_baseline:
-        v, dt, swl = cpu_oracle_baseline(6, 1 << 26, base)
+        sample = min(1 << 26, wl.psi)
+        reps_cpu = 6 * (1 << 26) // sample   # about the same CPU work at any workload size
+        v, dt, swl = cpu_oracle_baseline(reps_cpu, sample, base)
         line["cpu_baseline"] = {"value": v, "unit": "params/s", "cores": 1, "kind": "oracle",
-                                "sample": f"6 oracle steps of the {'Llama-7B' if base is W.C3 else 'GPT-2-1.5B'} "
-                                          f"recipe at psi={swl.psi} "
-                                          f"(N=8 bf16 copies, random fp32 state), {dt:.1f} s "
+                                "sample": f"{reps_cpu} oracle steps of the {_recipe_name(base)} "
+                                          f"recipe at psi={swl.psi} (N={swl.n_ranks} "
+                                          f"{swl.grad_dtype} copies), {dt:.1f} s "
                                           f"single-threaded"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
     return 0
+
+
+def _pct(sorted_vals, q):  # nearest-rank percentile
+    return sorted_vals[min(len(sorted_vals) - 1, max(0, round(q / 100 * len(sorted_vals)) - 1))]
 
 
 def _traffic_from_profile(psi_padded):
@@ -404,15 +470,16 @@ def _e2e(args, z, torch, dev, wl, hp, reps, g, partials, master, m, v, out, st, 
     for h, r in zip(hreps, reps):
         h.copy_(r)
     staging = torch.empty(2 * N * W, dtype=torch.int16, device=dev)
+    gdt = z.ZERO_F16 if wl.grad_dtype == "f16" else z.ZERO_BF16
     hstate = torch.empty(z.STATE_BYTES, dtype=torch.uint8, pin_memory=True)
     cs = torch.cuda.Stream(dev)
     steps = max(1, args.e2e_steps)
-    z.zero_step_host(lay, hp, z.ZERO_BF16, hreps, staging, staging.numel() * 2, g, partials,
+    z.zero_step_host(lay, hp, gdt, hreps, staging, staging.numel() * 2, g, partials,
                      master, m, v, out, st, hstate, stream, cs)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
     for _ in range(steps):
-        z.zero_step_host(lay, hp, z.ZERO_BF16, hreps, staging, staging.numel() * 2, g, partials,
+        z.zero_step_host(lay, hp, gdt, hreps, staging, staging.numel() * 2, g, partials,
                          master, m, v, out, st, hstate, stream, cs)
         stream.synchronize()  # the step's result (norm, flag, scale) is on the host
     dt = time.perf_counter() - t0
@@ -477,6 +544,9 @@ def run_sweep(args):
                     reread = N == 2 and not bucketed and not args.sweep_materialise
                     g_arg = None if reread else bufs["g"]
                     moved = 26 + 4 * N if reread else 34 + 2 * N
+                    launches = z.zero_step_launches(lay, z.ZERO_BF16)
+                    if launches == 1:  # one launch, g kept on chip (written when given)
+                        moved = 26 + 2 * N if reread else 30 + 2 * N
 
                     def step():
                         z.zero_step(lay, hp, z.ZERO_BF16, ptrs, g_arg, partials, bufs["master"],
@@ -507,7 +577,10 @@ def run_sweep(args):
                     print(json.dumps({
                         "sweep": True, "psi": psi, "n_ranks": N, "stage": stage,
                         "mode": "bucketed 2^27" if bucketed else "resident", "steps": steps,
-                        "schedule": "re-read copies" if reread else "materialise g",
+                        "schedule": ("single launch, g not written" if reread else
+                                     "single launch, g written") if launches == 1 else
+                                    ("re-read copies" if reread else "materialise g"),
+                        "launches_per_step": launches,
                         "launch": "cuda graph replay" if args.graph else "direct",
                         "ms_per_step": ms, "params_per_s": psi / (ms / 1e3),
                         "gbs_at_26p2n": (26 + 2 * N) * P / (ms / 1e3) / 1e9,
@@ -679,11 +752,9 @@ def run_offload(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     link = _link_bandwidth(torch, dev)
-    base = W.C3 if args.workload == "llama-7b" else W.C2
-    wl = base if args.psi in (None, base.psi) else W.scaled(base, args.psi)
-    lay = z.zero_partition(wl.psi, wl.n_ranks, wl.stage, 1, wl.bucket_elems)
+    wl = W.C2 if args.psi in (None, W.C2.psi) else W.scaled(W.C2, args.psi)
+    lay = z.zero_partition(wl.psi, wl.n_ranks, wl.stage)
     P, N = lay.psi_padded, lay.n_ranks
-    Wb, nb = lay.bucket_elems, lay.n_buckets
     hp = z.hparams(**wl.hp.__dict__)
     stream = torch.cuda.current_stream(dev)
     s = stream.cuda_stream
@@ -770,9 +841,11 @@ def main():
                     help="optimizer state (master/m/v) in pinned host memory, updated over "
                          "the CPU-GPU link")
     ap.add_argument("--sweep-n", default="2,4,8,16,64")
-    ap.add_argument("--workload", default="gpt2-1.5b", choices=["gpt2-1.5b", "llama-7b"],
+    ap.add_argument("--workload", default="gpt2-1.5b", choices=["gpt2-1.5b", "llama-7b", "c1"],
                     help="gpt2-1.5b: psi=1,557,611,200, N=8, ZeRO-2 (the headline); llama-7b: "
-                         "psi=6,738,415,616, N=8, ZeRO-3, 51 gradient buckets of 2^27 elements")
+                         "psi=6,738,415,616, N=8, ZeRO-3, 51 gradient buckets of 2^27 elements; "
+                         "c1: psi=1,000,003, N=4, fp16 copies, dynamic loss scale (latency-bound, "
+                         "L2 flushed before every step)")
     ap.add_argument("--psi", type=int, default=None,
                     help="profiling only: the same recipe at another size (default: the "
                          "GPT-2-1.5B buffer)")

@@ -297,11 +297,25 @@ int zero_adamw_cast_gather_host_state(const zero_layout_t* layout,
  *              N = 2 the second moves 34 instead of 38 B.  The reduce then stores no g
  *              and AdamW forms each g[i] again from the two copies with the same
  *              arithmetic (same bits).  ZERO_EINVAL for NULL g with any other layout.
- *   other arguments as in the three calls above.  3 + n_buckets - 1 kernel launches.
+ *   other arguments as in the three calls above.
+ * Launches: n_buckets + 2 kernels (the reduce per bucket, the norm, AdamW).  A small
+ * layout (one bucket, at most 128 tile slots per rank, and every one of its n_tiles tiles
+ * able to hold a resident block at once: up to a few million parameters) runs instead
+ * as ONE cooperative kernel with the same bits: each block reduces one tile and keeps
+ * its g in shared memory, the block that finishes last forms the global norm and the
+ * step's scalars, and every block then updates its tile.  g is still written when given
+ * (never read back), so such a step moves 2N + 30 bytes per parameter, 2N + 26 with
+ * g = NULL.  zero_step_launches tells which way a layout goes.
  * ------------------------------------------------------------------------------------- */
 int zero_step(const zero_layout_t* layout, const zero_adamw_hparams_t* hp, zero_dtype_t dtype,
               const void* const* replicas, float* g, double* partials, float* master, float* m,
               float* v, uint16_t* params, zero_step_state_t* st, zero_stream_t stream);
+
+/* Kernel launches one zero_step call makes for this layout and gradient type on the
+ * current device: 1 (the single-launch step) or n_buckets + 2.  ZERO_EINVAL (negative) for
+ * an invalid layout or dtype.  Enqueues nothing; the first call on a device queries the
+ * kernel's occupancy there. */
+int zero_step_launches(const zero_layout_t* layout, zero_dtype_t dtype);
 
 /* -------------------------------------------------------------------------------------
  * zero_step_host -- zero_step with the gradients in HOST memory.

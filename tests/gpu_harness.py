@@ -25,11 +25,14 @@ def dtype_code(wl) -> int:
 
 class GpuRun:
     def __init__(self, wl, bucket_elems: int = 0, device: str = "cuda:0", guarded: bool = True,
-                 hp=None, host_state: bool = False):
+                 hp=None, host_state: bool = False, split: bool = False):
         """host_state: master/m/v in page-locked host memory (the offloaded optimizer
-        state), updated by zero_adamw_cast_gather_host_state."""
+        state), updated by zero_adamw_cast_gather_host_state.  split: run each step as
+        the separate calls (reduce per bucket, norm, AdamW) even where zero_step would
+        take the single-launch path."""
         self.wl = wl
         self.host_state = host_state
+        self.split = split or host_state
         self.dev = torch.device(device)
         self.stream = torch.cuda.current_stream(self.dev)
         self.guarded = guarded
@@ -106,7 +109,7 @@ class GpuRun:
 
     def step(self, step: int) -> z.StepState:
         self.gen_grads(step)
-        if self.host_state:
+        if self.split:
             W, N, P = self.lay.bucket_elems, self.lay.n_ranks, self.lay.psi_padded
             ptrs = self.bucket_ptrs()
             for b in range(self.lay.n_buckets):
@@ -114,8 +117,9 @@ class GpuRun:
                                             b * W, min(W, P - b * W), self.g, self.partials,
                                             self.st, self.stream)
             z.zero_grad_norm(self.lay, self.hp, self.partials, self.st, self.stream)
-            z.zero_adamw_cast_gather_host_state(self.lay, self.hp, self.g, self.master, self.m,
-                                                self.v, self.out, self.st, self.stream)
+            adamw = z.zero_adamw_cast_gather_host_state if self.host_state else z.zero_adamw_cast_gather
+            adamw(self.lay, self.hp, self.g, self.master, self.m, self.v, self.out, self.st,
+                  self.stream)
         else:
             z.zero_step(self.lay, self.hp, dtype_code(self.wl), self.bucket_ptrs(), self.g,
                         self.partials, self.master, self.m, self.v, self.out, self.st, self.stream)

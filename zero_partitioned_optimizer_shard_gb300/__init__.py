@@ -230,6 +230,18 @@ def zero_step(layout: Layout, hp: HParams, dtype: int, replicas: Sequence, g, pa
         _ptr(master), _ptr(m), _ptr(v), _ptr(params), _ptr(st), _stream(stream)))
 
 
+def zero_step_launches(layout: Layout, dtype: int) -> int:
+    """Kernel launches of one zero_step call for this layout: 1 (single-launch step) or
+    n_buckets + 2."""
+    f = _lib().zero_step_launches
+    f.argtypes = [C.POINTER(Layout), C.c_int]
+    f.restype = C.c_int
+    n = f(C.byref(layout), dtype)
+    if n < 0:
+        _check("zero_step_launches", n)
+    return n
+
+
 def zero_step_host(layout: Layout, hp: HParams, dtype: int, host_replicas: Sequence, staging,
                    staging_bytes: int, g, partials, master, m, v, params, st,
                    host_state_out=None, stream=None, copy_stream=None) -> None:
@@ -259,6 +271,6 @@ __all__ = [
     "ZERO_F16", "ZERO_BF16", "Segment", "zero_partition", "zero_segment_map", "zero_workspace_bytes", "zero_step_state_init",
     "zero_step_state_read", "zero_step_state_write", "zero_reduce_shard_unscale",
     "zero_grad_norm", "zero_adamw_cast_gather", "zero_adamw_cast_gather_host_state", "zero_step",
-    "zero_step_host",
+    "zero_step_host", "zero_step_launches",
     "zero_step_static_workspace",
 ]

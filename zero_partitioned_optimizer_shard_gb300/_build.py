@@ -11,9 +11,9 @@ ROOT = os.path.dirname(PKG)
 OBJ = os.path.join(ROOT, "_build", "zero_shard")
 LIB = os.path.join(PKG, "libzero_shard.so")
 SOURCES = ["partition.cu", "reduce.cu", "finalize.cu", "adamw.cu", "adamw_variants.cu", "api.cu",
-           "noalloc.cu"]
-HEADERS = [os.path.join(CSRC, "zero_internal.h"), os.path.join(CSRC, "adamw_elem.cuh"),
-           os.path.join(ROOT, "include", "zero.h")]
+           "noalloc.cu", "fused.cu"]
+HEADERS = [os.path.join(CSRC, h) for h in ("zero_internal.h", "adamw_elem.cuh", "reduce_elem.cuh",
+                                           "step_scalars.cuh")] + [os.path.join(ROOT, "include", "zero.h")]
 
 ARCH = os.environ.get("ZERO_CUDA_ARCH", "103a")
 NVCC_FLAGS = [

@@ -343,6 +343,28 @@ extern "C" int zero_step(const zero_layout_t* layout, const zero_adamw_hparams_t
     if (!aligned16(partials))
         return ZERO_EALIGN;
     const cudaStream_t s = (cudaStream_t)stream;
+    if (fused_fits(layout, dtype)) {
+        // small layout: the whole step in one launch, with the same bits (fused.cu)
+        FusedArgs f;
+        memset(&f, 0, sizeof f);
+        for (uint64_t k = 0; k < N; ++k)
+            f.rep[k] = replicas[k];
+        f.g = g;
+        f.partials = partials;
+        f.master = master;
+        f.m = m;
+        f.v = v;
+        f.out = params;
+        f.st = st;
+        f.psi = layout->psi;
+        f.psi_padded = P;
+        f.shard = layout->shard;
+        f.tiles_per_rank = layout->tiles_per_rank;
+        f.n_ranks = layout->n_ranks;
+        f.out_f16 = hp->params_dtype == ZERO_F16 ? 1u : 0u;
+        f.hp = *hp;
+        return cuda_status(launch_step_fused(f, dtype, layout->n_tiles, s));
+    }
     for (uint64_t b = 0; b < layout->n_buckets; ++b) {
         const uint64_t begin = b * W, count = begin + W < P ? W : P - begin;
         rc = reduce_window(layout, dtype, replicas + b * N, begin, count, g, partials, st, s);
@@ -356,6 +378,13 @@ extern "C" int zero_step(const zero_layout_t* layout, const zero_adamw_hparams_t
         return adamw_rereduce(layout, hp, dtype, replicas[0], replicas[1], master, m, v, params,
                               st, s);
     return adamw(layout, hp, g, master, m, v, params, st, s);
+}
+
+extern "C" int zero_step_launches(const zero_layout_t* layout, zero_dtype_t dtype)
+{
+    if (!kernel_layout_ok(layout) || (dtype != ZERO_F16 && dtype != ZERO_BF16))
+        return ZERO_EINVAL;
+    return fused_fits(layout, dtype) ? 1 : (int)(layout->n_buckets + 2);
 }
 
 extern "C" int zero_step_host(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,

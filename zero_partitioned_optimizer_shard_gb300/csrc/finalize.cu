@@ -29,29 +29,10 @@
  * is the same on any GPU.  All partial slots end at zero, ready for the next step's
  * reduce windows.
  */
-#include "zero_internal.h"
-
-#include <math.h>
+#include "step_scalars.cuh"
 
 namespace zero {
 namespace {
-
-/* beta^e in fp64 by binary exponentiation: about log2(e) squarings and popcount(e)
- * multiplications, each correctly rounded.  On GB300's narrow fp64 pipe this chain is
- * about 2 us shorter than pow(), whose result it matches to a few ulp (the bias
- * corrections are rounded to fp32 once, as with pow). */
-__device__ __forceinline__ double pow_uint(double beta, uint32_t e)
-{
-    double r = 1.0;
-    while (e) {
-        if (e & 1u)
-            r *= beta;
-        e >>= 1;
-        if (e)
-            beta *= beta;
-    }
-    return r;
-}
 
 constexpr int kFinThreads = 256;
 constexpr int kFinWarps = kFinThreads / 32;
@@ -81,36 +62,11 @@ __global__ void __launch_bounds__(kFinThreads) k_finalize(const __grid_constant_
         __syncthreads();
         const uint32_t t = s_t + 1;  // the step count if this step is applied
         if (lane == 0 && w == 1 && !s_overflow)
-            st->step_size = (float)((double)a.hp.lr / (1.0 - pow_uint((double)a.hp.beta1, t)));
+            st->step_size = bias_step_size(a.hp, t);
         if (lane == 0 && w == 2 && !s_overflow)
-            st->rbc2 = (float)sqrt(1.0 - pow_uint((double)a.hp.beta2, t));
-        if (lane == 0 && w == 3) {
-            st->inv_scale_used = st->inv_scale;  // this step's unscale, for a re-reading AdamW
-            float L = st->loss_scale;
-            if (s_overflow) {
-                st->skip = 1;
-                st->n_skipped += 1;
-                if (st->dynamic) {
-                    const float half = L * 0.5f;
-                    L = half < 1.0f ? 1.0f : half;
-                    st->good_steps = 0;
-                }
-            } else {
-                st->t = t;
-                st->skip = 0;
-                st->decay = (float)(1.0 - (double)a.hp.lr * (double)a.hp.weight_decay);
-                if (st->dynamic && st->growth_interval > 0) {
-                    st->good_steps += 1;
-                    if (st->good_steps == st->growth_interval) {
-                        const float twice = L * 2.0f;
-                        L = twice > 16777216.0f ? 16777216.0f : twice;
-                        st->good_steps = 0;
-                    }
-                }
-            }
-            st->loss_scale = L;
-            st->inv_scale = (float)(1.0 / ((double)N * (double)L));
-        }
+            st->rbc2 = bias_rbc2(a.hp, t);
+        if (lane == 0 && w == 3)
+            scaler_update(st, a.hp, N, s_overflow, t);
     } else {
         // this block's chunk [j0, j1) of every rank's tile partials: one warp per rank,
         // each lane adds its slots in order, a fixed shuffle tree folds the warp.  The
@@ -182,12 +138,7 @@ __global__ void __launch_bounds__(kFinThreads) k_finalize(const __grid_constant_
     const double norm = sqrt(total);
     st->sumsq = total;
     st->norm = norm;
-    float c = 1.0f;
-    if (!__ldcg(&st->skip) && a.hp.max_grad_norm > 0.0f) {
-        const double cc = (double)a.hp.max_grad_norm / (norm + 1e-6);
-        c = cc < 1.0 ? (float)cc : 1.0f;
-    }
-    st->clip_coef = c;
+    st->clip_coef = clip_coefficient(norm, __ldcg(&st->skip), a.hp.max_grad_norm);
     st->overflow = 0;
     st->n_steps += 1;
 }

@@ -1,0 +1,492 @@
+/*
+ * fused.cu -- the whole step in one launch for small layouts (k_step_fused).
+ *
+ * Below a few million parameters the three-launch step (reduce, norm, AdamW) is bound by
+ * latency, not bandwidth: each launch costs a few microseconds of ramp-up and drain, the
+ * norm kernel's chain of fp64 operations sits between the other two, and the fp32
+ * gradient makes a round trip through memory.  When every tile of the layout can have a
+ * block resident at the same time, one cooperative launch does it all:
+ *
+ *   1. block u takes tile u of the sum-of-squares grid (a shard cut at the flat multiples
+ *      of 8192, as in the reduce pass) and forms g there with the reduce pass's own
+ *      arithmetic and thread-to-element mapping (reduce_elem.cuh), so g and the tile's
+ *      partial come out with the same bits; g stays in shared memory (and is written to
+ *      the caller's g buffer when one is given);
+ *   2. the block stores its tile partial, ORs its overflow flag and arrives on the step
+ *      state's arrival counter; the last block to arrive forms the global norm from the
+ *      partials in the norm kernel's order (one warp per rank, the rank's slots
+ *      lane-strided, a fixed shuffle tree, ranks in order; the order finalize.cu uses for
+ *      layouts of at most 128 tiles per rank), applies the clip coefficient, skip
+ *      decision and loss scaler (step_scalars.cuh), zeroes the partials and releases the
+ *      other blocks by resetting the counter;
+ *   3. every block applies AdamW to its tile from the g it holds (adamw_elem.cuh), reading
+ *      master, m and v that were prefetched into L2 while step 1 ran, and writes the
+ *      gathered parameters.
+ *
+ * So the results are bit-identical to the three-launch step, and the traffic is
+ * 2N + 26 bytes per parameter (+4 when g is written), not 2N + 34.  "【论文解读】ZeRO"
+ * sec. 6(2) describes the same three stages per rank (reduce-scatter, shard update,
+ * all-gather); only their scheduling differs.
+ *
+ * Waiting: the launch is cooperative (every block resident at once), and a block that
+ * waits for the last one gives up after ~2 s, records 1 in the step state's error word and
+ * writes nothing more.  A ninth warp computes the bias corrections of step t+1 while the
+ * eight others stream the gradients, so the fp64 powers never sit on the critical path.
+ */
+#include "adamw_elem.cuh"
+#include "reduce_elem.cuh"
+#include "step_scalars.cuh"
+
+namespace zero {
+namespace {
+
+#ifdef ZERO_TEST_HOOKS
+/* Test builds only (never the product library): the bounded-wait test names one block
+ * that leaves without arriving, so the other blocks' wait for the last one runs out
+ * without any fault. */
+__device__ unsigned long long zero_test_absent_block = ~0ull;
+#endif
+
+constexpr int kFusedWarps = 8;                       // stream gradients and state
+constexpr int kFusedThreads = kFusedWarps * 32;      // the reduce pass's block size
+constexpr int kFusedBlock = kFusedThreads + 32;      // + one warp for the scalar chains
+constexpr int kFusedLoads = 8;                       // replica loads in flight per thread
+constexpr uint64_t kT = ZERO_TILE_ELEMS;
+
+static_assert(kFusedThreads == 256, "the tile partial's bits depend on the reduce pass's block size");
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+/* Arrival on the counter: acquire-release, so this block's writes are ordered before it
+ * and the last block to arrive sees every block's writes. */
+__device__ __forceinline__ uint32_t arrive_acq_rel(uint32_t* p)
+{
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+    return old;
+}
+
+/* L2 prefetch of [p, p + n) floats, rounded inwards to 16-byte boundaries (a hint: the
+ * data is read with ordinary loads later). */
+__device__ __forceinline__ void prefetch_l2(const float* p, uint64_t n)
+{
+    const uintptr_t a0 = ((uintptr_t)p + 15u) & ~(uintptr_t)15u;
+    const uintptr_t a1 = ((uintptr_t)(p + n)) & ~(uintptr_t)15u;
+    if (a1 > a0)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                     ::"l"(a0), "r"((uint32_t)(a1 - a0)) : "memory");
+}
+
+/* AdamW of one element i < psi, or the padding's gathered 0. */
+__device__ __forceinline__ void update_one(const FusedArgs& a, uint64_t i, float g, const Scalars& s)
+{
+    if (i < a.psi) {
+        float p = a.master[i], m = a.m[i], v = a.v[i];
+        const float r = adamw_one(g, p, m, v, s);
+        a.master[i] = p;
+        a.m[i] = m;
+        a.v[i] = v;
+        a.out[i] = a.out_f16 ? pack1<true>(r) : pack1<false>(r);
+    } else {
+        a.out[i] = 0;
+    }
+}
+
+template <zero_dtype_t DT, int NR>
+__global__ void __launch_bounds__(kFusedBlock, 3) k_step_fused(const __grid_constant__ FusedArgs a)
+{
+    __shared__ __align__(16) float gc[kT + 8];  // the tile's g, from its first whole group
+    __shared__ double warp_part[2][kFusedWarps];
+    __shared__ double rank_sum[ZERO_MAX_KERNEL_RANKS];
+    __shared__ float s_step, s_rbc2;
+    __shared__ Scalars s_sc;
+    __shared__ __align__(16) zero_step_state_t s_st;  // the state as this step found it
+    __shared__ uint32_t s_flag;  // last block; then: go on to the update
+    grid_launch_dependents();
+    grid_dependency_wait();
+    zero_step_state_t* st = a.st;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t N = NR > 0 ? (uint32_t)NR : a.n_ranks;
+    const float inv = st->inv_scale;
+
+    // this block's tile: slot u = r * tiles_per_rank + j
+    const uint64_t u = blockIdx.x, tpr = a.tiles_per_rank;
+    const uint64_t r = u / tpr, j = u - r * tpr;
+    const uint64_t shard_lo = r * a.shard, shard_hi = shard_lo + a.shard;
+    const uint64_t cell = (shard_lo / kT + j) * kT;
+    const uint64_t lo = cell > shard_lo ? cell : shard_lo;
+    const uint64_t hi = cell + kT < shard_hi ? cell + kT : shard_hi;
+    const uint64_t base = lo & ~7ull;  // first group of the tile; gc[i - base] holds g[i]
+
+    if (w == kFusedWarps) {
+        // a copy of the state for the last block (no block writes it before the last one
+        // arrives), and the bias corrections of step t+1: lanes 0 and 1 run the two fp64
+        // power chains side by side
+        if (lane < (int)(sizeof(zero_step_state_t) / 16))
+            reinterpret_cast<uint4*>(&s_st)[lane] = __ldcg(reinterpret_cast<const uint4*>(st) + lane);
+        if (lane < 2) {
+            const uint32_t t_next = st->t + 1;
+            if (lane == 0)
+                s_step = bias_step_size(a.hp, t_next);
+            else
+                s_rbc2 = bias_rbc2(a.hp, t_next);
+        }
+        if (lane == 2 && lo < hi) {
+            prefetch_l2(a.master + lo, hi - lo);
+            prefetch_l2(a.m + lo, hi - lo);
+            prefetch_l2(a.v + lo, hi - lo);
+        }
+    }
+
+    // 1. g over the tile: the reduce pass's groups and order; several groups' loads in
+    // flight per thread before their ordered sums
+    SumSq acc;
+    bool bad = false;
+    if (w < kFusedWarps && lo < hi) {
+        constexpr int GB = NR > 0 && NR < kFusedLoads ? kFusedLoads / NR : 1;  // groups per batch
+        for (uint64_t b0 = base + 8ull * threadIdx.x; b0 < hi; b0 += 8ull * kFusedThreads * GB) {
+            uint4 v[GB][NR > 0 && NR < kFusedLoads ? NR : kFusedLoads];
+            if (NR > 0 && NR < kFusedLoads) {
+#pragma unroll
+                for (int q = 0; q < GB; ++q) {
+                    const uint64_t b = b0 + 8ull * kFusedThreads * q;
+                    if (b < hi && b + 8 <= a.psi_padded) {
+#pragma unroll
+                        for (int k = 0; k < (NR > 0 ? NR : 1); ++k)
+                            v[q][k] = ld_stream_v4((const uint16_t*)a.rep[k] + b);
+                    }
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < GB; ++q) {
+                const uint64_t b = b0 + 8ull * kFusedThreads * q;
+                if (b >= hi)
+                    break;
+                float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                if (b + 8 <= a.psi_padded) {
+                    if (NR > 0 && NR < kFusedLoads) {
+#pragma unroll
+                        for (int k = 0; k < (NR > 0 ? NR : 1); ++k)
+                            add8<DT>(s, v[q][k]);
+                    } else {
+#pragma unroll 1
+                        for (uint32_t k0 = 0; k0 < N; k0 += kFusedLoads) {
+#pragma unroll
+                            for (int kk = 0; kk < kFusedLoads; ++kk)
+                                if (k0 + kk < N)
+                                    v[0][kk] = ld_stream_v4((const uint16_t*)a.rep[k0 + kk] + b);
+#pragma unroll
+                            for (int kk = 0; kk < kFusedLoads; ++kk)
+                                if (k0 + kk < N)
+                                    add8<DT>(s, v[0][kk]);
+                        }
+                    }
+                } else {  // the buffer's last, ragged group: element loads inside the tile
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const uint64_t i = b + e;
+                        if (i >= lo && i < hi)
+                            for (uint32_t k = 0; k < N; ++k)
+                                s[e] = __fadd_rn(s[e], one16<DT>(ld_stream_u16((const uint16_t*)a.rep[k] + i)));
+                    }
+                }
+                float gv[8];
+                uint32_t in;
+                bool full;
+                group_values(a.psi, inv, s, b, lo, hi, acc, bad, gv, in, full);
+                float* c = gc + (b - base);
+                if (full) {
+                    *reinterpret_cast<float4*>(c) = make_float4(gv[0], gv[1], gv[2], gv[3]);
+                    *reinterpret_cast<float4*>(c + 4) = make_float4(gv[4], gv[5], gv[6], gv[7]);
+                    if (a.g) {
+                        __stcs(reinterpret_cast<float4*>(a.g + b), make_float4(gv[0], gv[1], gv[2], gv[3]));
+                        __stcs(reinterpret_cast<float4*>(a.g + b + 4), make_float4(gv[4], gv[5], gv[6], gv[7]));
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        if (in >> e & 1u) {
+                            c[e] = gv[e];
+                            if (a.g)
+                                a.g[b + e] = gv[e];
+                        }
+                }
+            }
+        }
+    }
+
+    // 2. the tile's partial (the reduce pass's fold), the overflow flag, and arrival
+    uint32_t parity = 0;
+    const double part = tile_fold<kFusedThreads>(acc, warp_part, parity);
+    if (threadIdx.x == 0 && lo < hi)
+        __stcg(a.partials + u, part);
+    if (__any_sync(0xffffffffu, bad) && lane == 0)
+        atomicOr(&st->overflow, 1u);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+#ifdef ZERO_TEST_HOOKS
+        if (blockIdx.x == zero_test_absent_block)
+            s_flag = 2;  // test builds only: this block never arrives
+        else
+#endif
+        s_flag = arrive_acq_rel(&st->arrivals) == gridDim.x - 1;
+    }
+    __syncthreads();
+#ifdef ZERO_TEST_HOOKS
+    if (s_flag == 2)
+        return;
+#endif
+
+    if (s_flag) {
+        // the last block: the norm in the norm kernel's order (at most 128 slots per
+        // rank: lane l adds slots l, l+32, l+64, l+96 in that order), partials zeroed
+        for (uint32_t rr = w; rr < N; rr += kFusedWarps + 1) {
+            double* p = a.partials + (uint64_t)rr * tpr;
+            double v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint64_t c = lane + 32u * q;
+                v[q] = c < tpr ? __ldcg(p + c) : 0.0;
+            }
+            double s = 0.0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint64_t c = lane + 32u * q;
+                if (c < tpr) {
+                    s += v[q];
+                    p[c] = 0.0;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (lane == 0)
+                rank_sum[rr] = s;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            // the step's scalars on the shared-memory copy, then written back whole; the
+            // counter is reset last, by a release store, which lets the others go on
+            double total = 0.0;
+            for (uint32_t rr = 0; rr < N; ++rr)
+                total += rank_sum[rr];
+            zero_step_state_t& ls = s_st;
+            const uint32_t overflow = __ldcg(&st->overflow) != 0;
+            const uint32_t t_next = ls.t + 1;
+            if (!overflow) {
+                ls.step_size = s_step;
+                ls.rbc2 = s_rbc2;
+            }
+            scaler_update(&ls, a.hp, N, overflow, t_next);
+            const double norm = sqrt(total);
+            ls.sumsq = total;
+            ls.norm = norm;
+            ls.clip_coef = clip_coefficient(norm, overflow, a.hp.max_grad_norm);
+            ls.overflow = 0;
+            ls.n_steps += 1;
+            ls.arrivals = gridDim.x;  // still "not released" until the store below
+            ls.error |= __ldcg(&st->error);
+            for (int q = 0; q < (int)(sizeof(zero_step_state_t) / 16); ++q)
+                __stcg(reinterpret_cast<uint4*>(st) + q, reinterpret_cast<const uint4*>(&ls)[q]);
+            st_release_u32(&st->arrivals, 0u);
+            s_flag = 1;
+        }
+    } else if (threadIdx.x == 0) {
+        // wait for the last block to reset the counter, at most ~2 s
+        const long long t0 = clock64();
+        uint32_t ok = 1;
+        while (ld_acquire_u32(&st->arrivals) != 0) {
+            if (clock64() - t0 > 4000000000LL) {
+                ok = 0;
+                atomicOr(&st->error, 1u);
+                break;
+            }
+            __nanosleep(64);
+        }
+        s_flag = ok;
+    }
+    __syncthreads();
+    if (!s_flag)
+        return;
+
+    // 3. AdamW over the tile from the g held in shared memory
+    if (threadIdx.x == 0) {
+        s_flag = __ldcg(&st->skip) == 0;
+        s_sc.c = __ldcg(&st->clip_coef);
+        s_sc.step = __ldcg(&st->step_size);
+        s_sc.rbc2 = __ldcg(&st->rbc2);
+        s_sc.decay = __ldcg(&st->decay);
+        s_sc.b1 = a.hp.beta1;
+        s_sc.b2 = a.hp.beta2;
+        s_sc.omb1 = __fsub_rn(1.0f, a.hp.beta1);
+        s_sc.omb2 = __fsub_rn(1.0f, a.hp.beta2);
+        s_sc.eps = a.hp.eps;
+    }
+    __syncthreads();
+    if (!s_flag || lo >= hi)
+        return;
+    const Scalars& sc = s_sc;
+    const uint64_t v_lo = (lo + 3) & ~3ull, v_hi = hi & ~3ull;  // 16-byte-aligned body
+    if (v_lo >= v_hi) {
+        for (uint64_t i = lo + threadIdx.x; i < hi; i += kFusedBlock)
+            update_one(a, i, gc[i - base], sc);
+        return;
+    }
+    if (lo + threadIdx.x < v_lo)
+        update_one(a, lo + threadIdx.x, gc[lo + threadIdx.x - base], sc);
+    if (v_hi + threadIdx.x < hi)
+        update_one(a, v_hi + threadIdx.x, gc[v_hi + threadIdx.x - base], sc);
+    // three 4-element groups per thread at a time: all their loads before any store (the
+    // arrays may alias as far as the compiler knows, so it would not hoist them itself)
+    constexpr int Q = 3;
+    const uint64_t v_end = v_hi < (a.psi & ~3ull) ? v_hi : (a.psi & ~3ull);  // groups all < psi
+    for (uint64_t i0 = v_lo + 4ull * threadIdx.x; i0 < v_hi; i0 += 4ull * kFusedBlock * Q) {
+        float4 p4[Q], m4[Q], v4[Q];
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            const uint64_t i = i0 + 4ull * kFusedBlock * q;
+            if (i < v_end) {
+                p4[q] = __ldcs(reinterpret_cast<const float4*>(a.master + i));
+                m4[q] = __ldcs(reinterpret_cast<const float4*>(a.m + i));
+                v4[q] = __ldcs(reinterpret_cast<const float4*>(a.v + i));
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            const uint64_t i = i0 + 4ull * kFusedBlock * q;
+            if (i >= v_hi)
+                break;
+            if (i < v_end) {
+                const float4 g4 = *reinterpret_cast<const float4*>(gc + (i - base));
+                uint2 o;
+                if (a.out_f16) {
+                    o.x = pack2<true>(adamw_one(g4.x, p4[q].x, m4[q].x, v4[q].x, sc),
+                                      adamw_one(g4.y, p4[q].y, m4[q].y, v4[q].y, sc));
+                    o.y = pack2<true>(adamw_one(g4.z, p4[q].z, m4[q].z, v4[q].z, sc),
+                                      adamw_one(g4.w, p4[q].w, m4[q].w, v4[q].w, sc));
+                } else {
+                    o.x = pack2<false>(adamw_one(g4.x, p4[q].x, m4[q].x, v4[q].x, sc),
+                                       adamw_one(g4.y, p4[q].y, m4[q].y, v4[q].y, sc));
+                    o.y = pack2<false>(adamw_one(g4.z, p4[q].z, m4[q].z, v4[q].z, sc),
+                                       adamw_one(g4.w, p4[q].w, m4[q].w, v4[q].w, sc));
+                }
+                __stcs(reinterpret_cast<float4*>(a.master + i), p4[q]);
+                __stcs(reinterpret_cast<float4*>(a.m + i), m4[q]);
+                __stcs(reinterpret_cast<float4*>(a.v + i), v4[q]);
+                __stcs(reinterpret_cast<uint2*>(a.out + i), o);
+            } else {  // the group holding psi, or padding: element by element
+                for (int e = 0; e < 4; ++e)
+                    update_one(a, i + e, gc[i + e - base], sc);
+            }
+        }
+    }
+}
+
+template <zero_dtype_t DT, int NR>
+struct FusedKernel {
+    static int capacity()  // blocks that can be resident at once, cached per device
+    {
+        static int cap[64] = {0};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        int& c = cap[dev & 63];
+        if (c == 0) {
+            int o = 0;
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, k_step_fused<DT, NR>, kFusedBlock, 0);
+            c = o > 0 ? o * sm_count() : -1;
+        }
+        return c;
+    }
+    static cudaError_t launch(const FusedArgs& a, unsigned grid, cudaStream_t s)
+    {
+        // cooperative (all blocks resident together) and, where the driver accepts the
+        // pair, programmatic dependent launch; the choice is remembered per device
+        static int mode[64] = {0};  // 0 unknown, 1 both attributes, 2 cooperative only
+        int dev = 0;
+        cudaGetDevice(&dev);
+        int& md = mode[dev & 63];
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(kFusedBlock);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = s;
+        cudaLaunchAttribute at[2];
+        at[0].id = cudaLaunchAttributeCooperative;
+        at[0].val.cooperative = 1;
+        at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = at;
+        if (md != 2) {
+            cfg.numAttrs = 2;
+            cudaError_t e = cudaLaunchKernelEx(&cfg, k_step_fused<DT, NR>, a);
+            if (e == cudaSuccess) {
+                md = 1;
+                return e;
+            }
+            if (md == 1)
+                return e;
+            cudaGetLastError();  // the pair was refused: clear it, use cooperative alone
+            md = 2;
+        }
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, k_step_fused<DT, NR>, a);
+    }
+};
+
+template <zero_dtype_t DT>
+int capacity_dt(uint32_t n)
+{
+    switch (n) {
+    case 2: return FusedKernel<DT, 2>::capacity();
+    case 4: return FusedKernel<DT, 4>::capacity();
+    case 8: return FusedKernel<DT, 8>::capacity();
+    default: return FusedKernel<DT, 0>::capacity();
+    }
+}
+
+template <zero_dtype_t DT>
+cudaError_t launch_dt(const FusedArgs& a, unsigned grid, cudaStream_t s)
+{
+    switch (a.n_ranks) {
+    case 2: return FusedKernel<DT, 2>::launch(a, grid, s);
+    case 4: return FusedKernel<DT, 4>::launch(a, grid, s);
+    case 8: return FusedKernel<DT, 8>::launch(a, grid, s);
+    default: return FusedKernel<DT, 0>::launch(a, grid, s);
+    }
+}
+
+}  // namespace
+
+#ifdef ZERO_TEST_HOOKS
+extern "C" int zero_test_absent_fused_block(unsigned long long block)
+{
+    return cudaMemcpyToSymbol(zero_test_absent_block, &block, sizeof block) == cudaSuccess ? 0 : -4;
+}
+#endif
+
+bool fused_fits(const zero_layout_t* L, zero_dtype_t dtype)
+{
+    if (L->n_buckets != 1 || L->tiles_per_rank > kFusedMaxTilesPerRank)
+        return false;
+    const int cap = dtype == ZERO_F16 ? capacity_dt<ZERO_F16>(L->n_ranks)
+                                      : capacity_dt<ZERO_BF16>(L->n_ranks);
+    return cap > 0 && L->n_tiles <= (uint64_t)cap;
+}
+
+cudaError_t launch_step_fused(const FusedArgs& a, zero_dtype_t dtype, uint64_t n_tiles, cudaStream_t s)
+{
+    return dtype == ZERO_F16 ? launch_dt<ZERO_F16>(a, (unsigned)n_tiles, s)
+                             : launch_dt<ZERO_BF16>(a, (unsigned)n_tiles, s);
+}
+
+}  // namespace zero

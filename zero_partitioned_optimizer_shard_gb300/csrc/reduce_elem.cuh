@@ -1,0 +1,217 @@
+/*
+ * reduce_elem.cuh -- the element arithmetic of the reduce-scatter pass, shared by the
+ * reduce kernel (reduce.cu) and the single-launch step for small layouts (fused.cu), so
+ * both compute the same bits: 16-bit gradient decoding, streaming loads, the rank-ordered
+ * fp32 sum, the unscaled group values with their padding and tile masks, the error-free
+ * sum of squares and its fixed-order fold per tile.
+ */
+#pragma once
+
+#include "zero_internal.h"
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace zero {
+namespace {
+
+template <zero_dtype_t DT>
+__device__ __forceinline__ float lo16(uint32_t w);
+template <zero_dtype_t DT>
+__device__ __forceinline__ float hi16(uint32_t w);
+
+template <>
+__device__ __forceinline__ float lo16<ZERO_BF16>(uint32_t w) { return __uint_as_float(w << 16); }
+template <>
+__device__ __forceinline__ float hi16<ZERO_BF16>(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+template <>
+__device__ __forceinline__ float lo16<ZERO_F16>(uint32_t w)
+{
+    return __half2float(__ushort_as_half((unsigned short)(w & 0xffffu)));
+}
+template <>
+__device__ __forceinline__ float hi16<ZERO_F16>(uint32_t w)
+{
+    return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+}
+
+template <zero_dtype_t DT>
+__device__ __forceinline__ float one16(uint16_t b)
+{
+    return lo16<DT>((uint32_t)b);
+}
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p)
+{
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint16_t ld_stream_u16(const void* p)
+{
+    unsigned short v;
+    asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+template <zero_dtype_t DT>
+__device__ __forceinline__ void add8(float (&s)[8], const uint4& v)
+{
+    s[0] = __fadd_rn(s[0], lo16<DT>(v.x));
+    s[1] = __fadd_rn(s[1], hi16<DT>(v.x));
+    s[2] = __fadd_rn(s[2], lo16<DT>(v.y));
+    s[3] = __fadd_rn(s[3], hi16<DT>(v.y));
+    s[4] = __fadd_rn(s[4], lo16<DT>(v.z));
+    s[5] = __fadd_rn(s[5], hi16<DT>(v.z));
+    s[6] = __fadd_rn(s[6], lo16<DT>(v.w));
+    s[7] = __fadd_rn(s[7], hi16<DT>(v.w));
+}
+
+/* Sum of squares of the fp32 gradient, carried as an unevaluated pair hi + lo of fp32
+ * values.  TwoProduct: x*x = p + pe exactly (FMA); TwoSum: hi + p = s + err exactly.
+ * The values are scaled by 2^24 first (exact) and the tile's total by 2^-48 at the end,
+ * which moves the range where every step is exact and nothing can overflow (1024 squares
+ * per warp before the fp64 fold) to |x| in [2^-74, 2^34), plus zeros: gradients of
+ * ~1e-4 often come within 2^-50 of zero, which unscaled would need the fp64 path.
+ * Power-of-two scaling changes no rounding, so the result is the unscaled pair sum's.
+ * Groups holding anything outside that range take the fp64 path below. */
+constexpr float kSqScale = 16777216.0f;  // 2^24
+constexpr double kSqUnscale = 0x1p-48;
+struct SumSq {
+    float hi = 0.0f, lo = 0.0f;
+    double wide = 0.0;
+
+    __device__ __forceinline__ void add_fast(float x)
+    {
+        const float p = __fmul_rn(x, x);
+        const float pe = __fmaf_rn(x, x, -p);
+        const float s = __fadd_rn(hi, p);
+        const float bb = __fsub_rn(s, hi);
+        const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(p, bb));
+        hi = s;
+        lo = __fadd_rn(lo, __fadd_rn(err, pe));
+    }
+};
+
+/* True when all 8 values are finite and every scaled square is exact in the fp32 pair
+ * arithmetic: magnitudes in [2^-74, 2^34) or zero.  Integer compares on the magnitude
+ * bits, so NaN (above inf) and inf fail the test too. */
+__device__ __forceinline__ bool squares_in_range(const float (&x)[8])
+{
+    uint32_t mx = 0u, mn = 0x3f800000u;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const uint32_t u = __float_as_uint(x[e]) & 0x7fffffffu;
+        mx = max(mx, u);
+        mn = min(mn, u == 0u ? 0x3f800000u : u);
+    }
+    return mx < 0x50800000u && mn >= 0x1a800000u;  // 2^34 and 2^-74
+}
+
+/* fp64 sum of squares of the elements of a group selected by mask; a real call, so the
+ * fp64 work runs only for the rare groups that need it. */
+__device__ __noinline__ double sumsq_wide(float x0, float x1, float x2, float x3, float x4, float x5,
+                                          float x6, float x7, uint32_t mask)
+{
+    const float x[8] = {x0, x1, x2, x3, x4, x5, x6, x7};
+    double t = 0.0;
+    for (int e = 0; e < 8; ++e)
+        if (mask >> e & 1u)
+            t += (double)x[e] * (double)x[e];
+    return t;
+}
+
+/* hi1 + lo1 += hi2 + lo2 in pair arithmetic (TwoSum on the leading parts). */
+__device__ __forceinline__ void pair_add(float& hi, float& lo, float h2, float l2)
+{
+    const float s = __fadd_rn(hi, h2);
+    const float bb = __fsub_rn(s, hi);
+    const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(h2, bb));
+    hi = s;
+    lo = __fadd_rn(__fadd_rn(lo, l2), err);
+}
+
+__device__ __forceinline__ bool not_finite(float x)
+{
+    return (__float_as_uint(x) & 0x7f800000u) == 0x7f800000u;
+}
+
+/* Elements b .. b+7 once their rank sums s[] are known: unscale (gv), zero the padding,
+ * mask what lies outside the tile [lo, hi) (bit e of `in` set for the tile's elements),
+ * add the tile's squares to acc and flag its non-finite values.  `full`: all 8 elements
+ * belong to the tile. */
+__device__ __forceinline__ void group_values(uint64_t psi, float inv, const float (&s)[8], uint64_t b,
+                                             uint64_t lo, uint64_t hi, SumSq& acc, bool& bad,
+                                             float (&gv)[8], uint32_t& in, bool& full)
+{
+    full = b >= lo && b + 8 <= hi;
+    float sq[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        gv[e] = sq[e] = __fmul_rn(s[e], inv);
+    in = 0xffu;
+    if (b + 8 > psi || !full) {  // padding, or a group cut by the tile/window edge
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const uint64_t i = b + e;
+            if (i >= psi)
+                gv[e] = 0.0f;
+            if (!(i >= lo && i < hi))
+                in &= ~(1u << e);
+            sq[e] = (in >> e & 1u) ? gv[e] : 0.0f;
+        }
+    }
+    if (squares_in_range(sq)) {  // every counted element finite: no overflow
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            acc.add_fast(__fmul_rn(sq[e], kSqScale));
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            bad |= (in >> e & 1u) && not_finite(gv[e]);
+        acc.wide += sumsq_wide(gv[0], gv[1], gv[2], gv[3], gv[4], gv[5], gv[6], gv[7], in);
+    }
+}
+
+/* A tile's sum of squares from every thread's accumulator: a fixed-order pair-arithmetic
+ * shuffle tree in fp32, fp64 once per warp, then the warps in order.  One block barrier;
+ * the per-warp values alternate between two buffers (`parity`), so a following tile
+ * cannot overwrite them before thread 0 has read them.  The result is valid in thread 0
+ * only.  Every thread of the block calls it; warps beyond the first kThreads / 32 take
+ * part in the barrier only. */
+template <int kThreads>
+__device__ __forceinline__ double tile_fold(const SumSq& acc, double (*warp_part)[kThreads / 32],
+                                            uint32_t& parity)
+{
+    float ph = acc.hi, pl = acc.lo;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float h2 = __shfl_xor_sync(0xffffffffu, ph, o);
+        const float l2 = __shfl_xor_sync(0xffffffffu, pl, o);
+        pair_add(ph, pl, h2, l2);
+    }
+    double wide = acc.wide;
+    if (__any_sync(0xffffffffu, wide != 0.0)) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            wide += __shfl_xor_sync(0xffffffffu, wide, o);
+    }
+    double* wp = warp_part[parity];
+    if ((threadIdx.x & 31) == 0 && threadIdx.x < kThreads)  // extra warps of a block add nothing
+        wp[threadIdx.x >> 5] = ((double)ph + (double)pl) * kSqUnscale + wide;
+    __syncthreads();
+    double t = 0.0;
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w)
+            t += wp[w];
+    }
+    parity ^= 1u;
+    return t;
+}
+
+}  // namespace
+}  // namespace zero

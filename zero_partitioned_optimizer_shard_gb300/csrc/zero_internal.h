@@ -49,6 +49,27 @@ struct AdamwArgs {
     uint32_t grad_f16;                       // copies are fp16 (else bf16)
 };
 
+/* Kernel arguments of the single-launch step for small layouts (fused.cu). */
+struct FusedArgs {
+    const void* rep[ZERO_MAX_KERNEL_RANKS];  // replica k, pointing at flat 0
+    float* g;                                // flat fp32 gradient, or null: not written
+    double* partials;                        // the tile partials: zero on entry and on exit
+    float* master;
+    float* m;
+    float* v;
+    uint16_t* out;
+    zero_step_state_t* st;
+    uint64_t psi, psi_padded, shard, tiles_per_rank;
+    uint32_t n_ranks;
+    uint32_t out_f16;                        // gathered parameters as fp16 instead of bf16
+    zero_adamw_hparams_t hp;
+};
+
+/* The single-launch step takes layouts of at most this many tile slots per rank (the norm
+ * kernel then sums each rank's slots in one lane-strided pass) whose n_tiles blocks can
+ * all be resident at once. */
+constexpr uint64_t kFusedMaxTilesPerRank = 128;
+
 struct InitArgs {
     zero_step_state_t* st;
     double* partials;
@@ -65,6 +86,14 @@ struct InitArgs {
 __device__ __forceinline__ void grid_dependency_wait()
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+/* Lets the next kernel in the stream (launched with programmatic dependent launch) start
+ * now: its blocks become resident and wait in grid_dependency_wait() until this grid has
+ * completed, so no launch latency is left between the two. */
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 template <typename... Params, typename... Args>
@@ -91,6 +120,8 @@ cudaError_t launch_adamw(const AdamwArgs& a, cudaStream_t s);
 cudaError_t launch_adamw_host_state(const AdamwArgs& a, cudaStream_t s);
 cudaError_t launch_adamw_rereduce(const AdamwArgs& a, cudaStream_t s);  // g from rep0 + rep1  // master/m/v in pinned host memory
 cudaError_t launch_state_init(const InitArgs& a, cudaStream_t s);
+bool fused_fits(const zero_layout_t* L, zero_dtype_t dtype);  // single window, small enough
+cudaError_t launch_step_fused(const FusedArgs& a, zero_dtype_t dtype, uint64_t n_tiles, cudaStream_t s);
 
 /* Resident blocks per SM times SM count for a kernel, cached per device. */
 bool layout_ok(const zero_layout_t* L);  // the invariants zero_partition establishes
