@@ -302,8 +302,9 @@ int zero_adamw_cast_gather_host_state(const zero_layout_t* layout,
  * layout (one bucket, at most 128 tile slots per rank, and every one of its n_tiles tiles
  * able to hold a resident block at once: up to a few million parameters) runs instead
  * as ONE cooperative kernel with the same bits: each block reduces one tile and keeps
- * its g in shared memory, the block that finishes last forms the global norm and the
- * step's scalars, and every block then updates its tile.  g is still written when given
+ * its g in shared memory (with at most one tile per SM, also the tile's master, m and v,
+ * bulk-copied in as the block starts), the block that finishes last forms the global norm
+ * and the step's scalars, and every block then updates its tile.  g is still written when given
  * (never read back), so such a step moves 2N + 30 bytes per parameter, 2N + 26 with
  * g = NULL.  zero_step_launches tells which way a layout goes.
  * ------------------------------------------------------------------------------------- */

@@ -1,4 +1,6 @@
-"""The single-launch step that zero_step takes for small layouts (k_step_fused).
+"""The single-launch step that zero_step takes for small layouts (k_step_fused), in both
+of its shapes: staged (at most one tile per SM; the tile's optimizer state is copied into
+shared memory) and unstaged (more tiles than SMs).
 
 It must give the same bits as the three separate calls (reduce, norm, AdamW) in every
 output and in the whole 128-byte step state, over several steps, on ragged sizes, every
@@ -42,6 +44,9 @@ CASES = {
                        hp=replace(W.C2.hp, max_grad_norm=0.0)),
     "psi5": replace(W.scaled(W.C1, 5, steps=2), n_ranks=4),
     "psi1": replace(W.scaled(W.C1, 1, steps=2), n_ranks=4),
+    # more tiles than SMs: the unstaged shape (up to 3 blocks per SM, state read from L2)
+    "n8-many-tiles": W.scaled(W.C2, 8 * 8192 * 20 + 5, steps=2),
+    "n3-many-tiles": replace(W.scaled(W.C2, 3 * 8192 * 60 + 1, steps=2), n_ranks=3),
 }
 
 
@@ -82,6 +87,12 @@ def test_single_launch_matches_oracle(name):
         assert_state_close(gpu.arrays(), orc.arrays(), wl.psi,
                            exact_expected=bool(rep.skipped) or s.clip_coef == rep.clip_coef)
     gpu.check_guards()
+
+
+def test_both_shapes_are_exercised():
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles = [z.zero_partition(w.psi, w.n_ranks, w.stage).n_tiles for w in CASES.values()]
+    assert min(tiles) <= sms < max(tiles)
 
 
 def test_launch_counts():

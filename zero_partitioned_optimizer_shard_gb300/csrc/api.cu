@@ -228,6 +228,7 @@ extern "C" int zero_step_state_init(const zero_layout_t* layout, float loss_scal
                                     uint32_t growth_interval, zero_step_state_t* st,
                                     double* partials, zero_stream_t stream)
 {
+    const NvtxRange range("zero_step_state_init");
     if (!kernel_layout_ok(layout) || !st || !partials || !(loss_scale > 0.0f) || loss_scale > 3.0e38f)
         return ZERO_EINVAL;
     if (!aligned16(st) || !aligned16(partials))
@@ -272,6 +273,7 @@ extern "C" int zero_reduce_shard_unscale(const zero_layout_t* layout, zero_dtype
                                          float* g, double* partials, zero_step_state_t* st,
                                          zero_stream_t stream)
 {
+    const NvtxRange range("zero_reduce_shard_unscale");
     const int rc = check_reduce_args(layout, dtype, replicas, begin, count, g, partials, st);
     if (rc != ZERO_OK)
         return rc;
@@ -281,6 +283,7 @@ extern "C" int zero_reduce_shard_unscale(const zero_layout_t* layout, zero_dtype
 extern "C" int zero_grad_norm(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,
                               double* partials, zero_step_state_t* st, zero_stream_t stream)
 {
+    const NvtxRange range("zero_grad_norm");
     if (!kernel_layout_ok(layout) || !hparams_ok(hp) || !partials || !st)
         return ZERO_EINVAL;
     if (!aligned16(partials) || !aligned16(st))
@@ -293,6 +296,7 @@ extern "C" int zero_adamw_cast_gather(const zero_layout_t* layout, const zero_ad
                                       uint16_t* params, const zero_step_state_t* st,
                                       zero_stream_t stream)
 {
+    const NvtxRange range("zero_adamw_cast_gather");
     const int rc = check_adamw_args(layout, hp, g, master, m, v, params, st);
     if (rc != ZERO_OK)
         return rc;
@@ -305,6 +309,7 @@ extern "C" int zero_adamw_cast_gather_host_state(const zero_layout_t* layout,
                                                  uint16_t* params, const zero_step_state_t* st,
                                                  zero_stream_t stream)
 {
+    const NvtxRange range("zero_adamw_cast_gather_host_state");
     const int rc = check_adamw_args(layout, hp, g, master, m, v, params, st);
     if (rc != ZERO_OK)
         return rc;
@@ -323,6 +328,7 @@ extern "C" int zero_step(const zero_layout_t* layout, const zero_adamw_hparams_t
                          float* master, float* m, float* v, uint16_t* params, zero_step_state_t* st,
                          zero_stream_t stream)
 {
+    const NvtxRange range("zero_step");
     if (!kernel_layout_ok(layout) || !replicas)
         return ZERO_EINVAL;
     // g == NULL: the re-reading schedule (N = 2, one window over resident copies)
@@ -343,7 +349,8 @@ extern "C" int zero_step(const zero_layout_t* layout, const zero_adamw_hparams_t
     if (!aligned16(partials))
         return ZERO_EALIGN;
     const cudaStream_t s = (cudaStream_t)stream;
-    if (fused_fits(layout, dtype)) {
+    const int shape = fused_shape(layout, dtype);
+    if (shape > 0) {
         // small layout: the whole step in one launch, with the same bits (fused.cu)
         FusedArgs f;
         memset(&f, 0, sizeof f);
@@ -363,7 +370,7 @@ extern "C" int zero_step(const zero_layout_t* layout, const zero_adamw_hparams_t
         f.n_ranks = layout->n_ranks;
         f.out_f16 = hp->params_dtype == ZERO_F16 ? 1u : 0u;
         f.hp = *hp;
-        return cuda_status(launch_step_fused(f, dtype, layout->n_tiles, s));
+        return cuda_status(launch_step_fused(f, dtype, layout->n_tiles, shape, s));
     }
     for (uint64_t b = 0; b < layout->n_buckets; ++b) {
         const uint64_t begin = b * W, count = begin + W < P ? W : P - begin;
@@ -384,7 +391,7 @@ extern "C" int zero_step_launches(const zero_layout_t* layout, zero_dtype_t dtyp
 {
     if (!kernel_layout_ok(layout) || (dtype != ZERO_F16 && dtype != ZERO_BF16))
         return ZERO_EINVAL;
-    return fused_fits(layout, dtype) ? 1 : (int)(layout->n_buckets + 2);
+    return fused_shape(layout, dtype) > 0 ? 1 : (int)(layout->n_buckets + 2);
 }
 
 extern "C" int zero_step_host(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,
@@ -394,6 +401,7 @@ extern "C" int zero_step_host(const zero_layout_t* layout, const zero_adamw_hpar
                               zero_step_state_t* host_state_out, zero_stream_t stream,
                               zero_stream_t copy_stream)
 {
+    const NvtxRange range("zero_step_host");
     if (!kernel_layout_ok(layout) || (dtype != ZERO_F16 && dtype != ZERO_BF16) || !host_replicas ||
         !staging || stream == copy_stream)
         return ZERO_EINVAL;

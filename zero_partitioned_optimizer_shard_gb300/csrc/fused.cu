@@ -47,13 +47,26 @@ namespace {
 __device__ unsigned long long zero_test_absent_block = ~0ull;
 #endif
 
-constexpr int kFusedWarps = 8;                       // stream gradients and state
+constexpr int kFusedWarps = 8;                       // stream the gradients (phase 1)
 constexpr int kFusedThreads = kFusedWarps * 32;      // the reduce pass's block size
-constexpr int kFusedBlock = kFusedThreads + 32;      // + one warp for the scalar chains
 constexpr int kFusedLoads = 8;                       // replica loads in flight per thread
 constexpr uint64_t kT = ZERO_TILE_ELEMS;
+constexpr int kGcFloats = (int)kT + 8;               // the tile's g from its first whole group
 
 static_assert(kFusedThreads == 256, "the tile partial's bits depend on the reduce pass's block size");
+
+/* Two shapes of the same kernel.  Unstaged: 9 warps (8 streaming, 1 for the scalar chains),
+ * up to 3 blocks per SM, master/m/v prefetched into L2.  Staged, for layouts of at most one
+ * tile per SM: 17 warps (the 8 streaming ones, 8 more that join the AdamW phase, the scalar
+ * warp) and the tile's master, m and v bulk-copied into shared memory when the block starts,
+ * so the AdamW phase reads no global memory. */
+template <bool STAGED>
+struct Shape {
+    static constexpr int kScalarWarp = STAGED ? 16 : 8;
+    static constexpr int kThreads = (kScalarWarp + 1) * 32;
+    static constexpr int kMinBlocks = STAGED ? 1 : 3;
+    static constexpr size_t kSmem = (size_t)kGcFloats * 4 * (STAGED ? 4 : 1);  // g (+ master, m, v)
+};
 
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p)
 {
@@ -87,6 +100,14 @@ __device__ __forceinline__ void prefetch_l2(const float* p, uint64_t n)
                      ::"l"(a0), "r"((uint32_t)(a1 - a0)) : "memory");
 }
 
+/* Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) into shared
+ * memory, completing on the mbarrier `bar`. */
+__device__ __forceinline__ void bulk_to_smem(void* dst, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
 /* AdamW of one element i < psi, or the padding's gathered 0. */
 __device__ __forceinline__ void update_one(const FusedArgs& a, uint64_t i, float g, const Scalars& s)
 {
@@ -102,15 +123,19 @@ __device__ __forceinline__ void update_one(const FusedArgs& a, uint64_t i, float
     }
 }
 
-template <zero_dtype_t DT, int NR>
-__global__ void __launch_bounds__(kFusedBlock, 3) k_step_fused(const __grid_constant__ FusedArgs a)
+template <zero_dtype_t DT, int NR, bool STAGED>
+__global__ void __launch_bounds__(Shape<STAGED>::kThreads, Shape<STAGED>::kMinBlocks)
+k_step_fused(const __grid_constant__ FusedArgs a)
 {
-    __shared__ __align__(16) float gc[kT + 8];  // the tile's g, from its first whole group
+    using S = Shape<STAGED>;
+    extern __shared__ __align__(16) float dyn[];  // g of the tile; staged: then master, m, v
+    float* const gc = dyn;                        // gc[i - base] holds g[i]
     __shared__ double warp_part[2][kFusedWarps];
     __shared__ double rank_sum[ZERO_MAX_KERNEL_RANKS];
     __shared__ float s_step, s_rbc2;
     __shared__ Scalars s_sc;
     __shared__ __align__(16) zero_step_state_t s_st;  // the state as this step found it
+    __shared__ __align__(8) uint64_t s_bar;            // staged: the bulk copies
     __shared__ uint32_t s_flag;  // last block; then: go on to the update
     grid_launch_dependents();
     grid_dependency_wait();
@@ -126,9 +151,27 @@ __global__ void __launch_bounds__(kFusedBlock, 3) k_step_fused(const __grid_cons
     const uint64_t cell = (shard_lo / kT + j) * kT;
     const uint64_t lo = cell > shard_lo ? cell : shard_lo;
     const uint64_t hi = cell + kT < shard_hi ? cell + kT : shard_hi;
-    const uint64_t base = lo & ~7ull;  // first group of the tile; gc[i - base] holds g[i]
+    const uint64_t base = lo & ~7ull;                           // first group of the tile
+    const uint64_t v_lo = (lo + 3) & ~3ull, v_hi = hi & ~3ull;  // 16-byte-aligned body
+    const bool staged_copy = STAGED && lo < hi && v_lo < v_hi;
+    float* const sp = dyn + kGcFloats;  // staged master, m, v, indexed like gc
+    float* const sm = sp + kGcFloats;
+    float* const sv = sm + kGcFloats;
+    const uint32_t bar = smem_addr(&s_bar);
 
-    if (w == kFusedWarps) {
+    if (staged_copy && threadIdx.x == 0) {
+        // the tile's optimizer state into shared memory, in flight while the gradients are
+        // summed; only the 16-byte-aligned body, the few edge elements are read directly
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        const uint32_t bytes = (uint32_t)((v_hi - v_lo) * sizeof(float));
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                     ::"r"(bar), "r"(3 * bytes) : "memory");
+        bulk_to_smem(sp + (v_lo - base), a.master + v_lo, bytes, bar);
+        bulk_to_smem(sm + (v_lo - base), a.m + v_lo, bytes, bar);
+        bulk_to_smem(sv + (v_lo - base), a.v + v_lo, bytes, bar);
+    }
+    if (w == S::kScalarWarp) {
         // a copy of the state for the last block (no block writes it before the last one
         // arrives), and the bias corrections of step t+1: lanes 0 and 1 run the two fp64
         // power chains side by side
@@ -141,7 +184,7 @@ __global__ void __launch_bounds__(kFusedBlock, 3) k_step_fused(const __grid_cons
             else
                 s_rbc2 = bias_rbc2(a.hp, t_next);
         }
-        if (lane == 2 && lo < hi) {
+        if (!STAGED && lane == 2 && lo < hi) {
             prefetch_l2(a.master + lo, hi - lo);
             prefetch_l2(a.m + lo, hi - lo);
             prefetch_l2(a.v + lo, hi - lo);
@@ -242,15 +285,11 @@ __global__ void __launch_bounds__(kFusedBlock, 3) k_step_fused(const __grid_cons
         s_flag = arrive_acq_rel(&st->arrivals) == gridDim.x - 1;
     }
     __syncthreads();
-#ifdef ZERO_TEST_HOOKS
-    if (s_flag == 2)
-        return;
-#endif
 
-    if (s_flag) {
+    if (s_flag == 1) {
         // the last block: the norm in the norm kernel's order (at most 128 slots per
         // rank: lane l adds slots l, l+32, l+64, l+96 in that order), partials zeroed
-        for (uint32_t rr = w; rr < N; rr += kFusedWarps + 1) {
+        for (uint32_t rr = w; rr < N; rr += S::kScalarWarp + 1) {
             double* p = a.partials + (uint64_t)rr * tpr;
             double v[4];
 #pragma unroll
@@ -299,9 +338,8 @@ __global__ void __launch_bounds__(kFusedBlock, 3) k_step_fused(const __grid_cons
             for (int q = 0; q < (int)(sizeof(zero_step_state_t) / 16); ++q)
                 __stcg(reinterpret_cast<uint4*>(st) + q, reinterpret_cast<const uint4*>(&ls)[q]);
             st_release_u32(&st->arrivals, 0u);
-            s_flag = 1;
         }
-    } else if (threadIdx.x == 0) {
+    } else if (s_flag == 0 && threadIdx.x == 0) {
         // wait for the last block to reset the counter, at most ~2 s
         const long long t0 = clock64();
         uint32_t ok = 1;
@@ -316,12 +354,16 @@ __global__ void __launch_bounds__(kFusedBlock, 3) k_step_fused(const __grid_cons
         s_flag = ok;
     }
     __syncthreads();
-    if (!s_flag)
-        return;
 
-    // 3. AdamW over the tile from the g held in shared memory
+    // 3. AdamW over the tile from the g held in shared memory, unless the step is skipped
+    // or this block gave up waiting
     if (threadIdx.x == 0) {
-        s_flag = __ldcg(&st->skip) == 0;
+        uint32_t go = s_flag == 1 && __ldcg(&st->skip) == 0 && lo < hi;
+        if (go && staged_copy && !wait_parity_bounded(bar, 0)) {
+            atomicOr(&st->error, 1u);
+            go = 0;
+        }
+        s_flag = go;
         s_sc.c = __ldcg(&st->clip_coef);
         s_sc.step = __ldcg(&st->step_size);
         s_sc.rbc2 = __ldcg(&st->rbc2);
@@ -333,67 +375,79 @@ __global__ void __launch_bounds__(kFusedBlock, 3) k_step_fused(const __grid_cons
         s_sc.eps = a.hp.eps;
     }
     __syncthreads();
-    if (!s_flag || lo >= hi)
-        return;
-    const Scalars& sc = s_sc;
-    const uint64_t v_lo = (lo + 3) & ~3ull, v_hi = hi & ~3ull;  // 16-byte-aligned body
-    if (v_lo >= v_hi) {
-        for (uint64_t i = lo + threadIdx.x; i < hi; i += kFusedBlock)
-            update_one(a, i, gc[i - base], sc);
-        return;
-    }
-    if (lo + threadIdx.x < v_lo)
-        update_one(a, lo + threadIdx.x, gc[lo + threadIdx.x - base], sc);
-    if (v_hi + threadIdx.x < hi)
-        update_one(a, v_hi + threadIdx.x, gc[v_hi + threadIdx.x - base], sc);
-    // three 4-element groups per thread at a time: all their loads before any store (the
-    // arrays may alias as far as the compiler knows, so it would not hoist them itself)
-    constexpr int Q = 3;
-    const uint64_t v_end = v_hi < (a.psi & ~3ull) ? v_hi : (a.psi & ~3ull);  // groups all < psi
-    for (uint64_t i0 = v_lo + 4ull * threadIdx.x; i0 < v_hi; i0 += 4ull * kFusedBlock * Q) {
-        float4 p4[Q], m4[Q], v4[Q];
+    if (s_flag) {
+        const Scalars& sc = s_sc;
+        if (v_lo >= v_hi) {
+            for (uint64_t i = lo + threadIdx.x; i < hi; i += S::kThreads)
+                update_one(a, i, gc[i - base], sc);
+        } else {
+            if (lo + threadIdx.x < v_lo)
+                update_one(a, lo + threadIdx.x, gc[lo + threadIdx.x - base], sc);
+            if (v_hi + threadIdx.x < hi)
+                update_one(a, v_hi + threadIdx.x, gc[v_hi + threadIdx.x - base], sc);
+            // Q 4-element groups per thread at a time: all their loads before any store
+            // (the arrays may alias as far as the compiler knows, so it would not hoist
+            // them itself)
+            constexpr int Q = STAGED ? 1 : 3;
+            const uint64_t v_end = v_hi < (a.psi & ~3ull) ? v_hi : (a.psi & ~3ull);  // groups < psi
+            for (uint64_t i0 = v_lo + 4ull * threadIdx.x; i0 < v_hi; i0 += 4ull * S::kThreads * Q) {
+                float4 p4[Q], m4[Q], v4[Q];
 #pragma unroll
-        for (int q = 0; q < Q; ++q) {
-            const uint64_t i = i0 + 4ull * kFusedBlock * q;
-            if (i < v_end) {
-                p4[q] = __ldcs(reinterpret_cast<const float4*>(a.master + i));
-                m4[q] = __ldcs(reinterpret_cast<const float4*>(a.m + i));
-                v4[q] = __ldcs(reinterpret_cast<const float4*>(a.v + i));
-            }
-        }
-#pragma unroll
-        for (int q = 0; q < Q; ++q) {
-            const uint64_t i = i0 + 4ull * kFusedBlock * q;
-            if (i >= v_hi)
-                break;
-            if (i < v_end) {
-                const float4 g4 = *reinterpret_cast<const float4*>(gc + (i - base));
-                uint2 o;
-                if (a.out_f16) {
-                    o.x = pack2<true>(adamw_one(g4.x, p4[q].x, m4[q].x, v4[q].x, sc),
-                                      adamw_one(g4.y, p4[q].y, m4[q].y, v4[q].y, sc));
-                    o.y = pack2<true>(adamw_one(g4.z, p4[q].z, m4[q].z, v4[q].z, sc),
-                                      adamw_one(g4.w, p4[q].w, m4[q].w, v4[q].w, sc));
-                } else {
-                    o.x = pack2<false>(adamw_one(g4.x, p4[q].x, m4[q].x, v4[q].x, sc),
-                                       adamw_one(g4.y, p4[q].y, m4[q].y, v4[q].y, sc));
-                    o.y = pack2<false>(adamw_one(g4.z, p4[q].z, m4[q].z, v4[q].z, sc),
-                                       adamw_one(g4.w, p4[q].w, m4[q].w, v4[q].w, sc));
+                for (int q = 0; q < Q; ++q) {
+                    const uint64_t i = i0 + 4ull * S::kThreads * q;
+                    if (i < v_end) {
+                        if (STAGED) {
+                            p4[q] = *reinterpret_cast<const float4*>(sp + (i - base));
+                            m4[q] = *reinterpret_cast<const float4*>(sm + (i - base));
+                            v4[q] = *reinterpret_cast<const float4*>(sv + (i - base));
+                        } else {
+                            p4[q] = __ldcs(reinterpret_cast<const float4*>(a.master + i));
+                            m4[q] = __ldcs(reinterpret_cast<const float4*>(a.m + i));
+                            v4[q] = __ldcs(reinterpret_cast<const float4*>(a.v + i));
+                        }
+                    }
                 }
-                __stcs(reinterpret_cast<float4*>(a.master + i), p4[q]);
-                __stcs(reinterpret_cast<float4*>(a.m + i), m4[q]);
-                __stcs(reinterpret_cast<float4*>(a.v + i), v4[q]);
-                __stcs(reinterpret_cast<uint2*>(a.out + i), o);
-            } else {  // the group holding psi, or padding: element by element
-                for (int e = 0; e < 4; ++e)
-                    update_one(a, i + e, gc[i + e - base], sc);
+#pragma unroll
+                for (int q = 0; q < Q; ++q) {
+                    const uint64_t i = i0 + 4ull * S::kThreads * q;
+                    if (i >= v_hi)
+                        break;
+                    if (i < v_end) {
+                        const float4 g4 = *reinterpret_cast<const float4*>(gc + (i - base));
+                        uint2 o;
+                        if (a.out_f16) {
+                            o.x = pack2<true>(adamw_one(g4.x, p4[q].x, m4[q].x, v4[q].x, sc),
+                                              adamw_one(g4.y, p4[q].y, m4[q].y, v4[q].y, sc));
+                            o.y = pack2<true>(adamw_one(g4.z, p4[q].z, m4[q].z, v4[q].z, sc),
+                                              adamw_one(g4.w, p4[q].w, m4[q].w, v4[q].w, sc));
+                        } else {
+                            o.x = pack2<false>(adamw_one(g4.x, p4[q].x, m4[q].x, v4[q].x, sc),
+                                               adamw_one(g4.y, p4[q].y, m4[q].y, v4[q].y, sc));
+                            o.y = pack2<false>(adamw_one(g4.z, p4[q].z, m4[q].z, v4[q].z, sc),
+                                               adamw_one(g4.w, p4[q].w, m4[q].w, v4[q].w, sc));
+                        }
+                        __stcs(reinterpret_cast<float4*>(a.master + i), p4[q]);
+                        __stcs(reinterpret_cast<float4*>(a.m + i), m4[q]);
+                        __stcs(reinterpret_cast<float4*>(a.v + i), v4[q]);
+                        __stcs(reinterpret_cast<uint2*>(a.out + i), o);
+                    } else {  // the group holding psi, or padding: element by element
+                        for (int e = 0; e < 4; ++e)
+                            update_one(a, i + e, gc[i + e - base], sc);
+                    }
+                }
             }
         }
     }
+    // staged: the bulk copies land in this block's shared memory; never leave before they
+    // have (bounded), whatever the path taken above
+    if (staged_copy && threadIdx.x == 0 && !s_flag && !wait_parity_bounded(bar, 0))
+        atomicOr(&st->error, 1u);
 }
 
-template <zero_dtype_t DT, int NR>
+template <zero_dtype_t DT, int NR, bool STAGED>
 struct FusedKernel {
+    static constexpr auto kernel = k_step_fused<DT, NR, STAGED>;
+    using S = Shape<STAGED>;
     static int capacity()  // blocks that can be resident at once, cached per device
     {
         static int cap[64] = {0};
@@ -402,7 +456,10 @@ struct FusedKernel {
         int& c = cap[dev & 63];
         if (c == 0) {
             int o = 0;
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, k_step_fused<DT, NR>, kFusedBlock, 0);
+            if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)S::kSmem) == cudaSuccess)
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kernel, S::kThreads, S::kSmem);
+            cudaGetLastError();  // a refused attribute or query leaves no error behind
             c = o > 0 ? o * sm_count() : -1;
         }
         return c;
@@ -417,8 +474,8 @@ struct FusedKernel {
         int& md = mode[dev & 63];
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(grid);
-        cfg.blockDim = dim3(kFusedBlock);
-        cfg.dynamicSmemBytes = 0;
+        cfg.blockDim = dim3(S::kThreads);
+        cfg.dynamicSmemBytes = S::kSmem;
         cfg.stream = s;
         cudaLaunchAttribute at[2];
         at[0].id = cudaLaunchAttributeCooperative;
@@ -428,7 +485,7 @@ struct FusedKernel {
         cfg.attrs = at;
         if (md != 2) {
             cfg.numAttrs = 2;
-            cudaError_t e = cudaLaunchKernelEx(&cfg, k_step_fused<DT, NR>, a);
+            cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a);
             if (e == cudaSuccess) {
                 md = 1;
                 return e;
@@ -439,29 +496,29 @@ struct FusedKernel {
             md = 2;
         }
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, k_step_fused<DT, NR>, a);
+        return cudaLaunchKernelEx(&cfg, kernel, a);
     }
 };
 
-template <zero_dtype_t DT>
+template <zero_dtype_t DT, bool STAGED>
 int capacity_dt(uint32_t n)
 {
     switch (n) {
-    case 2: return FusedKernel<DT, 2>::capacity();
-    case 4: return FusedKernel<DT, 4>::capacity();
-    case 8: return FusedKernel<DT, 8>::capacity();
-    default: return FusedKernel<DT, 0>::capacity();
+    case 2: return FusedKernel<DT, 2, STAGED>::capacity();
+    case 4: return FusedKernel<DT, 4, STAGED>::capacity();
+    case 8: return FusedKernel<DT, 8, STAGED>::capacity();
+    default: return FusedKernel<DT, 0, STAGED>::capacity();
     }
 }
 
-template <zero_dtype_t DT>
+template <zero_dtype_t DT, bool STAGED>
 cudaError_t launch_dt(const FusedArgs& a, unsigned grid, cudaStream_t s)
 {
     switch (a.n_ranks) {
-    case 2: return FusedKernel<DT, 2>::launch(a, grid, s);
-    case 4: return FusedKernel<DT, 4>::launch(a, grid, s);
-    case 8: return FusedKernel<DT, 8>::launch(a, grid, s);
-    default: return FusedKernel<DT, 0>::launch(a, grid, s);
+    case 2: return FusedKernel<DT, 2, STAGED>::launch(a, grid, s);
+    case 4: return FusedKernel<DT, 4, STAGED>::launch(a, grid, s);
+    case 8: return FusedKernel<DT, 8, STAGED>::launch(a, grid, s);
+    default: return FusedKernel<DT, 0, STAGED>::launch(a, grid, s);
     }
 }
 
@@ -474,19 +531,25 @@ extern "C" int zero_test_absent_fused_block(unsigned long long block)
 }
 #endif
 
-bool fused_fits(const zero_layout_t* L, zero_dtype_t dtype)
+int fused_shape(const zero_layout_t* L, zero_dtype_t dtype)
 {
     if (L->n_buckets != 1 || L->tiles_per_rank > kFusedMaxTilesPerRank)
-        return false;
-    const int cap = dtype == ZERO_F16 ? capacity_dt<ZERO_F16>(L->n_ranks)
-                                      : capacity_dt<ZERO_BF16>(L->n_ranks);
-    return cap > 0 && L->n_tiles <= (uint64_t)cap;
+        return 0;
+    const bool f16 = dtype == ZERO_F16;
+    const int staged = f16 ? capacity_dt<ZERO_F16, true>(L->n_ranks) : capacity_dt<ZERO_BF16, true>(L->n_ranks);
+    if (staged > 0 && L->n_tiles <= (uint64_t)staged)
+        return 2;
+    const int plain = f16 ? capacity_dt<ZERO_F16, false>(L->n_ranks) : capacity_dt<ZERO_BF16, false>(L->n_ranks);
+    return plain > 0 && L->n_tiles <= (uint64_t)plain ? 1 : 0;
 }
 
-cudaError_t launch_step_fused(const FusedArgs& a, zero_dtype_t dtype, uint64_t n_tiles, cudaStream_t s)
+cudaError_t launch_step_fused(const FusedArgs& a, zero_dtype_t dtype, uint64_t n_tiles, int shape,
+                              cudaStream_t s)
 {
-    return dtype == ZERO_F16 ? launch_dt<ZERO_F16>(a, (unsigned)n_tiles, s)
-                             : launch_dt<ZERO_BF16>(a, (unsigned)n_tiles, s);
+    const unsigned grid = (unsigned)n_tiles;
+    if (dtype == ZERO_F16)
+        return shape == 2 ? launch_dt<ZERO_F16, true>(a, grid, s) : launch_dt<ZERO_F16, false>(a, grid, s);
+    return shape == 2 ? launch_dt<ZERO_BF16, true>(a, grid, s) : launch_dt<ZERO_BF16, false>(a, grid, s);
 }
 
 }  // namespace zero

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "../../include/zero.h"
@@ -113,6 +114,17 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
+/* An NVTX range named after an entry point, over its host-side work (checks and launches),
+ * so profilers can attribute and filter its kernels (e.g. ncu --nvtx --nvtx-include
+ * "zero_step/").  NVTX v3 is header-only: with no tool attached a range costs a few
+ * nanoseconds and loads nothing. */
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 /* Launchers (enqueue only; return the launch's cudaError_t). */
 cudaError_t launch_reduce(const ReduceArgs& a, zero_dtype_t dtype, cudaStream_t s);
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s);
@@ -120,8 +132,12 @@ cudaError_t launch_adamw(const AdamwArgs& a, cudaStream_t s);
 cudaError_t launch_adamw_host_state(const AdamwArgs& a, cudaStream_t s);
 cudaError_t launch_adamw_rereduce(const AdamwArgs& a, cudaStream_t s);  // g from rep0 + rep1  // master/m/v in pinned host memory
 cudaError_t launch_state_init(const InitArgs& a, cudaStream_t s);
-bool fused_fits(const zero_layout_t* L, zero_dtype_t dtype);  // single window, small enough
-cudaError_t launch_step_fused(const FusedArgs& a, zero_dtype_t dtype, uint64_t n_tiles, cudaStream_t s);
+/* Which single-launch shape a layout takes: 0 none (the three-launch step), 1 unstaged
+ * (up to 3 blocks per SM), 2 staged (one block per SM, the tile's optimizer state in
+ * shared memory). */
+int fused_shape(const zero_layout_t* L, zero_dtype_t dtype);
+cudaError_t launch_step_fused(const FusedArgs& a, zero_dtype_t dtype, uint64_t n_tiles, int shape,
+                              cudaStream_t s);
 
 /* Resident blocks per SM times SM count for a kernel, cached per device. */
 bool layout_ok(const zero_layout_t* L);  // the invariants zero_partition establishes
