@@ -133,6 +133,7 @@ k_step_fused(const __grid_constant__ FusedArgs a)
     __shared__ double warp_part[2][kFusedWarps];
     __shared__ double rank_sum[ZERO_MAX_KERNEL_RANKS];
     __shared__ float s_step, s_rbc2;
+    __shared__ ScalerCand s_cand;  // staged: the scaler's outcomes, formed ahead of time
     __shared__ Scalars s_sc;
     __shared__ __align__(16) zero_step_state_t s_st;  // the state as this step found it
     __shared__ __align__(8) uint64_t s_bar;            // staged: the bulk copies
@@ -189,6 +190,13 @@ k_step_fused(const __grid_constant__ FusedArgs a)
             prefetch_l2(a.m + lo, hi - lo);
             prefetch_l2(a.v + lo, hi - lo);
         }
+    }
+    if (STAGED && w == kFusedWarps && lane == 0) {
+        // a warp that is idle until the AdamW phase forms the scaler's two outcomes (two
+        // fp64 divisions) for the last block; only the last block's own copy is used, and
+        // no block writes the state before every block has arrived
+        const zero_step_state_t s0 = *st;
+        s_cand = scaler_candidates(s0, a.hp, N);
     }
 
     // 1. g over the tile: the reduce pass's groups and order; several groups' loads in
@@ -268,14 +276,18 @@ k_step_fused(const __grid_constant__ FusedArgs a)
         }
     }
 
-    // 2. the tile's partial (the reduce pass's fold), the overflow flag, and arrival
-    uint32_t parity = 0;
-    const double part = tile_fold<kFusedThreads>(acc, warp_part, parity);
-    if (threadIdx.x == 0 && lo < hi)
-        __stcg(a.partials + u, part);
-    if (__any_sync(0xffffffffu, bad) && lane == 0)
-        atomicOr(&st->overflow, 1u);
-    __syncthreads();
+    // 2. the tile's partial (the reduce pass's fold), the overflow flag, and arrival: only
+    // the streaming warps meet here (named barriers), so the other warps' fp64 chains do
+    // not hold the arrival back
+    if (w < kFusedWarps) {
+        uint32_t parity = 0;
+        const double part = tile_fold<kFusedThreads>(acc, warp_part, parity);
+        if (threadIdx.x == 0 && lo < hi)
+            __stcg(a.partials + u, part);
+        if (__any_sync(0xffffffffu, bad) && lane == 0)
+            atomicOr(&st->overflow, 1u);
+        asm volatile("bar.sync 2, %0;" ::"n"(kFusedThreads) : "memory");
+    }
     if (threadIdx.x == 0) {
 #ifdef ZERO_TEST_HOOKS
         if (blockIdx.x == zero_test_absent_block)
@@ -326,7 +338,10 @@ k_step_fused(const __grid_constant__ FusedArgs a)
                 ls.step_size = s_step;
                 ls.rbc2 = s_rbc2;
             }
-            scaler_update(&ls, a.hp, N, overflow, t_next);
+            if (STAGED)
+                scaler_apply(&ls, s_cand, overflow, t_next);
+            else
+                scaler_update(&ls, a.hp, N, overflow, t_next);
             const double norm = sqrt(total);
             ls.sumsq = total;
             ls.norm = norm;

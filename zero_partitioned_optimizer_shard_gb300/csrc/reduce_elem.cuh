@@ -177,15 +177,18 @@ __device__ __forceinline__ void group_values(uint64_t psi, float inv, const floa
 }
 
 /* A tile's sum of squares from every thread's accumulator: a fixed-order pair-arithmetic
- * shuffle tree in fp32, fp64 once per warp, then the warps in order.  One block barrier;
- * the per-warp values alternate between two buffers (`parity`), so a following tile
- * cannot overwrite them before thread 0 has read them.  The result is valid in thread 0
- * only.  Every thread of the block calls it; warps beyond the first kThreads / 32 take
- * part in the barrier only. */
+ * shuffle tree in fp32, fp64 once per warp, then the kThreads / 32 warp values pairwise,
+ * ((w0 + w4) + (w2 + w6)) + ((w1 + w5) + (w3 + w7)) for 8 warps: three dependent fp64
+ * additions instead of eight, which matters on GB300's slow fp64 pipe.  The per-warp
+ * values alternate between two buffers (`parity`), so a following tile cannot overwrite
+ * them before thread 0 has read them.  Called by the block's
+ * first kThreads threads only, which meet at named barrier 1 (other warps of a larger block
+ * go on unhindered).  The result is valid in thread 0 only. */
 template <int kThreads>
 __device__ __forceinline__ double tile_fold(const SumSq& acc, double (*warp_part)[kThreads / 32],
                                             uint32_t& parity)
 {
+    static_assert(kThreads / 32 <= 32 && (kThreads / 32 & (kThreads / 32 - 1)) == 0, "warp tree");
     float ph = acc.hi, pl = acc.lo;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -200,14 +203,23 @@ __device__ __forceinline__ double tile_fold(const SumSq& acc, double (*warp_part
             wide += __shfl_xor_sync(0xffffffffu, wide, o);
     }
     double* wp = warp_part[parity];
-    if ((threadIdx.x & 31) == 0 && threadIdx.x < kThreads)  // extra warps of a block add nothing
+    const int lane = threadIdx.x & 31;
+    if (lane == 0)
         wp[threadIdx.x >> 5] = ((double)ph + (double)pl) * kSqUnscale + wide;
-    __syncthreads();
+    asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
     double t = 0.0;
     if (threadIdx.x == 0) {
+        // pairwise: independent additions, three levels deep for 8 warps
+        double x[kThreads / 32];
 #pragma unroll
         for (int w = 0; w < kThreads / 32; ++w)
-            t += wp[w];
+            x[w] = wp[w];
+#pragma unroll
+        for (int h = kThreads / 64; h > 0; h >>= 1)
+#pragma unroll
+            for (int w = 0; w < h; ++w)
+                x[w] = x[w] + x[w + h];
+        t = x[0];
     }
     parity ^= 1u;
     return t;

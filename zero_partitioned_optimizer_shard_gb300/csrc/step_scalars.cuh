@@ -47,37 +47,76 @@ __device__ __forceinline__ float bias_rbc2(const zero_adamw_hparams_t& hp, uint3
     return (float)sqrt(1.0 - pow_uint((double)hp.beta2, t));
 }
 
-/* Skip decision, t, decay and the loss scaler of the step being finalised (everything
- * that does not need the norm).  `overflow`: the step's reduced gradient held inf/NaN;
- * `t_next` = st->t + 1, the step count if the step is applied. */
-__device__ __forceinline__ void scaler_update(zero_step_state_t* st, const zero_adamw_hparams_t& hp,
-                                              uint32_t n_ranks, uint32_t overflow, uint32_t t_next)
+/* The scaler's outcome for either value of the step's overflow flag, computed from the
+ * state before the step (it needs no norm, so it can be formed ahead of time):
+ *   overflow:  the dynamic scale halves (floor 1), the good-step count restarts;
+ *   no overflow: the good-step count grows and every growth_interval good steps the
+ *   dynamic scale doubles (cap 2^24); the decoupled decay 1 - lr*wd;
+ * and the unscale factor f32(1 / (N*L)) of the next step's reduce in each case. */
+struct ScalerCand {
+    float L_skip, inv_skip;
+    float L_ok, inv_ok;
+    uint32_t good_ok;
+    float decay;
+};
+
+__device__ __forceinline__ ScalerCand scaler_candidates(const zero_step_state_t& s,
+                                                        const zero_adamw_hparams_t& hp,
+                                                        uint32_t n_ranks)
+{
+    ScalerCand c;
+    const float L = s.loss_scale;
+    c.L_skip = L;
+    if (s.dynamic) {
+        const float half = L * 0.5f;
+        c.L_skip = half < 1.0f ? 1.0f : half;
+    }
+    c.L_ok = L;
+    c.good_ok = s.good_steps;
+    if (s.dynamic && s.growth_interval > 0) {
+        c.good_ok = s.good_steps + 1;
+        if (c.good_ok == s.growth_interval) {
+            const float twice = L * 2.0f;
+            c.L_ok = twice > 16777216.0f ? 16777216.0f : twice;
+            c.good_ok = 0;
+        }
+    }
+    c.inv_skip = (float)(1.0 / ((double)n_ranks * (double)c.L_skip));
+    c.inv_ok = (float)(1.0 / ((double)n_ranks * (double)c.L_ok));
+    c.decay = (float)(1.0 - (double)hp.lr * (double)hp.weight_decay);
+    return c;
+}
+
+/* Skip decision, t, decay and the loss scaler of the step being finalised, from its
+ * candidates.  `overflow`: the step's reduced gradient held inf/NaN; `t_next` = st->t + 1,
+ * the step count if the step is applied. */
+__device__ __forceinline__ void scaler_apply(zero_step_state_t* st, const ScalerCand& c,
+                                             uint32_t overflow, uint32_t t_next)
 {
     st->inv_scale_used = st->inv_scale;  // this step's unscale, for a re-reading AdamW
-    float L = st->loss_scale;
     if (overflow) {
         st->skip = 1;
         st->n_skipped += 1;
-        if (st->dynamic) {
-            const float half = L * 0.5f;
-            L = half < 1.0f ? 1.0f : half;
+        if (st->dynamic)
             st->good_steps = 0;
-        }
+        st->loss_scale = c.L_skip;
+        st->inv_scale = c.inv_skip;
     } else {
         st->t = t_next;
         st->skip = 0;
-        st->decay = (float)(1.0 - (double)hp.lr * (double)hp.weight_decay);
-        if (st->dynamic && st->growth_interval > 0) {
-            st->good_steps += 1;
-            if (st->good_steps == st->growth_interval) {
-                const float twice = L * 2.0f;
-                L = twice > 16777216.0f ? 16777216.0f : twice;
-                st->good_steps = 0;
-            }
-        }
+        st->decay = c.decay;
+        st->good_steps = c.good_ok;
+        st->loss_scale = c.L_ok;
+        st->inv_scale = c.inv_ok;
     }
-    st->loss_scale = L;
-    st->inv_scale = (float)(1.0 / ((double)n_ranks * (double)L));
+}
+
+/* Both together: everything that does not need the norm. */
+__device__ __forceinline__ void scaler_update(zero_step_state_t* st, const zero_adamw_hparams_t& hp,
+                                              uint32_t n_ranks, uint32_t overflow, uint32_t t_next)
+{
+    const ScalerCand c = scaler_candidates(*st, hp, n_ranks);
+    scaler_apply(st, c, overflow, t_next);
 }
 
 /* c = min(1, max_norm / (norm + 1e-6)) in fp64, rounded to fp32 once; 1 when the step is
