@@ -47,3 +47,16 @@ def test_reference_arm_under_torchrun_two_ranks():
     lines = _lines(r.stdout)
     assert len(lines) == 1  # rank 0 only
     _check(lines[0], 2)
+
+
+def test_reference_arm_names_each_workload():
+    for wl, psi, n in (("c1", 1_000_003, 4), ("llama-7b", 6_738_415_616, 8)):
+        r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
+                            "--warmup", "3", "--workload", wl], cwd=ROOT, capture_output=True,
+                           text=True, timeout=600)
+        assert r.returncode == 0, r.stderr[-2000:]
+        lines = _lines(r.stdout)
+        assert len(lines) == 1
+        _check(lines[0], 1)
+        c = lines[0]["config"]
+        assert c["psi"] == psi and c["n_ranks"] == n
