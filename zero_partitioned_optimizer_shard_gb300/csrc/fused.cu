@@ -19,9 +19,10 @@
  *      layouts of at most 128 tiles per rank), applies the clip coefficient, skip
  *      decision and loss scaler (step_scalars.cuh), zeroes the partials and releases the
  *      other blocks by resetting the counter;
- *   3. every block applies AdamW to its tile from the g it holds (adamw_elem.cuh), reading
- *      master, m and v that were prefetched into L2 while step 1 ran, and writes the
- *      gathered parameters.
+ *   3. every block applies AdamW to its tile from the g it holds (adamw_elem.cuh) and
+ *      writes the gathered parameters.  Master, m and v were fetched while step 1 ran:
+ *      into shared memory by bulk copies when the layout has at most one tile per SM
+ *      (the staged shape, 17 warps), else into L2 by prefetches (9 warps, 3 blocks/SM).
  *
  * So the results are bit-identical to the three-launch step, and the traffic is
  * 2N + 26 bytes per parameter (+4 when g is written), not 2N + 34.  "【论文解读】ZeRO"
@@ -30,8 +31,11 @@
  *
  * Waiting: the launch is cooperative (every block resident at once), and a block that
  * waits for the last one gives up after ~2 s, records 1 in the step state's error word and
- * writes nothing more.  A ninth warp computes the bias corrections of step t+1 while the
- * eight others stream the gradients, so the fp64 powers never sit on the critical path.
+ * writes nothing more.  GB300's fp64 arithmetic is slow (64 cycles per dependent add,
+ * about 650 per division or square root), so the fp64 chains that need no norm run in
+ * warps of their own beside the streaming ones: the bias corrections of step t+1 and, in
+ * the staged shape, the loss scaler's two possible outcomes; only the streaming warps
+ * meet before the arrival (named barriers).
  */
 #include "adamw_elem.cuh"
 #include "reduce_elem.cuh"
