@@ -306,7 +306,9 @@ int zero_adamw_cast_gather_host_state(const zero_layout_t* layout,
  * bulk-copied in as the block starts), the block that finishes last forms the global norm
  * and the step's scalars, and every block then updates its tile.  g is still written when given
  * (never read back), so such a step moves 2N + 30 bytes per parameter, 2N + 26 with
- * g = NULL.  zero_step_launches tells which way a layout goes.
+ * g = NULL.  zero_step_launches tells which way a layout goes.  If the cooperative launch
+ * is refused because fewer blocks fit on the GPU than its occupancy promised (another
+ * context holds part of it), the same call makes the three launches instead.
  * ------------------------------------------------------------------------------------- */
 int zero_step(const zero_layout_t* layout, const zero_adamw_hparams_t* hp, zero_dtype_t dtype,
               const void* const* replicas, float* g, double* partials, float* master, float* m,

@@ -370,7 +370,12 @@ extern "C" int zero_step(const zero_layout_t* layout, const zero_adamw_hparams_t
         f.n_ranks = layout->n_ranks;
         f.out_f16 = hp->params_dtype == ZERO_F16 ? 1u : 0u;
         f.hp = *hp;
-        return cuda_status(launch_step_fused(f, dtype, layout->n_tiles, shape, s));
+        const cudaError_t e = launch_step_fused(f, dtype, layout->n_tiles, shape, s);
+        if (e != cudaErrorCooperativeLaunchTooLarge)
+            return cuda_status(e);
+        // fewer blocks can be resident than the occupancy query promised (another context
+        // holds part of the GPU): nothing was enqueued, so take the three launches instead
+        cudaGetLastError();
     }
     for (uint64_t b = 0; b < layout->n_buckets; ++b) {
         const uint64_t begin = b * W, count = begin + W < P ? W : P - begin;
