@@ -509,8 +509,8 @@ struct FusedKernel {
                 md = 1;
                 return e;
             }
-            if (md == 1)
-                return e;
+            if (md == 1 || e == cudaErrorCooperativeLaunchTooLarge)
+                return e;  // not about the pair of attributes
             cudaGetLastError();  // the pair was refused: clear it, use cooperative alone
             md = 2;
         }
