@@ -14,6 +14,9 @@
  *                     gathered buffer (the layout the parameter all-gather produces);
  *                     the state may also live in host memory
  * plus the per-tensor segment map (which rank owns which piece of each model tensor).
+ * zero_step runs steps 2-4 as one kernel per part (a reduce per gradient bucket, the
+ * norm, AdamW) on large layouts and as ONE cooperative kernel, with the same bits, on
+ * small ones (zero_step_launches).
  *
  * Sources (web pages on ZeRO):
  *   [ZW] "【论文解读】ZeRO", wkq9411.github.io: sec. 4(1)-(3) the three partitioning stages,
@@ -40,6 +43,7 @@
  *     is reported in the step state and the step is skipped.
  *   - Thread safety: calls on different streams may run concurrently if they share no
  *     buffers.
+ *   - Profiling: every device entry point opens an NVTX range named after itself.
  */
 #ifndef ZERO_H
 #define ZERO_H
