@@ -42,6 +42,10 @@ CASES = {
                            hp=replace(W.C2.hp, params_dtype=z.ZERO_F16)),
     "no-clip": replace(W.scaled(W.C2, 8 * 5000 + 1, steps=2),
                        hp=replace(W.C2.hp, max_grad_norm=0.0)),
+    # clipping active in every step (c < 1): the staged shape's speculative update with
+    # c = 1 is dropped and the tile is updated again from global memory
+    "clip-active": replace(W.scaled(W.C2, 8 * 8192 * 4 + 3, steps=3),
+                           hp=replace(W.C2.hp, max_grad_norm=1e-4)),
     "psi5": replace(W.scaled(W.C1, 5, steps=2), n_ranks=4),
     "psi1": replace(W.scaled(W.C1, 1, steps=2), n_ranks=4),
     # more tiles than SMs: the unstaged shape (up to 3 blocks per SM, state read from L2)
@@ -66,6 +70,8 @@ def test_single_launch_equals_split_calls_bit_for_bit(name):
         sf, ss = fused.step(step), split.step(step)
         assert bytes(sf) == bytes(ss), (step, sf.norm, ss.norm, sf.clip_coef, ss.clip_coef)
         assert sf.error == 0 and sf.arrivals == 0
+        if name == "clip-active":
+            assert sf.clip_coef < 1.0
         skipped += sf.skip
         _arrays_equal(fused.arrays(), split.arrays())
     if wl.inject_every:
@@ -74,7 +80,7 @@ def test_single_launch_equals_split_calls_bit_for_bit(name):
     split.check_guards()
 
 
-@pytest.mark.parametrize("name", ["c1", "n16-overflow", "n3-ragged"])
+@pytest.mark.parametrize("name", ["c1", "n16-overflow", "n3-ragged", "clip-active"])
 def test_single_launch_matches_oracle(name):
     wl = CASES[name]
     gpu = GpuRun(wl)

@@ -61,15 +61,20 @@ static_assert(kFusedThreads == 256, "the tile partial's bits depend on the reduc
 
 /* Two shapes of the same kernel.  Unstaged: 9 warps (8 streaming, 1 for the scalar chains),
  * up to 3 blocks per SM, master/m/v prefetched into L2.  Staged, for layouts of at most one
- * tile per SM: 17 warps (the 8 streaming ones, 8 more that join the AdamW phase, the scalar
- * warp) and the tile's master, m and v bulk-copied into shared memory when the block starts,
- * so the AdamW phase reads no global memory. */
+ * tile per SM: 17 warps (the 8 streaming ones, 8 more, the scalar warp); the tile's master,
+ * m and v are bulk-copied into shared memory when the block starts, and the 9 other warps
+ * update the tile speculatively with c = 1 there while the streaming warps fold, arrive
+ * and wait for the norm. */
 template <bool STAGED>
 struct Shape {
     static constexpr int kScalarWarp = STAGED ? 16 : 8;
     static constexpr int kThreads = (kScalarWarp + 1) * 32;
     static constexpr int kMinBlocks = STAGED ? 1 : 3;
-    static constexpr size_t kSmem = (size_t)kGcFloats * 4 * (STAGED ? 4 : 1);  // g (+ master, m, v)
+    // named barrier 5: the streaming warps wait there for the warps that read the state
+    // and form the step's scalars (the scalar warp; staged also warp 8)
+    static constexpr int kScalarsReady = kFusedThreads + 32 * (STAGED ? 2 : 1);
+    // g (+ master, m, v and the speculative gathered parameters)
+    static constexpr size_t kSmem = (size_t)kGcFloats * 4 * (STAGED ? 4 : 1) + (STAGED ? (size_t)kGcFloats * 2 : 0);
 };
 
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p)
@@ -142,6 +147,7 @@ k_step_fused(const __grid_constant__ FusedArgs a)
     __shared__ __align__(16) zero_step_state_t s_st;  // the state as this step found it
     __shared__ __align__(8) uint64_t s_bar;            // staged: the bulk copies
     __shared__ uint32_t s_flag;  // last block; then: go on to the update
+    __shared__ uint32_t s_spec;  // staged: the bulk copies landed and the speculation ran
     grid_launch_dependents();
     grid_dependency_wait();
     zero_step_state_t* st = a.st;
@@ -164,6 +170,8 @@ k_step_fused(const __grid_constant__ FusedArgs a)
     float* const sv = sm + kGcFloats;
     const uint32_t bar = smem_addr(&s_bar);
 
+    if (threadIdx.x == 0)
+        s_spec = 0;
     if (staged_copy && threadIdx.x == 0) {
         // the tile's optimizer state into shared memory, in flight while the gradients are
         // summed; only the 16-byte-aligned body, the few edge elements are read directly
@@ -194,13 +202,18 @@ k_step_fused(const __grid_constant__ FusedArgs a)
             prefetch_l2(a.m + lo, hi - lo);
             prefetch_l2(a.v + lo, hi - lo);
         }
+        __syncwarp();
+        asm volatile("bar.arrive 5, %0;" ::"n"(S::kScalarsReady) : "memory");
     }
-    if (STAGED && w == kFusedWarps && lane == 0) {
+    if (STAGED && w == kFusedWarps) {
         // a warp that is idle until the AdamW phase forms the scaler's two outcomes (two
-        // fp64 divisions) for the last block; only the last block's own copy is used, and
-        // no block writes the state before every block has arrived
-        const zero_step_state_t s0 = *st;
-        s_cand = scaler_candidates(s0, a.hp, N);
+        // fp64 divisions) for the last block
+        if (lane == 0) {
+            const zero_step_state_t s0 = *st;
+            s_cand = scaler_candidates(s0, a.hp, N);
+        }
+        __syncwarp();
+        asm volatile("bar.arrive 5, %0;" ::"n"(S::kScalarsReady) : "memory");
     }
 
     // 1. g over the tile: the reduce pass's groups and order; several groups' loads in
@@ -280,9 +293,14 @@ k_step_fused(const __grid_constant__ FusedArgs a)
         }
     }
 
+    // staged: g of the tile is ready for the warps that only update (named barrier 3:
+    // the streaming warps arrive, the others wait)
+    if (STAGED && w < kFusedWarps)
+        asm volatile("bar.arrive 3, %0;" ::"n"(S::kThreads) : "memory");
+
     // 2. the tile's partial (the reduce pass's fold), the overflow flag, and arrival: only
-    // the streaming warps meet here (named barriers), so the other warps' fp64 chains do
-    // not hold the arrival back
+    // the streaming warps meet here (named barriers), so the other warps' fp64 chains and
+    // the staged speculation below do not hold the arrival or the norm back
     if (w < kFusedWarps) {
         uint32_t parity = 0;
         const double part = tile_fold<kFusedThreads>(acc, warp_part, parity);
@@ -290,99 +308,147 @@ k_step_fused(const __grid_constant__ FusedArgs a)
             __stcg(a.partials + u, part);
         if (__any_sync(0xffffffffu, bad) && lane == 0)
             atomicOr(&st->overflow, 1u);
-        asm volatile("bar.sync 2, %0;" ::"n"(kFusedThreads) : "memory");
-    }
-    if (threadIdx.x == 0) {
-#ifdef ZERO_TEST_HOOKS
-        if (blockIdx.x == zero_test_absent_block)
-            s_flag = 2;  // test builds only: this block never arrives
-        else
-#endif
-        s_flag = arrive_acq_rel(&st->arrivals) == gridDim.x - 1;
-    }
-    __syncthreads();
-
-    if (s_flag == 1) {
-        // the last block: the norm in the norm kernel's order (at most 128 slots per
-        // rank: lane l adds slots l, l+32, l+64, l+96 in that order), partials zeroed
-        for (uint32_t rr = w; rr < N; rr += S::kScalarWarp + 1) {
-            double* p = a.partials + (uint64_t)rr * tpr;
-            double v[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint64_t c = lane + 32u * q;
-                v[q] = c < tpr ? __ldcg(p + c) : 0.0;
-            }
-            double s = 0.0;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint64_t c = lane + 32u * q;
-                if (c < tpr) {
-                    s += v[q];
-                    p[c] = 0.0;
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-                s += __shfl_xor_sync(0xffffffffu, s, o);
-            if (lane == 0)
-                rank_sum[rr] = s;
-        }
-        __syncthreads();
+        // before this block arrives, its scalar warps have read the state (which the last
+        // block rewrites once every block has arrived) and formed the scalars the last
+        // block uses
+        asm volatile("bar.sync 5, %0;" ::"n"(S::kScalarsReady) : "memory");
         if (threadIdx.x == 0) {
-            // the step's scalars on the shared-memory copy, then written back whole; the
-            // counter is reset last, by a release store, which lets the others go on
-            double total = 0.0;
-            for (uint32_t rr = 0; rr < N; ++rr)
-                total += rank_sum[rr];
-            zero_step_state_t& ls = s_st;
-            const uint32_t overflow = __ldcg(&st->overflow) != 0;
-            const uint32_t t_next = ls.t + 1;
-            if (!overflow) {
-                ls.step_size = s_step;
-                ls.rbc2 = s_rbc2;
-            }
-            if (STAGED)
-                scaler_apply(&ls, s_cand, overflow, t_next);
+#ifdef ZERO_TEST_HOOKS
+            if (blockIdx.x == zero_test_absent_block)
+                s_flag = 2;  // test builds only: this block never arrives
             else
-                scaler_update(&ls, a.hp, N, overflow, t_next);
-            const double norm = sqrt(total);
-            ls.sumsq = total;
-            ls.norm = norm;
-            ls.clip_coef = clip_coefficient(norm, overflow, a.hp.max_grad_norm);
-            ls.overflow = 0;
-            ls.n_steps += 1;
-            ls.arrivals = gridDim.x;  // still "not released" until the store below
-            ls.error |= __ldcg(&st->error);
-            for (int q = 0; q < (int)(sizeof(zero_step_state_t) / 16); ++q)
-                __stcg(reinterpret_cast<uint4*>(st) + q, reinterpret_cast<const uint4*>(&ls)[q]);
-            st_release_u32(&st->arrivals, 0u);
+#endif
+            s_flag = arrive_acq_rel(&st->arrivals) == gridDim.x - 1;
         }
-    } else if (s_flag == 0 && threadIdx.x == 0) {
-        // wait for the last block to reset the counter, at most ~2 s
-        const long long t0 = clock64();
-        uint32_t ok = 1;
-        while (ld_acquire_u32(&st->arrivals) != 0) {
-            if (clock64() - t0 > 4000000000LL) {
-                ok = 0;
-                atomicOr(&st->error, 1u);
-                break;
+        asm volatile("bar.sync 2, %0;" ::"n"(kFusedThreads) : "memory");
+
+        if (s_flag == 1) {
+            // the last block: the norm in the norm kernel's order (at most 128 slots per
+            // rank: lane l adds slots l, l+32, l+64, l+96 in that order), partials zeroed
+            for (uint32_t rr = w; rr < N; rr += kFusedWarps) {
+                double* p = a.partials + (uint64_t)rr * tpr;
+                double v[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint64_t c = lane + 32u * q;
+                    v[q] = c < tpr ? __ldcg(p + c) : 0.0;
+                }
+                double s = 0.0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint64_t c = lane + 32u * q;
+                    if (c < tpr) {
+                        s += v[q];
+                        p[c] = 0.0;
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    s += __shfl_xor_sync(0xffffffffu, s, o);
+                if (lane == 0)
+                    rank_sum[rr] = s;
             }
-            __nanosleep(64);
+            asm volatile("bar.sync 2, %0;" ::"n"(kFusedThreads) : "memory");
+            if (threadIdx.x == 0) {
+                // the step's scalars on the shared-memory copy, then written back whole;
+                // the counter is reset last, by a release store, which lets the others go
+                double total = 0.0;
+                for (uint32_t rr = 0; rr < N; ++rr)
+                    total += rank_sum[rr];
+                zero_step_state_t& ls = s_st;
+                const uint32_t overflow = __ldcg(&st->overflow) != 0;
+                const uint32_t t_next = ls.t + 1;
+                if (!overflow) {
+                    ls.step_size = s_step;
+                    ls.rbc2 = s_rbc2;
+                }
+                if (STAGED)
+                    scaler_apply(&ls, s_cand, overflow, t_next);
+                else
+                    scaler_update(&ls, a.hp, N, overflow, t_next);
+                const double norm = sqrt(total);
+                ls.sumsq = total;
+                ls.norm = norm;
+                ls.clip_coef = clip_coefficient(norm, overflow, a.hp.max_grad_norm);
+                ls.overflow = 0;
+                ls.n_steps += 1;
+                ls.arrivals = gridDim.x;  // still "not released" until the store below
+                ls.error |= __ldcg(&st->error);
+                for (int q = 0; q < (int)(sizeof(zero_step_state_t) / 16); ++q)
+                    __stcg(reinterpret_cast<uint4*>(st) + q, reinterpret_cast<const uint4*>(&ls)[q]);
+                st_release_u32(&st->arrivals, 0u);
+            }
+        } else if (s_flag == 0 && threadIdx.x == 0) {
+            // wait for the last block to reset the counter, at most ~2 s
+            const long long t0 = clock64();
+            uint32_t ok = 1;
+            while (ld_acquire_u32(&st->arrivals) != 0) {
+                if (clock64() - t0 > 4000000000LL) {
+                    ok = 0;
+                    atomicOr(&st->error, 1u);
+                    break;
+                }
+                __nanosleep(64);
+            }
+            s_flag = ok;
         }
-        s_flag = ok;
+    } else if (STAGED && staged_copy) {
+        // staged: meanwhile the other warps update the tile speculatively with c = 1 (the
+        // step's other scalars need no norm) into the shared-memory copies of master, m
+        // and v and a shared-memory copy of the gathered parameters.  c = 1 multiplies g
+        // exactly, so if the step's clip coefficient turns out to be 1 these are the
+        // step's bits; otherwise they are dropped and the update is made from global memory
+        asm volatile("bar.sync 3, %0;" ::"n"(S::kThreads) : "memory");
+        const int t = threadIdx.x - kFusedThreads;
+        if (t == 0) {
+            s_spec = wait_parity_bounded(bar, 0);
+            if (!s_spec)
+                atomicOr(&st->error, 1u);
+        }
+        asm volatile("bar.sync 4, %0;" ::"n"(S::kThreads - kFusedThreads) : "memory");
+        if (s_spec) {
+            Scalars sc;
+            sc.c = 1.0f;
+            sc.step = s_step;
+            sc.rbc2 = s_rbc2;
+            sc.decay = s_cand.decay;
+            sc.b1 = a.hp.beta1;
+            sc.b2 = a.hp.beta2;
+            sc.omb1 = __fsub_rn(1.0f, a.hp.beta1);
+            sc.omb2 = __fsub_rn(1.0f, a.hp.beta2);
+            sc.eps = a.hp.eps;
+            const uint64_t v_end = v_hi < (a.psi & ~3ull) ? v_hi : (a.psi & ~3ull);  // may be < v_lo
+            uint16_t* const so = reinterpret_cast<uint16_t*>(sv + kGcFloats);
+            for (uint64_t i = v_lo + 4ull * t; i < v_end; i += 4ull * (S::kThreads - kFusedThreads)) {
+                const uint64_t k = i - base;
+                const float4 g4 = *reinterpret_cast<const float4*>(gc + k);
+                float4 p4 = *reinterpret_cast<const float4*>(sp + k);
+                float4 m4 = *reinterpret_cast<const float4*>(sm + k);
+                float4 v4 = *reinterpret_cast<const float4*>(sv + k);
+                uint2 o;
+                if (a.out_f16) {
+                    o.x = pack2<true>(adamw_one(g4.x, p4.x, m4.x, v4.x, sc), adamw_one(g4.y, p4.y, m4.y, v4.y, sc));
+                    o.y = pack2<true>(adamw_one(g4.z, p4.z, m4.z, v4.z, sc), adamw_one(g4.w, p4.w, m4.w, v4.w, sc));
+                } else {
+                    o.x = pack2<false>(adamw_one(g4.x, p4.x, m4.x, v4.x, sc), adamw_one(g4.y, p4.y, m4.y, v4.y, sc));
+                    o.y = pack2<false>(adamw_one(g4.z, p4.z, m4.z, v4.z, sc), adamw_one(g4.w, p4.w, m4.w, v4.w, sc));
+                }
+                *reinterpret_cast<float4*>(sp + k) = p4;
+                *reinterpret_cast<float4*>(sm + k) = m4;
+                *reinterpret_cast<float4*>(sv + k) = v4;
+                *reinterpret_cast<uint2*>(so + k) = o;
+            }
+        }
+    } else if (STAGED) {
+        asm volatile("bar.sync 3, %0;" ::"n"(S::kThreads) : "memory");
     }
     __syncthreads();
 
-    // 3. AdamW over the tile from the g held in shared memory, unless the step is skipped
-    // or this block gave up waiting
+    // 3. AdamW over the tile, unless the step is skipped or this block gave up waiting:
+    // staged with c = 1, write the speculative results out; otherwise update from the g
+    // held in shared memory and master, m, v in global memory
     if (threadIdx.x == 0) {
         uint32_t go = s_flag == 1 && __ldcg(&st->skip) == 0 && lo < hi;
-        if (go && staged_copy && !wait_parity_bounded(bar, 0)) {
-            atomicOr(&st->error, 1u);
-            go = 0;
-        }
-        s_flag = go;
         s_sc.c = __ldcg(&st->clip_coef);
         s_sc.step = __ldcg(&st->step_size);
         s_sc.rbc2 = __ldcg(&st->rbc2);
@@ -392,10 +458,30 @@ k_step_fused(const __grid_constant__ FusedArgs a)
         s_sc.omb1 = __fsub_rn(1.0f, a.hp.beta1);
         s_sc.omb2 = __fsub_rn(1.0f, a.hp.beta2);
         s_sc.eps = a.hp.eps;
+        // mode: 0 nothing, 1 write the speculative results out, 3 update from global
+        // memory
+        uint32_t mode = 0;
+        if (go) {
+            if (!STAGED)
+                mode = 3;
+            else if (!staged_copy)
+                mode = 3;  // no body: only edge elements, from global memory
+            else if (s_spec && s_sc.c == 1.0f)
+                mode = 1;
+            else
+                mode = s_spec ? 3 : 0;  // speculation overwrote the copies; a failed copy wrote nothing
+        }
+        s_flag = mode;
     }
     __syncthreads();
-    if (s_flag) {
+    const uint32_t mode = s_flag;
+    if (mode != 0) {
         const Scalars& sc = s_sc;
+        // [v_lo, v_end): whole 4-element groups below psi; [v_end, v_hi): the group holding
+        // psi and the padding (v_end is never below v_lo: a tile that starts past psi has
+        // no vector part)
+        uint64_t v_end = v_hi < (a.psi & ~3ull) ? v_hi : (a.psi & ~3ull);
+        v_end = v_end > v_lo ? v_end : v_lo;
         if (v_lo >= v_hi) {
             for (uint64_t i = lo + threadIdx.x; i < hi; i += S::kThreads)
                 update_one(a, i, gc[i - base], sc);
@@ -404,34 +490,40 @@ k_step_fused(const __grid_constant__ FusedArgs a)
                 update_one(a, lo + threadIdx.x, gc[lo + threadIdx.x - base], sc);
             if (v_hi + threadIdx.x < hi)
                 update_one(a, v_hi + threadIdx.x, gc[v_hi + threadIdx.x - base], sc);
-            // Q 4-element groups per thread at a time: all their loads before any store
-            // (the arrays may alias as far as the compiler knows, so it would not hoist
-            // them itself)
-            constexpr int Q = STAGED ? 1 : 3;
-            const uint64_t v_end = v_hi < (a.psi & ~3ull) ? v_hi : (a.psi & ~3ull);  // groups < psi
-            for (uint64_t i0 = v_lo + 4ull * threadIdx.x; i0 < v_hi; i0 += 4ull * S::kThreads * Q) {
-                float4 p4[Q], m4[Q], v4[Q];
+            // the groups holding psi or padding, element by element
+            for (uint64_t i = v_end + 4ull * threadIdx.x; i < v_hi; i += 4ull * S::kThreads)
+                for (int e = 0; e < 4; ++e)
+                    update_one(a, i + e, gc[i + e - base], sc);
+            if (mode == 1) {
+                const uint16_t* const so = reinterpret_cast<const uint16_t*>(sv + kGcFloats);
+                for (uint64_t i = v_lo + 4ull * threadIdx.x; i < v_end; i += 4ull * S::kThreads) {
+                    const uint64_t k = i - base;
+                    __stcs(reinterpret_cast<float4*>(a.master + i), *reinterpret_cast<const float4*>(sp + k));
+                    __stcs(reinterpret_cast<float4*>(a.m + i), *reinterpret_cast<const float4*>(sm + k));
+                    __stcs(reinterpret_cast<float4*>(a.v + i), *reinterpret_cast<const float4*>(sv + k));
+                    __stcs(reinterpret_cast<uint2*>(a.out + i), *reinterpret_cast<const uint2*>(so + k));
+                }
+            } else {
+                // Q 4-element groups per thread at a time: all their loads before any store
+                // (the arrays may alias as far as the compiler knows, so it would not hoist
+                // them itself)
+                constexpr int Q = 3;
+                for (uint64_t i0 = v_lo + 4ull * threadIdx.x; i0 < v_end; i0 += 4ull * S::kThreads * Q) {
+                    float4 p4[Q], m4[Q], v4[Q];
 #pragma unroll
-                for (int q = 0; q < Q; ++q) {
-                    const uint64_t i = i0 + 4ull * S::kThreads * q;
-                    if (i < v_end) {
-                        if (STAGED) {
-                            p4[q] = *reinterpret_cast<const float4*>(sp + (i - base));
-                            m4[q] = *reinterpret_cast<const float4*>(sm + (i - base));
-                            v4[q] = *reinterpret_cast<const float4*>(sv + (i - base));
-                        } else {
+                    for (int q = 0; q < Q; ++q) {
+                        const uint64_t i = i0 + 4ull * S::kThreads * q;
+                        if (i < v_end) {
                             p4[q] = __ldcs(reinterpret_cast<const float4*>(a.master + i));
                             m4[q] = __ldcs(reinterpret_cast<const float4*>(a.m + i));
                             v4[q] = __ldcs(reinterpret_cast<const float4*>(a.v + i));
                         }
                     }
-                }
 #pragma unroll
-                for (int q = 0; q < Q; ++q) {
-                    const uint64_t i = i0 + 4ull * S::kThreads * q;
-                    if (i >= v_hi)
-                        break;
-                    if (i < v_end) {
+                    for (int q = 0; q < Q; ++q) {
+                        const uint64_t i = i0 + 4ull * S::kThreads * q;
+                        if (i >= v_end)
+                            break;
                         const float4 g4 = *reinterpret_cast<const float4*>(gc + (i - base));
                         uint2 o;
                         if (a.out_f16) {
@@ -449,9 +541,6 @@ k_step_fused(const __grid_constant__ FusedArgs a)
                         __stcs(reinterpret_cast<float4*>(a.m + i), m4[q]);
                         __stcs(reinterpret_cast<float4*>(a.v + i), v4[q]);
                         __stcs(reinterpret_cast<uint2*>(a.out + i), o);
-                    } else {  // the group holding psi, or padding: element by element
-                        for (int e = 0; e < 4; ++e)
-                            update_one(a, i + e, gc[i + e - base], sc);
                     }
                 }
             }
@@ -459,7 +548,7 @@ k_step_fused(const __grid_constant__ FusedArgs a)
     }
     // staged: the bulk copies land in this block's shared memory; never leave before they
     // have (bounded), whatever the path taken above
-    if (staged_copy && threadIdx.x == 0 && !s_flag && !wait_parity_bounded(bar, 0))
+    if (staged_copy && threadIdx.x == 0 && !s_spec && !wait_parity_bounded(bar, 0))
         atomicOr(&st->error, 1u);
 }
 
