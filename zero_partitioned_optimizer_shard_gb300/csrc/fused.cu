@@ -23,6 +23,9 @@
  *      writes the gathered parameters.  Master, m and v were fetched while step 1 ran:
  *      into shared memory by bulk copies when the layout has at most one tile per SM
  *      (the staged shape, 17 warps), else into L2 by prefetches (9 warps, 3 blocks/SM).
+ *      In the staged shape the 9 warps that do not stream have already updated the tile
+ *      in shared memory with c = 1 while the norm was formed; a block whose step has
+ *      c = 1 (c = 1 multiplies g exactly: the same bits) only writes those results out.
  *
  * So the results are bit-identical to the three-launch step, and the traffic is
  * 2N + 26 bytes per parameter (+4 when g is written), not 2N + 34.  "【论文解读】ZeRO"
