@@ -473,10 +473,16 @@ def _e2e(args, z, torch, dev, wl, hp, reps, g, partials, master, m, v, out, st, 
     gdt = z.ZERO_F16 if wl.grad_dtype == "f16" else z.ZERO_BF16
     hstate = torch.empty(z.STATE_BYTES, dtype=torch.uint8, pin_memory=True)
     cs = torch.cuda.Stream(dev)
-    steps = max(1, args.e2e_steps)
     z.zero_step_host(lay, hp, gdt, hreps, staging, staging.numel() * 2, g, partials,
                      master, m, v, out, st, hstate, stream, cs)
     torch.cuda.synchronize(dev)
+    # at least --e2e-steps, and enough steps for ~50 ms of host-clock timing on small buffers
+    t0 = time.perf_counter()
+    z.zero_step_host(lay, hp, gdt, hreps, staging, staging.numel() * 2, g, partials,
+                     master, m, v, out, st, hstate, stream, cs)
+    stream.synchronize()
+    one = time.perf_counter() - t0
+    steps = max(1, args.e2e_steps, min(1000, int(0.05 / max(one, 1e-6))))
     t0 = time.perf_counter()
     for _ in range(steps):
         z.zero_step_host(lay, hp, gdt, hreps, staging, staging.numel() * 2, g, partials,
