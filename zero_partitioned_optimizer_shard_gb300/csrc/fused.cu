@@ -56,7 +56,8 @@ __device__ unsigned long long zero_test_absent_block = ~0ull;
 
 constexpr int kFusedWarps = 8;                       // stream the gradients (phase 1)
 constexpr int kFusedThreads = kFusedWarps * 32;      // the reduce pass's block size
-constexpr int kFusedLoads = 8;                       // replica loads in flight per thread
+constexpr int kFusedLoads = 8;                       // replica loads in flight per thread (N <= 8)
+constexpr int kFusedLoadsWide = 16;                  // the generic kernel (N = 16, 64, ...)
 constexpr uint64_t kT = ZERO_TILE_ELEMS;
 constexpr int kGcFloats = (int)kT + 8;               // the tile's g from its first whole group
 
@@ -136,7 +137,7 @@ __device__ __forceinline__ void update_one(const FusedArgs& a, uint64_t i, float
 }
 
 template <zero_dtype_t DT, int NR, bool STAGED>
-__global__ void __launch_bounds__(Shape<STAGED>::kThreads, Shape<STAGED>::kMinBlocks)
+__global__ void __launch_bounds__(Shape<STAGED>::kThreads, NR == 0 && !STAGED ? 2 : Shape<STAGED>::kMinBlocks)
 k_step_fused(const __grid_constant__ FusedArgs a)
 {
     using S = Shape<STAGED>;
@@ -225,8 +226,9 @@ k_step_fused(const __grid_constant__ FusedArgs a)
     bool bad = false;
     if (w < kFusedWarps && lo < hi) {
         constexpr int GB = NR > 0 && NR < kFusedLoads ? kFusedLoads / NR : 1;  // groups per batch
+        constexpr int LB = NR > 0 && NR <= kFusedLoads ? kFusedLoads : kFusedLoadsWide;  // loads per batch
         for (uint64_t b0 = base + 8ull * threadIdx.x; b0 < hi; b0 += 8ull * kFusedThreads * GB) {
-            uint4 v[GB][NR > 0 && NR < kFusedLoads ? NR : kFusedLoads];
+            uint4 v[GB][NR > 0 && NR < kFusedLoads ? NR : LB];
             if (NR > 0 && NR < kFusedLoads) {
 #pragma unroll
                 for (int q = 0; q < GB; ++q) {
@@ -251,13 +253,13 @@ k_step_fused(const __grid_constant__ FusedArgs a)
                             add8<DT>(s, v[q][k]);
                     } else {
 #pragma unroll 1
-                        for (uint32_t k0 = 0; k0 < N; k0 += kFusedLoads) {
+                        for (uint32_t k0 = 0; k0 < N; k0 += LB) {
 #pragma unroll
-                            for (int kk = 0; kk < kFusedLoads; ++kk)
+                            for (int kk = 0; kk < LB; ++kk)
                                 if (k0 + kk < N)
                                     v[0][kk] = ld_stream_v4((const uint16_t*)a.rep[k0 + kk] + b);
 #pragma unroll
-                            for (int kk = 0; kk < kFusedLoads; ++kk)
+                            for (int kk = 0; kk < LB; ++kk)
                                 if (k0 + kk < N)
                                     add8<DT>(s, v[0][kk]);
                         }
