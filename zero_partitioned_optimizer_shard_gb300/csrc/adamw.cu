@@ -30,6 +30,8 @@
  */
 #include "adamw_elem.cuh"
 
+#include <atomic>
+
 namespace zero {
 namespace {
 
@@ -162,17 +164,17 @@ extern "C" int zero_test_withhold_adamw_chunk(unsigned long long chunk)
 
 cudaError_t launch_adamw(const AdamwArgs& a, cudaStream_t s)
 {
-    static bool configured[64] = {false};
+    static std::atomic<bool> configured[64];  // per device; a race only repeats the set-up
     int dev = 0;
     cudaGetDevice(&dev);
-    if (!configured[dev & 63]) {
+    if (!configured[dev & 63].load(std::memory_order_relaxed)) {
         for (auto kern : {k_adamw<false>, k_adamw<true>}) {
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  (int)kSmemBytes);
             if (e != cudaSuccess)
                 return e;
         }
-        configured[dev & 63] = true;
+        configured[dev & 63].store(true, std::memory_order_relaxed);
     }
     const uint64_t chunks = a.psi / kChunk;
     const uint64_t tail_blocks = (a.psi_padded - chunks * kChunk + kBlock - 1) / kBlock;

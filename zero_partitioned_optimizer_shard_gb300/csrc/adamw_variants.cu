@@ -8,6 +8,8 @@
  */
 #include "adamw_elem.cuh"
 
+#include <atomic>
+
 namespace zero {
 namespace {
 
@@ -241,10 +243,10 @@ __global__ void __launch_bounds__(kBlock) k_adamw_host_state(const __grid_consta
 
 cudaError_t launch_adamw_rereduce(const AdamwArgs& a, cudaStream_t s)
 {
-    static bool configured[64] = {false};
+    static std::atomic<bool> configured[64];  // per device; a race only repeats the set-up
     int dev = 0;
     cudaGetDevice(&dev);
-    if (!configured[dev & 63]) {
+    if (!configured[dev & 63].load(std::memory_order_relaxed)) {
         for (auto kern : {k_adamw_rereduce<ZERO_BF16, false>, k_adamw_rereduce<ZERO_BF16, true>,
                           k_adamw_rereduce<ZERO_F16, false>, k_adamw_rereduce<ZERO_F16, true>}) {
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -252,7 +254,7 @@ cudaError_t launch_adamw_rereduce(const AdamwArgs& a, cudaStream_t s)
             if (e != cudaSuccess)
                 return e;
         }
-        configured[dev & 63] = true;
+        configured[dev & 63].store(true, std::memory_order_relaxed);
     }
     const uint64_t chunks = a.psi / kChunk;
     const uint64_t tail_blocks = (a.psi_padded - chunks * kChunk + kBlock - 1) / kBlock;

@@ -44,6 +44,8 @@
 #include "reduce_elem.cuh"
 #include "step_scalars.cuh"
 
+#include <atomic>
+
 namespace zero {
 namespace {
 
@@ -563,10 +565,10 @@ struct FusedKernel {
     using S = Shape<STAGED>;
     static int capacity()  // blocks that can be resident at once, cached per device
     {
-        static int cap[64] = {0};
+        static std::atomic<int> cap[64];  // per device; a race only repeats the query
         int dev = 0;
         cudaGetDevice(&dev);
-        int& c = cap[dev & 63];
+        int c = cap[dev & 63].load(std::memory_order_relaxed);
         if (c == 0) {
             int o = 0;
             if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -574,6 +576,7 @@ struct FusedKernel {
                 cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kernel, S::kThreads, S::kSmem);
             cudaGetLastError();  // a refused attribute or query leaves no error behind
             c = o > 0 ? o * sm_count() : -1;
+            cap[dev & 63].store(c, std::memory_order_relaxed);
         }
         return c;
     }
@@ -581,10 +584,10 @@ struct FusedKernel {
     {
         // cooperative (all blocks resident together) and, where the driver accepts the
         // pair, programmatic dependent launch; the choice is remembered per device
-        static int mode[64] = {0};  // 0 unknown, 1 both attributes, 2 cooperative only
+        static std::atomic<int> mode[64];  // 0 unknown, 1 both attributes, 2 cooperative only
         int dev = 0;
         cudaGetDevice(&dev);
-        int& md = mode[dev & 63];
+        std::atomic<int>& md = mode[dev & 63];
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(grid);
         cfg.blockDim = dim3(S::kThreads);

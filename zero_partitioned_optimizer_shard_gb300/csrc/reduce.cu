@@ -34,6 +34,8 @@
  */
 #include "reduce_elem.cuh"
 
+#include <atomic>
+
 namespace zero {
 namespace {
 
@@ -159,14 +161,15 @@ __global__ void __launch_bounds__(kBlock) k_reduce(const __grid_constant__ Reduc
 template <zero_dtype_t DT, int NR>
 cudaError_t launch_t(const ReduceArgs& a, cudaStream_t s)
 {
-    static int per_sm[64] = {0};
+    static std::atomic<int> per_sm[64];  // per device; a race only repeats the query
     int dev = 0;
     cudaGetDevice(&dev);
-    int& occ = per_sm[dev & 63];
+    int occ = per_sm[dev & 63].load(std::memory_order_relaxed);
     if (occ == 0) {
         int o = 0;
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, k_reduce<DT, NR>, kBlock, 0);
         occ = o > 0 ? o : 1;
+        per_sm[dev & 63].store(occ, std::memory_order_relaxed);
     }
     const uint64_t cap = (uint64_t)sm_count() * (uint64_t)occ;
     const unsigned grid = (unsigned)(a.unit_count < cap ? a.unit_count : cap);
