@@ -127,7 +127,8 @@ typedef struct zero_step_state {
     uint32_t n_ranks;
     uint32_t n_steps;       /* finalised steps, applied or skipped */
     uint32_t n_skipped;
-    uint32_t error;         /* device error word: 0 = none; 1 = a bounded wait gave up */
+    uint32_t error;         /* device error word: 0 = none; 1 = a bounded wait gave up;
+                               2 = (checked test builds only) a store outside its range */
     uint32_t arrivals;      /* internal to zero_grad_norm: its blocks that have finished
                                (0 between steps; keep it 0 when writing a state) */
     float inv_scale_used;   /* the inv_scale the last finalised step's reduce used */

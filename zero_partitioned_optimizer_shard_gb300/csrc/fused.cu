@@ -123,9 +123,12 @@ __device__ __forceinline__ void bulk_to_smem(void* dst, const void* src, uint32_
                  ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
 
-/* AdamW of one element i < psi, or the padding's gathered 0. */
-__device__ __forceinline__ void update_one(const FusedArgs& a, uint64_t i, float g, const Scalars& s)
+/* AdamW of one element i < psi, or the padding's gathered 0; [lo, hi) is the block's tile. */
+__device__ __forceinline__ void update_one(const FusedArgs& a, uint64_t i, float g, const Scalars& s,
+                                           uint64_t lo, uint64_t hi)
 {
+    if (!ZERO_OWNED(i, 1, lo, hi, &a.st->error))
+        return;
     if (i < a.psi) {
         float p = a.master[i], m = a.m[i], v = a.v[i];
         const float r = adamw_one(g, p, m, v, s);
@@ -281,9 +284,11 @@ k_step_fused(const __grid_constant__ FusedArgs a)
                 group_values(a.psi, inv, s, b, lo, hi, acc, bad, gv, in, full);
                 float* c = gc + (b - base);
                 if (full) {
-                    *reinterpret_cast<float4*>(c) = make_float4(gv[0], gv[1], gv[2], gv[3]);
-                    *reinterpret_cast<float4*>(c + 4) = make_float4(gv[4], gv[5], gv[6], gv[7]);
-                    if (a.g) {
+                    if (ZERO_OWNED(b - base, 8, 0, kGcFloats, &st->error)) {
+                        *reinterpret_cast<float4*>(c) = make_float4(gv[0], gv[1], gv[2], gv[3]);
+                        *reinterpret_cast<float4*>(c + 4) = make_float4(gv[4], gv[5], gv[6], gv[7]);
+                    }
+                    if (a.g && ZERO_OWNED(b, 8, lo, hi, &st->error)) {
                         __stcs(reinterpret_cast<float4*>(a.g + b), make_float4(gv[0], gv[1], gv[2], gv[3]));
                         __stcs(reinterpret_cast<float4*>(a.g + b + 4), make_float4(gv[4], gv[5], gv[6], gv[7]));
                     }
@@ -291,8 +296,9 @@ k_step_fused(const __grid_constant__ FusedArgs a)
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         if (in >> e & 1u) {
-                            c[e] = gv[e];
-                            if (a.g)
+                            if (ZERO_OWNED(b + e - base, 1, 0, kGcFloats, &st->error))
+                                c[e] = gv[e];
+                            if (a.g && ZERO_OWNED(b + e, 1, lo, hi, &st->error))
                                 a.g[b + e] = gv[e];
                         }
                 }
@@ -440,10 +446,12 @@ k_step_fused(const __grid_constant__ FusedArgs a)
                     o.x = pack2<false>(adamw_one(g4.x, p4.x, m4.x, v4.x, sc), adamw_one(g4.y, p4.y, m4.y, v4.y, sc));
                     o.y = pack2<false>(adamw_one(g4.z, p4.z, m4.z, v4.z, sc), adamw_one(g4.w, p4.w, m4.w, v4.w, sc));
                 }
-                *reinterpret_cast<float4*>(sp + k) = p4;
-                *reinterpret_cast<float4*>(sm + k) = m4;
-                *reinterpret_cast<float4*>(sv + k) = v4;
-                *reinterpret_cast<uint2*>(so + k) = o;
+                if (ZERO_OWNED(k, 4, 0, kGcFloats, &st->error)) {
+                    *reinterpret_cast<float4*>(sp + k) = p4;
+                    *reinterpret_cast<float4*>(sm + k) = m4;
+                    *reinterpret_cast<float4*>(sv + k) = v4;
+                    *reinterpret_cast<uint2*>(so + k) = o;
+                }
             }
         }
     } else if (STAGED) {
@@ -491,20 +499,22 @@ k_step_fused(const __grid_constant__ FusedArgs a)
         v_end = v_end > v_lo ? v_end : v_lo;
         if (v_lo >= v_hi) {
             for (uint64_t i = lo + threadIdx.x; i < hi; i += S::kThreads)
-                update_one(a, i, gc[i - base], sc);
+                update_one(a, i, gc[i - base], sc, lo, hi);
         } else {
             if (lo + threadIdx.x < v_lo)
-                update_one(a, lo + threadIdx.x, gc[lo + threadIdx.x - base], sc);
+                update_one(a, lo + threadIdx.x, gc[lo + threadIdx.x - base], sc, lo, hi);
             if (v_hi + threadIdx.x < hi)
-                update_one(a, v_hi + threadIdx.x, gc[v_hi + threadIdx.x - base], sc);
+                update_one(a, v_hi + threadIdx.x, gc[v_hi + threadIdx.x - base], sc, lo, hi);
             // the groups holding psi or padding, element by element
             for (uint64_t i = v_end + 4ull * threadIdx.x; i < v_hi; i += 4ull * S::kThreads)
                 for (int e = 0; e < 4; ++e)
-                    update_one(a, i + e, gc[i + e - base], sc);
+                    update_one(a, i + e, gc[i + e - base], sc, lo, hi);
             if (mode == 1) {
                 const uint16_t* const so = reinterpret_cast<const uint16_t*>(sv + kGcFloats);
                 for (uint64_t i = v_lo + 4ull * threadIdx.x; i < v_end; i += 4ull * S::kThreads) {
                     const uint64_t k = i - base;
+                    if (!ZERO_OWNED(i, 4, lo, hi, &st->error))
+                        continue;
                     __stcs(reinterpret_cast<float4*>(a.master + i), *reinterpret_cast<const float4*>(sp + k));
                     __stcs(reinterpret_cast<float4*>(a.m + i), *reinterpret_cast<const float4*>(sm + k));
                     __stcs(reinterpret_cast<float4*>(a.v + i), *reinterpret_cast<const float4*>(sv + k));
@@ -544,6 +554,8 @@ k_step_fused(const __grid_constant__ FusedArgs a)
                             o.y = pack2<false>(adamw_one(g4.z, p4[q].z, m4[q].z, v4[q].z, sc),
                                                adamw_one(g4.w, p4[q].w, m4[q].w, v4[q].w, sc));
                         }
+                        if (!ZERO_OWNED(i, 4, lo, hi, &st->error))
+                            continue;
                         __stcs(reinterpret_cast<float4*>(a.master + i), p4[q]);
                         __stcs(reinterpret_cast<float4*>(a.m + i), m4[q]);
                         __stcs(reinterpret_cast<float4*>(a.v + i), v4[q]);

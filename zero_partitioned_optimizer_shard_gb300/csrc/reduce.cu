@@ -74,12 +74,14 @@ __device__ __forceinline__ void finish_group(const ReduceArgs& a, float inv, flo
     if (!a.g) {
         // no g: the AdamW pass re-reads the gradient copies instead (small N)
     } else if (full) {
-        __stcs(reinterpret_cast<float4*>(a.g + b), make_float4(gv[0], gv[1], gv[2], gv[3]));
-        __stcs(reinterpret_cast<float4*>(a.g + b + 4), make_float4(gv[4], gv[5], gv[6], gv[7]));
+        if (ZERO_OWNED(b, 8, lo, hi, &a.st->error)) {
+            __stcs(reinterpret_cast<float4*>(a.g + b), make_float4(gv[0], gv[1], gv[2], gv[3]));
+            __stcs(reinterpret_cast<float4*>(a.g + b + 4), make_float4(gv[4], gv[5], gv[6], gv[7]));
+        }
     } else {
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-            if (in >> e & 1u)
+            if ((in >> e & 1u) && ZERO_OWNED(b + e, 1, lo, hi, &a.st->error))
                 a.g[b + e] = gv[e];
     }
 }

@@ -125,6 +125,26 @@ struct NvtxRange {
     NvtxRange& operator=(const NvtxRange&) = delete;
 };
 
+/* Checked builds (-DZERO_CHECKED, made by a test; never the product library): before each
+ * store of the reduce pass and of the single-launch step, ZERO_OWNED checks that elements
+ * [i, i+n) lie in [lo, hi), the range the storing block owns; a failed check records 2 in
+ * the step state's error word and the store is skipped, so an indexing mistake shows up
+ * as a status, not as a fault or a silently overwritten neighbour.  In the product build
+ * the check is the constant true and costs nothing. */
+#ifdef ZERO_CHECKED
+__device__ __forceinline__ bool zero_owned(uint64_t i, uint64_t n, uint64_t lo, uint64_t hi,
+                                           uint32_t* err)
+{
+    if (i >= lo && i + n <= hi)
+        return true;
+    atomicOr(err, 2u);
+    return false;
+}
+#define ZERO_OWNED(i, n, lo, hi, err) zero_owned((i), (n), (lo), (hi), (err))
+#else
+#define ZERO_OWNED(i, n, lo, hi, err) true
+#endif
+
 /* Launchers (enqueue only; return the launch's cudaError_t). */
 cudaError_t launch_reduce(const ReduceArgs& a, zero_dtype_t dtype, cudaStream_t s);
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s);
