@@ -194,9 +194,9 @@ k_step_fused(const __grid_constant__ FusedArgs a)
         bulk_to_smem(sv + (v_lo - base), a.v + v_lo, bytes, bar);
     }
     if (w == S::kScalarWarp) {
-        // a copy of the state for the last block (no block writes it before the last one
-        // arrives), and the bias corrections of step t+1: lanes 0 and 1 run the two fp64
-        // power chains side by side
+        // a copy of the state for the last block, and the bias corrections of step t+1
+        // (lanes 0 and 1 run the two fp64 power chains side by side); all read before this
+        // block arrives (barrier 5), so before the last block rewrites the state
         if (lane < (int)(sizeof(zero_step_state_t) / 16))
             reinterpret_cast<uint4*>(&s_st)[lane] = __ldcg(reinterpret_cast<const uint4*>(st) + lane);
         if (lane < 2) {
