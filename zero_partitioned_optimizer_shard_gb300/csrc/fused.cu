@@ -24,8 +24,11 @@
  *      into shared memory by bulk copies when the layout has at most one tile per SM
  *      (the staged shape, 17 warps), else into L2 by prefetches (9 warps, 3 blocks/SM).
  *      In the staged shape the 9 warps that do not stream have already updated the tile
- *      in shared memory with c = 1 while the norm was formed; a block whose step has
- *      c = 1 (c = 1 multiplies g exactly: the same bits) only writes those results out.
+ *      with c = 1 while the norm was formed (master, m, v written through to global
+ *      memory, the shared-memory copies kept); a block whose step has c = 1 (c = 1
+ *      multiplies g exactly: the same bits) only writes the gathered parameters; with
+ *      another c it updates again from the copies, and if the step does not apply it puts
+ *      master, m and v back from them.
  *
  * So the results are bit-identical to the three-launch step, and the traffic is
  * 2N + 26 bytes per parameter (+4 when g is written), not 2N + 34.  "【论文解读】ZeRO"
@@ -69,8 +72,8 @@ static_assert(kFusedThreads == 256, "the tile partial's bits depend on the reduc
  * up to 3 blocks per SM, master/m/v prefetched into L2.  Staged, for layouts of at most one
  * tile per SM: 17 warps (the 8 streaming ones, 8 more, the scalar warp); the tile's master,
  * m and v are bulk-copied into shared memory when the block starts, and the 9 other warps
- * update the tile speculatively with c = 1 there while the streaming warps fold, arrive
- * and wait for the norm. */
+ * update the tile speculatively with c = 1 from there while the streaming warps fold,
+ * arrive and wait for the norm. */
 template <bool STAGED>
 struct Shape {
     static constexpr int kScalarWarp = STAGED ? 16 : 8;
@@ -157,6 +160,7 @@ k_step_fused(const __grid_constant__ FusedArgs a)
     __shared__ __align__(8) uint64_t s_bar;            // staged: the bulk copies
     __shared__ uint32_t s_flag;  // last block; then: go on to the update
     __shared__ uint32_t s_spec;  // staged: the bulk copies landed and the speculation ran
+    __shared__ uint32_t s_edges;  // the tile's edge elements are updated
     grid_launch_dependents();
     grid_dependency_wait();
     zero_step_state_t* st = a.st;
@@ -407,10 +411,13 @@ k_step_fused(const __grid_constant__ FusedArgs a)
         }
     } else if (STAGED && staged_copy) {
         // staged: meanwhile the other warps update the tile speculatively with c = 1 (the
-        // step's other scalars need no norm) into the shared-memory copies of master, m
-        // and v and a shared-memory copy of the gathered parameters.  c = 1 multiplies g
-        // exactly, so if the step's clip coefficient turns out to be 1 these are the
-        // step's bits; otherwise they are dropped and the update is made from global memory
+        // step's other scalars need no norm) from the shared-memory copies of master, m
+        // and v, which stay as they are.  The new master, m and v go straight to global
+        // memory, so their writing overlaps the wait for the norm; the gathered parameters
+        // go to shared memory.  c = 1 multiplies g exactly, so if the step's clip
+        // coefficient turns out to be 1 these are the step's bits; if not they are made
+        // again with the real c, and if the step does not apply they are undone, both from
+        // the shared-memory copies
         asm volatile("bar.sync 3, %0;" ::"n"(S::kThreads) : "memory");
         const int t = threadIdx.x - kFusedThreads;
         if (t == 0) {
@@ -446,11 +453,12 @@ k_step_fused(const __grid_constant__ FusedArgs a)
                     o.x = pack2<false>(adamw_one(g4.x, p4.x, m4.x, v4.x, sc), adamw_one(g4.y, p4.y, m4.y, v4.y, sc));
                     o.y = pack2<false>(adamw_one(g4.z, p4.z, m4.z, v4.z, sc), adamw_one(g4.w, p4.w, m4.w, v4.w, sc));
                 }
-                if (ZERO_OWNED(k, 4, 0, kGcFloats, &st->error)) {
-                    *reinterpret_cast<float4*>(sp + k) = p4;
-                    *reinterpret_cast<float4*>(sm + k) = m4;
-                    *reinterpret_cast<float4*>(sv + k) = v4;
+                if (ZERO_OWNED(k, 4, 0, kGcFloats, &st->error))
                     *reinterpret_cast<uint2*>(so + k) = o;
+                if (ZERO_OWNED(i, 4, lo, hi, &st->error)) {
+                    __stcs(reinterpret_cast<float4*>(a.master + i), p4);
+                    __stcs(reinterpret_cast<float4*>(a.m + i), m4);
+                    __stcs(reinterpret_cast<float4*>(a.v + i), v4);
                 }
             }
         }
@@ -459,11 +467,13 @@ k_step_fused(const __grid_constant__ FusedArgs a)
     }
     __syncthreads();
 
-    // 3. AdamW over the tile, unless the step is skipped or this block gave up waiting:
-    // staged with c = 1, write the speculative results out; otherwise update from the g
-    // held in shared memory and master, m, v in global memory
+    // 3. AdamW over the tile, unless the step is skipped or this block gave up waiting.
+    // Staged, after the speculative update (master, m, v already written with c = 1): with
+    // c = 1 only the gathered parameters remain; with another c the tile is updated again
+    // from the shared-memory copies; if the step does not apply here, master, m and v are
+    // put back from them.  Otherwise the update reads master, m, v from global memory.
     if (threadIdx.x == 0) {
-        uint32_t go = s_flag == 1 && __ldcg(&st->skip) == 0 && lo < hi;
+        const uint32_t go = s_flag == 1 && __ldcg(&st->skip) == 0 && lo < hi;
         s_sc.c = __ldcg(&st->clip_coef);
         s_sc.step = __ldcg(&st->step_size);
         s_sc.rbc2 = __ldcg(&st->rbc2);
@@ -473,94 +483,103 @@ k_step_fused(const __grid_constant__ FusedArgs a)
         s_sc.omb1 = __fsub_rn(1.0f, a.hp.beta1);
         s_sc.omb2 = __fsub_rn(1.0f, a.hp.beta2);
         s_sc.eps = a.hp.eps;
-        // mode: 0 nothing, 1 write the speculative results out, 3 update from global
-        // memory
+        // mode: 0 nothing; 1 speculation kept (gathered parameters from shared memory);
+        // 2 update again from the shared-memory copies; 3 update from global memory;
+        // 4 undo the speculation (put master, m, v back)
         uint32_t mode = 0;
-        if (go) {
-            if (!STAGED)
-                mode = 3;
-            else if (!staged_copy)
-                mode = 3;  // no body: only edge elements, from global memory
-            else if (s_spec && s_sc.c == 1.0f)
-                mode = 1;
-            else
-                mode = s_spec ? 3 : 0;  // speculation overwrote the copies; a failed copy wrote nothing
-        }
+        const bool copy_failed = STAGED && staged_copy && !s_spec;  // error recorded: write nothing
+        if (STAGED && staged_copy && s_spec)
+            mode = !go ? 4 : s_sc.c == 1.0f ? 1 : 2;
+        else if (go && !copy_failed)
+            mode = 3;
         s_flag = mode;
+        s_edges = go && !copy_failed;
     }
     __syncthreads();
     const uint32_t mode = s_flag;
-    if (mode != 0) {
+    const bool edges = s_edges != 0;
+    {
         const Scalars& sc = s_sc;
         // [v_lo, v_end): whole 4-element groups below psi; [v_end, v_hi): the group holding
         // psi and the padding (v_end is never below v_lo: a tile that starts past psi has
         // no vector part)
         uint64_t v_end = v_hi < (a.psi & ~3ull) ? v_hi : (a.psi & ~3ull);
         v_end = v_end > v_lo ? v_end : v_lo;
-        if (v_lo >= v_hi) {
-            for (uint64_t i = lo + threadIdx.x; i < hi; i += S::kThreads)
-                update_one(a, i, gc[i - base], sc, lo, hi);
-        } else {
-            if (lo + threadIdx.x < v_lo)
-                update_one(a, lo + threadIdx.x, gc[lo + threadIdx.x - base], sc, lo, hi);
-            if (v_hi + threadIdx.x < hi)
-                update_one(a, v_hi + threadIdx.x, gc[v_hi + threadIdx.x - base], sc, lo, hi);
-            // the groups holding psi or padding, element by element
-            for (uint64_t i = v_end + 4ull * threadIdx.x; i < v_hi; i += 4ull * S::kThreads)
-                for (int e = 0; e < 4; ++e)
-                    update_one(a, i + e, gc[i + e - base], sc, lo, hi);
-            if (mode == 1) {
-                const uint16_t* const so = reinterpret_cast<const uint16_t*>(sv + kGcFloats);
-                for (uint64_t i = v_lo + 4ull * threadIdx.x; i < v_end; i += 4ull * S::kThreads) {
-                    const uint64_t k = i - base;
-                    if (!ZERO_OWNED(i, 4, lo, hi, &st->error))
-                        continue;
-                    __stcs(reinterpret_cast<float4*>(a.master + i), *reinterpret_cast<const float4*>(sp + k));
-                    __stcs(reinterpret_cast<float4*>(a.m + i), *reinterpret_cast<const float4*>(sm + k));
-                    __stcs(reinterpret_cast<float4*>(a.v + i), *reinterpret_cast<const float4*>(sv + k));
-                    __stcs(reinterpret_cast<uint2*>(a.out + i), *reinterpret_cast<const uint2*>(so + k));
-                }
+        if (edges) {
+            if (v_lo >= v_hi) {
+                for (uint64_t i = lo + threadIdx.x; i < hi; i += S::kThreads)
+                    update_one(a, i, gc[i - base], sc, lo, hi);
             } else {
-                // Q 4-element groups per thread at a time: all their loads before any store
-                // (the arrays may alias as far as the compiler knows, so it would not hoist
-                // them itself)
-                constexpr int Q = 3;
-                for (uint64_t i0 = v_lo + 4ull * threadIdx.x; i0 < v_end; i0 += 4ull * S::kThreads * Q) {
-                    float4 p4[Q], m4[Q], v4[Q];
+                if (lo + threadIdx.x < v_lo)
+                    update_one(a, lo + threadIdx.x, gc[lo + threadIdx.x - base], sc, lo, hi);
+                if (v_hi + threadIdx.x < hi)
+                    update_one(a, v_hi + threadIdx.x, gc[v_hi + threadIdx.x - base], sc, lo, hi);
+                // the groups holding psi or padding, element by element
+                for (uint64_t i = v_end + 4ull * threadIdx.x; i < v_hi; i += 4ull * S::kThreads)
+                    for (int e = 0; e < 4; ++e)
+                        update_one(a, i + e, gc[i + e - base], sc, lo, hi);
+            }
+        }
+        if (mode == 1) {
+            const uint16_t* const so = reinterpret_cast<const uint16_t*>(sv + kGcFloats);
+            for (uint64_t i = v_lo + 4ull * threadIdx.x; i < v_end; i += 4ull * S::kThreads)
+                if (ZERO_OWNED(i, 4, lo, hi, &st->error))
+                    __stcs(reinterpret_cast<uint2*>(a.out + i), *reinterpret_cast<const uint2*>(so + (i - base)));
+        } else if (mode == 4) {
+            for (uint64_t i = v_lo + 4ull * threadIdx.x; i < v_end; i += 4ull * S::kThreads) {
+                const uint64_t k = i - base;
+                if (!ZERO_OWNED(i, 4, lo, hi, &st->error))
+                    continue;
+                __stcs(reinterpret_cast<float4*>(a.master + i), *reinterpret_cast<const float4*>(sp + k));
+                __stcs(reinterpret_cast<float4*>(a.m + i), *reinterpret_cast<const float4*>(sm + k));
+                __stcs(reinterpret_cast<float4*>(a.v + i), *reinterpret_cast<const float4*>(sv + k));
+            }
+        } else if (mode == 2 || mode == 3) {
+            // Q 4-element groups per thread at a time: all their loads before any store
+            // (the arrays may alias as far as the compiler knows, so it would not hoist
+            // them itself)
+            constexpr int Q = 3;
+            for (uint64_t i0 = v_lo + 4ull * threadIdx.x; i0 < v_end; i0 += 4ull * S::kThreads * Q) {
+                float4 p4[Q], m4[Q], v4[Q];
 #pragma unroll
-                    for (int q = 0; q < Q; ++q) {
-                        const uint64_t i = i0 + 4ull * S::kThreads * q;
-                        if (i < v_end) {
+                for (int q = 0; q < Q; ++q) {
+                    const uint64_t i = i0 + 4ull * S::kThreads * q;
+                    if (i < v_end) {
+                        if (STAGED && mode == 2) {
+                            p4[q] = *reinterpret_cast<const float4*>(sp + (i - base));
+                            m4[q] = *reinterpret_cast<const float4*>(sm + (i - base));
+                            v4[q] = *reinterpret_cast<const float4*>(sv + (i - base));
+                        } else {
                             p4[q] = __ldcs(reinterpret_cast<const float4*>(a.master + i));
                             m4[q] = __ldcs(reinterpret_cast<const float4*>(a.m + i));
                             v4[q] = __ldcs(reinterpret_cast<const float4*>(a.v + i));
                         }
                     }
+                }
 #pragma unroll
-                    for (int q = 0; q < Q; ++q) {
-                        const uint64_t i = i0 + 4ull * S::kThreads * q;
-                        if (i >= v_end)
-                            break;
-                        const float4 g4 = *reinterpret_cast<const float4*>(gc + (i - base));
-                        uint2 o;
-                        if (a.out_f16) {
-                            o.x = pack2<true>(adamw_one(g4.x, p4[q].x, m4[q].x, v4[q].x, sc),
-                                              adamw_one(g4.y, p4[q].y, m4[q].y, v4[q].y, sc));
-                            o.y = pack2<true>(adamw_one(g4.z, p4[q].z, m4[q].z, v4[q].z, sc),
-                                              adamw_one(g4.w, p4[q].w, m4[q].w, v4[q].w, sc));
-                        } else {
-                            o.x = pack2<false>(adamw_one(g4.x, p4[q].x, m4[q].x, v4[q].x, sc),
-                                               adamw_one(g4.y, p4[q].y, m4[q].y, v4[q].y, sc));
-                            o.y = pack2<false>(adamw_one(g4.z, p4[q].z, m4[q].z, v4[q].z, sc),
-                                               adamw_one(g4.w, p4[q].w, m4[q].w, v4[q].w, sc));
-                        }
-                        if (!ZERO_OWNED(i, 4, lo, hi, &st->error))
-                            continue;
-                        __stcs(reinterpret_cast<float4*>(a.master + i), p4[q]);
-                        __stcs(reinterpret_cast<float4*>(a.m + i), m4[q]);
-                        __stcs(reinterpret_cast<float4*>(a.v + i), v4[q]);
-                        __stcs(reinterpret_cast<uint2*>(a.out + i), o);
+                for (int q = 0; q < Q; ++q) {
+                    const uint64_t i = i0 + 4ull * S::kThreads * q;
+                    if (i >= v_end)
+                        break;
+                    const float4 g4 = *reinterpret_cast<const float4*>(gc + (i - base));
+                    uint2 o;
+                    if (a.out_f16) {
+                        o.x = pack2<true>(adamw_one(g4.x, p4[q].x, m4[q].x, v4[q].x, sc),
+                                          adamw_one(g4.y, p4[q].y, m4[q].y, v4[q].y, sc));
+                        o.y = pack2<true>(adamw_one(g4.z, p4[q].z, m4[q].z, v4[q].z, sc),
+                                          adamw_one(g4.w, p4[q].w, m4[q].w, v4[q].w, sc));
+                    } else {
+                        o.x = pack2<false>(adamw_one(g4.x, p4[q].x, m4[q].x, v4[q].x, sc),
+                                           adamw_one(g4.y, p4[q].y, m4[q].y, v4[q].y, sc));
+                        o.y = pack2<false>(adamw_one(g4.z, p4[q].z, m4[q].z, v4[q].z, sc),
+                                           adamw_one(g4.w, p4[q].w, m4[q].w, v4[q].w, sc));
                     }
+                    if (!ZERO_OWNED(i, 4, lo, hi, &st->error))
+                        continue;
+                    __stcs(reinterpret_cast<float4*>(a.master + i), p4[q]);
+                    __stcs(reinterpret_cast<float4*>(a.m + i), m4[q]);
+                    __stcs(reinterpret_cast<float4*>(a.v + i), v4[q]);
+                    __stcs(reinterpret_cast<uint2*>(a.out + i), o);
                 }
             }
         }
