@@ -355,7 +355,7 @@ def run_ours(args):
         spread = None  # back-to-back steps: no event between them to keep launches overlapped
     params_per_s = wl.psi * args.steps * ws / (elapsed_ms / 1e3)
     bytes_26 = (26 + 2 * N) * P
-    moved = (30 + 2 * N) if launches == 1 else (34 + 2 * N)  # g written; re-read if split
+    moved = _fused_moved(N, lay, True) if launches == 1 else (34 + 2 * N)  # g re-read if split
     adamw_avg = statistics.mean(adamw_ms)
     reduce_avg = statistics.mean(reduce_ms)
     ach = ADAMW_BYTES * P / (adamw_avg / 1e3) / 1e9
@@ -393,7 +393,9 @@ def run_ours(args):
             "note": "(26+2N) B/param is the headline roofline; an exact step must also write "
                     "and re-read the fp32 gradient (34+2N) because clipping needs the global "
                     "norm before any update; the single-launch step of small layouts keeps g "
-                    "on chip (30+2N: g is written for the caller but not read back)",
+                    "on chip (30+2N: g is written for the caller but not read back; +2 with at "
+                    "most one tile per SM, where the gathered parameters are read so that the "
+                    "update made ahead of the norm can be undone)",
         },
         "roofline": roof,
         "kernels": {
@@ -430,6 +432,15 @@ def run_ours(args):
 
 def _pct(sorted_vals, q):  # nearest-rank percentile
     return sorted_vals[min(len(sorted_vals) - 1, max(0, round(q / 100 * len(sorted_vals)) - 1))]
+
+
+def _fused_moved(N: int, lay, g_written: bool) -> int:
+    """Bytes per parameter the single-launch step moves: the copies, master/m/v both ways
+    and the gathered parameters (26 + 2N), g when written (+4), and with at most one tile
+    per SM (the staged shape) the gathered parameters as found (+2)."""
+    import torch
+    staged = lay.n_tiles <= torch.cuda.get_device_properties(0).multi_processor_count
+    return 26 + 2 * N + (4 if g_written else 0) + (2 if staged else 0)
 
 
 def _traffic_from_profile(psi_padded):
@@ -552,7 +563,7 @@ def run_sweep(args):
                     moved = 26 + 4 * N if reread else 34 + 2 * N
                     launches = z.zero_step_launches(lay, z.ZERO_BF16)
                     if launches == 1:  # one launch, g kept on chip (written when given)
-                        moved = 26 + 2 * N if reread else 30 + 2 * N
+                        moved = _fused_moved(N, lay, not reread)
 
                     def step():
                         z.zero_step(lay, hp, z.ZERO_BF16, ptrs, g_arg, partials, bufs["master"],

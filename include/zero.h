@@ -132,7 +132,13 @@ typedef struct zero_step_state {
     uint32_t arrivals;      /* internal to zero_grad_norm: its blocks that have finished
                                (0 between steps; keep it 0 when writing a state) */
     float inv_scale_used;   /* the inv_scale the last finalised step's reduce used */
-    uint32_t reserved[10];
+    uint32_t launch_arrivals; /* internal to zero_step's single launch: its blocks that
+                               have finished their reduce (0 between steps; keep it 0
+                               when writing a state) */
+    float applied_c;        /* the clip coefficient the last finalised step applied, or -1
+                               when it was skipped; the single launch hands it to its
+                               blocks together with launch_arrivals in one 64-bit store */
+    uint32_t reserved[8];
 } zero_step_state_t;        /* 128 bytes */
 
 /* -------------------------------------------------------------------------------------
@@ -311,7 +317,8 @@ int zero_adamw_cast_gather_host_state(const zero_layout_t* layout,
  * bulk-copied in as the block starts), the block that finishes last forms the global norm
  * and the step's scalars, and every block then updates its tile.  g is still written when given
  * (never read back), so such a step moves 2N + 30 bytes per parameter, 2N + 26 with
- * g = NULL.  zero_step_launches tells which way a layout goes.  If the cooperative launch
+ * g = NULL (+2 with at most one tile per SM: the gathered parameters are read too, so
+ * that an update made ahead of the norm can be undone).  zero_step_launches tells which way a layout goes.  If the cooperative launch
  * is refused because fewer blocks fit on the GPU than its occupancy promised (another
  * context holds part of it), the same call makes the three launches instead.
  * ------------------------------------------------------------------------------------- */

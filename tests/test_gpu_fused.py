@@ -43,7 +43,7 @@ CASES = {
     "no-clip": replace(W.scaled(W.C2, 8 * 5000 + 1, steps=2),
                        hp=replace(W.C2.hp, max_grad_norm=0.0)),
     # clipping active in every step (c < 1): the staged shape's speculative update with
-    # c = 1 is dropped and the tile is updated again from global memory
+    # c = 1 is dropped and the tile is updated again from its shared-memory copies
     "clip-active": replace(W.scaled(W.C2, 8 * 8192 * 4 + 3, steps=3),
                            hp=replace(W.C2.hp, max_grad_norm=1e-4)),
     "psi5": replace(W.scaled(W.C1, 5, steps=2), n_ranks=4),
@@ -52,6 +52,32 @@ CASES = {
     "n8-many-tiles": W.scaled(W.C2, 8 * 8192 * 20 + 5, steps=2),
     "n3-many-tiles": replace(W.scaled(W.C2, 3 * 8192 * 60 + 1, steps=2), n_ranks=3),
 }
+
+
+@pytest.mark.parametrize("ulps", [-2, 0, 1, 40])
+def test_clip_threshold_same_bits_as_split(ulps):
+    """max_grad_norm a few float ulps around norm + 1e-6, so c is 1 exactly or just below.
+    Close to that threshold the single launch cannot release its blocks on the fp32
+    upper bound of the sum of squares and forms the exact norm first (ulps -2, 0, 1);
+    further above it releases them on the bound (40).  Both must give the separate
+    calls' bits."""
+    base = W.scaled(W.C2, 8 * 8192 * 4 + 3, steps=1)
+    norm = GpuRun(base).step(1).norm
+    m = np.float32(norm + 1e-6)
+    if float(m) < norm + 1e-6:
+        m = np.nextafter(m, np.float32(np.inf))  # the least float >= norm + 1e-6
+    for _ in range(abs(ulps)):
+        m = np.nextafter(m, np.float32(np.inf if ulps > 0 else -np.inf))
+    wl = replace(base, hp=replace(base.hp, max_grad_norm=float(m)))
+    fused, split = GpuRun(wl), GpuRun(wl, split=True)
+    assert z.zero_step_launches(fused.lay, dtype_code(wl)) == 1
+    sf, ss = fused.step(1), split.step(1)
+    assert bytes(sf) == bytes(ss), (sf.clip_coef, ss.clip_coef)
+    _arrays_equal(fused.arrays(), split.arrays())
+    if ulps >= 1:
+        assert sf.clip_coef == 1.0
+    if ulps < 0:
+        assert sf.clip_coef < 1.0
 
 
 def _arrays_equal(a: dict, b: dict):
@@ -69,7 +95,8 @@ def test_single_launch_equals_split_calls_bit_for_bit(name):
     for step in range(1, wl.steps + 1):
         sf, ss = fused.step(step), split.step(step)
         assert bytes(sf) == bytes(ss), (step, sf.norm, ss.norm, sf.clip_coef, ss.clip_coef)
-        assert sf.error == 0 and sf.arrivals == 0
+        assert sf.error == 0 and sf.arrivals == 0 and sf.launch_arrivals == 0
+        assert sf.applied_c == (-1.0 if sf.skip else sf.clip_coef)
         if name == "clip-active":
             assert sf.clip_coef < 1.0
         skipped += sf.skip

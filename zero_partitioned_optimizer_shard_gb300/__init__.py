@@ -55,7 +55,8 @@ class StepState(C.Structure):
         ("t", C.c_uint32), ("good_steps", C.c_uint32), ("growth_interval", C.c_uint32),
         ("dynamic", C.c_uint32), ("n_ranks", C.c_uint32), ("n_steps", C.c_uint32),
         ("n_skipped", C.c_uint32), ("error", C.c_uint32), ("arrivals", C.c_uint32),
-        ("inv_scale_used", C.c_float), ("reserved", C.c_uint32 * 10),
+        ("inv_scale_used", C.c_float), ("launch_arrivals", C.c_uint32),
+        ("applied_c", C.c_float), ("reserved", C.c_uint32 * 8),
     ]
 
 

@@ -138,7 +138,10 @@ __global__ void __launch_bounds__(kFinThreads) k_finalize(const __grid_constant_
     const double norm = sqrt(total);
     st->sumsq = total;
     st->norm = norm;
-    st->clip_coef = clip_coefficient(norm, __ldcg(&st->skip), a.hp.max_grad_norm);
+    const uint32_t skip = __ldcg(&st->skip);
+    const float c = clip_coefficient(norm, skip, a.hp.max_grad_norm);
+    st->clip_coef = c;
+    st->applied_c = skip ? -1.0f : c;
     st->overflow = 0;
     st->n_steps += 1;
 }

@@ -12,26 +12,32 @@
  *      arithmetic and thread-to-element mapping (reduce_elem.cuh), so g and the tile's
  *      partial come out with the same bits; g stays in shared memory (and is written to
  *      the caller's g buffer when one is given);
- *   2. the block stores its tile partial, ORs its overflow flag and arrives on the step
- *      state's arrival counter; the last block to arrive forms the global norm from the
+ *   2. the block stores its tile partial, ORs its overflow flag and arrives on the
+ *      launch's counter; the last block to arrive forms the global norm from the
  *      partials in the norm kernel's order (one warp per rank, the rank's slots
  *      lane-strided, a fixed shuffle tree, ranks in order; the order finalize.cu uses for
- *      layouts of at most 128 tiles per rank), applies the clip coefficient, skip
- *      decision and loss scaler (step_scalars.cuh), zeroes the partials and releases the
- *      other blocks by resetting the counter;
+ *      layouts of at most 128 tiles per rank) and the clip coefficient, and releases
+ *      the other blocks with one 64-bit store (the counter back to 0, the step's c or -1
+ *      for a skipped step) as soon as that outcome is certain (for c = 1, often from an
+ *      upward-rounded fp32 bound of the sum, before the exact norm); it zeroes the
+ *      partials and applies the skip decision and loss scaler to the state
+ *      (step_scalars.cuh); every block forms the step's other scalars (bias
+ *      corrections, decay) itself;
  *   3. every block applies AdamW to its tile from the g it holds (adamw_elem.cuh) and
  *      writes the gathered parameters.  Master, m and v were fetched while step 1 ran:
  *      into shared memory by bulk copies when the layout has at most one tile per SM
  *      (the staged shape, 17 warps), else into L2 by prefetches (9 warps, 3 blocks/SM).
  *      In the staged shape the 9 warps that do not stream have already updated the tile
- *      with c = 1 while the norm was formed (master, m, v written through to global
- *      memory, the shared-memory copies kept); a block whose step has c = 1 (c = 1
- *      multiplies g exactly: the same bits) only writes the gathered parameters; with
- *      another c it updates again from the copies, and if the step does not apply it puts
- *      master, m and v back from them.
+ *      with c = 1 while the norm was formed (master, m, v and the gathered parameters
+ *      written through to global memory, the shared-memory copies of master, m, v and of
+ *      the gathered parameters as found kept); a block whose step has c = 1 (c = 1
+ *      multiplies g exactly: the same bits) has only its tile's few edge elements left;
+ *      with another c it updates again from the copies, and if the step does not apply
+ *      it puts everything back from them.
  *
  * So the results are bit-identical to the three-launch step, and the traffic is
- * 2N + 26 bytes per parameter (+4 when g is written), not 2N + 34.  "【论文解读】ZeRO"
+ * 2N + 26 bytes per parameter (+4 when g is written; staged, +2 for reading the gathered
+ * parameters as found), not 2N + 34.  "【论文解读】ZeRO"
  * sec. 6(2) describes the same three stages per rank (reduce-scatter, shard update,
  * all-gather); only their scheduling differs.
  *
@@ -86,25 +92,44 @@ struct Shape {
     static constexpr size_t kSmem = (size_t)kGcFloats * 4 * (STAGED ? 4 : 1) + (STAGED ? (size_t)kGcFloats * 2 : 0);
 };
 
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p)
+/* The launch's 64-bit word: the state's launch_arrivals (low half, the arrival counter)
+ * and applied_c (high half, the step's outcome).  Arrival: acquire-release, so this
+ * block's writes are ordered before it and the last block to arrive sees every block's
+ * writes. */
+__device__ __forceinline__ uint64_t arrive_acq_rel(uint64_t* p)
 {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    uint64_t old;
+    asm volatile("atom.add.acq_rel.gpu.global.u64 %0, [%1], 1;" : "=l"(old) : "l"(p) : "memory");
+    return old;
+}
+
+/* The release and the wait for it: relaxed, single 64-bit accesses.  A waiting block
+ * takes nothing from the last block but the word itself (its other scalars are its own,
+ * its tile is disjoint from every other), so nothing needs ordering around them. */
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p)
+{
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
 
-__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v)
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v)
 {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-/* Arrival on the counter: acquire-release, so this block's writes are ordered before it
- * and the last block to arrive sees every block's writes. */
-__device__ __forceinline__ uint32_t arrive_acq_rel(uint32_t* p)
+/* True only when the clip coefficient min(1, max_norm / (norm + 1e-6)) of the exact fp64
+ * computation (clip_coefficient of the fp64 sum of the partials) is certainly 1, judged
+ * from u >= the exact sum of the partials, formed in fp32 with upward rounding.  With
+ * b = RU(sqrt(u)) >= sqrt(sum), the fp64 path's rounded sum exceeds the exact one by less
+ * than 2^-45 relatively, its square root and its + 1e-6 round up by 2^-53 at most, so its
+ * divisor is at most (b (1 + 2^-45) + 1e-6)(1 + 2^-53) < the bound formed here; a divisor
+ * <= max_norm gives a quotient >= 1, which stays >= 1 when rounded, so c = 1. */
+__device__ __forceinline__ bool clip_certainly_one(float u, float max_norm)
 {
-    uint32_t old;
-    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
-    return old;
+    const float b = __fsqrt_ru(u);
+    const float need = __fmul_ru(__fadd_ru(__fmul_ru(b, 1.000001f), 1.0000001e-6f), 1.000001f);
+    return max_norm >= need;
 }
 
 /* L2 prefetch of [p, p + n) floats, rounded inwards to 16-byte boundaries (a hint: the
@@ -153,17 +178,19 @@ k_step_fused(const __grid_constant__ FusedArgs a)
     float* const gc = dyn;                        // gc[i - base] holds g[i]
     __shared__ double warp_part[2][kFusedWarps];
     __shared__ double rank_sum[ZERO_MAX_KERNEL_RANKS];
-    __shared__ float s_step, s_rbc2;
+    __shared__ float rank_up[kFusedWarps];  // an upward-rounded fp32 bound of each rank's sum
+    __shared__ float s_step, s_rbc2, s_decay;
+    __shared__ float s_applied;  // the step's outcome: c, or -1 when the step is skipped
     __shared__ ScalerCand s_cand;  // staged: the scaler's outcomes, formed ahead of time
     __shared__ Scalars s_sc;
     __shared__ __align__(16) zero_step_state_t s_st;  // the state as this step found it
     __shared__ __align__(8) uint64_t s_bar;            // staged: the bulk copies
-    __shared__ uint32_t s_flag;  // last block; then: go on to the update
+    __shared__ uint32_t s_flag;  // last block; then: released (or last)
     __shared__ uint32_t s_spec;  // staged: the bulk copies landed and the speculation ran
-    __shared__ uint32_t s_edges;  // the tile's edge elements are updated
     grid_launch_dependents();
     grid_dependency_wait();
     zero_step_state_t* st = a.st;
+    uint64_t* const word = reinterpret_cast<uint64_t*>(&st->launch_arrivals);
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t N = NR > 0 ? (uint32_t)NR : a.n_ranks;
     const float inv = st->inv_scale;
@@ -183,8 +210,10 @@ k_step_fused(const __grid_constant__ FusedArgs a)
     float* const sv = sm + kGcFloats;
     const uint32_t bar = smem_addr(&s_bar);
 
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0) {
         s_spec = 0;
+        s_applied = -1.0f;
+    }
     if (staged_copy && threadIdx.x == 0) {
         // the tile's optimizer state into shared memory, in flight while the gradients are
         // summed; only the 16-byte-aligned body, the few edge elements are read directly
@@ -210,6 +239,8 @@ k_step_fused(const __grid_constant__ FusedArgs a)
             else
                 s_rbc2 = bias_rbc2(a.hp, t_next);
         }
+        if (lane == 3)
+            s_decay = decoupled_decay(a.hp);
         if (!STAGED && lane == 2 && lo < hi) {
             prefetch_l2(a.master + lo, hi - lo);
             prefetch_l2(a.m + lo, hi - lo);
@@ -335,21 +366,31 @@ k_step_fused(const __grid_constant__ FusedArgs a)
                 s_flag = 2;  // test builds only: this block never arrives
             else
 #endif
-            s_flag = arrive_acq_rel(&st->arrivals) == gridDim.x - 1;
+            s_flag = (uint32_t)arrive_acq_rel(word) == gridDim.x - 1;
         }
         asm volatile("bar.sync 2, %0;" ::"n"(kFusedThreads) : "memory");
 
         if (s_flag == 1) {
             // the last block: the norm in the norm kernel's order (at most 128 slots per
-            // rank: lane l adds slots l, l+32, l+64, l+96 in that order), partials zeroed
-            for (uint32_t rr = w; rr < N; rr += kFusedWarps) {
+            // rank: lane l adds slots l, l+32, l+64, l+96 in that order), partials zeroed;
+            // thread 0 fetches the overflow flag meanwhile.  The others are released as
+            // soon as their outcome is certain: at once for a skipped step, and, with at
+            // most one rank per warp, before the exact norm when an fp32 upper bound of
+            // the sum already shows c = 1 (clip_certainly_one); the exact norm, c and the
+            // state follow.
+            constexpr bool kEarly = NR > 0 && NR <= kFusedWarps;
+            uint32_t overflow = 0;
+            bool released = false;  // thread 0
+            if (threadIdx.x == 0)
+                overflow = __ldcg(&st->overflow) != 0;
+            auto release = [&](float applied) {
+                // the counter back to 0 and the outcome, in one store
+                st_relaxed_u64(word, (uint64_t)__float_as_uint(applied) << 32);
+                s_applied = applied;
+                released = true;
+            };
+            auto rank_sum_of = [&](uint32_t rr, const double (&v)[4]) {
                 double* p = a.partials + (uint64_t)rr * tpr;
-                double v[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint64_t c = lane + 32u * q;
-                    v[q] = c < tpr ? __ldcg(p + c) : 0.0;
-                }
                 double s = 0.0;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -364,16 +405,68 @@ k_step_fused(const __grid_constant__ FusedArgs a)
                     s += __shfl_xor_sync(0xffffffffu, s, o);
                 if (lane == 0)
                     rank_sum[rr] = s;
+            };
+            auto load_rank = [&](uint32_t rr, double (&v)[4]) {
+                const double* p = a.partials + (uint64_t)rr * tpr;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint64_t c = lane + 32u * q;
+                    v[q] = c < tpr ? __ldcg(p + c) : 0.0;
+                }
+            };
+            if (kEarly) {
+                double v[4];
+                if ((uint32_t)w < N) {
+                    load_rank(w, v);
+                    float up = 0.0f;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        up = __fadd_ru(up, __double2float_ru(v[q]));
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+                        up = __fadd_ru(up, __shfl_xor_sync(0xffffffffu, up, o));
+                    if (lane == 0)
+                        rank_up[w] = up;
+                }
+                asm volatile("bar.sync 2, %0;" ::"n"(kFusedThreads) : "memory");
+                if (threadIdx.x == 0) {
+                    if (overflow) {
+                        release(-1.0f);
+                    } else if (!(a.hp.max_grad_norm > 0.0f)) {
+                        release(1.0f);  // clipping disabled
+                    } else {
+                        float u = 0.0f;
+                        for (uint32_t rr = 0; rr < N; ++rr)
+                            u = __fadd_ru(u, rank_up[rr]);
+                        if (clip_certainly_one(u, a.hp.max_grad_norm))
+                            release(1.0f);
+                    }
+                }
+                if ((uint32_t)w < N)
+                    rank_sum_of(w, v);
+            } else {
+                if (threadIdx.x == 0 && overflow)
+                    release(-1.0f);
+                for (uint32_t rr = w; rr < N; rr += kFusedWarps) {
+                    double v[4];
+                    load_rank(rr, v);
+                    rank_sum_of(rr, v);
+                }
             }
             asm volatile("bar.sync 2, %0;" ::"n"(kFusedThreads) : "memory");
             if (threadIdx.x == 0) {
-                // the step's scalars on the shared-memory copy, then written back whole;
-                // the counter is reset last, by a release store, which lets the others go
                 double total = 0.0;
                 for (uint32_t rr = 0; rr < N; ++rr)
                     total += rank_sum[rr];
+                const double norm = sqrt(total);
+                const float c = clip_coefficient(norm, overflow, a.hp.max_grad_norm);
+                const float applied = overflow ? -1.0f : c;
+                if (!released)
+                    release(applied);
+                // the state for the next step, read after the launch: every field the step
+                // changes, never the error word (other blocks may still OR into it), the
+                // launch word (written above) or what the step leaves as it is
                 zero_step_state_t& ls = s_st;
-                const uint32_t overflow = __ldcg(&st->overflow) != 0;
                 const uint32_t t_next = ls.t + 1;
                 if (!overflow) {
                     ls.step_size = s_step;
@@ -383,23 +476,25 @@ k_step_fused(const __grid_constant__ FusedArgs a)
                     scaler_apply(&ls, s_cand, overflow, t_next);
                 else
                     scaler_update(&ls, a.hp, N, overflow, t_next);
-                const double norm = sqrt(total);
                 ls.sumsq = total;
                 ls.norm = norm;
-                ls.clip_coef = clip_coefficient(norm, overflow, a.hp.max_grad_norm);
+                ls.clip_coef = c;
                 ls.overflow = 0;
                 ls.n_steps += 1;
-                ls.arrivals = gridDim.x;  // still "not released" until the store below
-                ls.error |= __ldcg(&st->error);
-                for (int q = 0; q < (int)(sizeof(zero_step_state_t) / 16); ++q)
+                ls.applied_c = applied;
+                static_assert(offsetof(zero_step_state_t, n_ranks) == 64, "fields [0, 64) in four stores");
+                for (int q = 0; q < 4; ++q)
                     __stcg(reinterpret_cast<uint4*>(st) + q, reinterpret_cast<const uint4*>(&ls)[q]);
-                st_release_u32(&st->arrivals, 0u);
+                __stcg(&st->n_steps, ls.n_steps);
+                __stcg(&st->n_skipped, ls.n_skipped);
+                __stcg(&st->inv_scale_used, ls.inv_scale_used);
             }
         } else if (s_flag == 0 && threadIdx.x == 0) {
-            // wait for the last block to reset the counter, at most ~2 s
+            // wait for the last block's release, at most ~2 s
             const long long t0 = clock64();
             uint32_t ok = 1;
-            while (ld_acquire_u32(&st->arrivals) != 0) {
+            uint64_t wv;
+            while ((uint32_t)(wv = ld_relaxed_u64(word)) != 0) {
                 if (clock64() - t0 > 4000000000LL) {
                     ok = 0;
                     atomicOr(&st->error, 1u);
@@ -407,19 +502,54 @@ k_step_fused(const __grid_constant__ FusedArgs a)
                 }
                 __nanosleep(64);
             }
+            s_applied = __uint_as_float((uint32_t)(wv >> 32));
             s_flag = ok;
+        }
+        if (threadIdx.x == 0) {
+            // the update's scalars: the released c and this block's own step t + 1 scalars
+            // (the same bits as the last block's: same inputs, same arithmetic)
+            s_sc.c = s_applied;
+            s_sc.step = s_step;
+            s_sc.rbc2 = s_rbc2;
+            s_sc.decay = s_decay;
+            s_sc.b1 = a.hp.beta1;
+            s_sc.b2 = a.hp.beta2;
+            s_sc.omb1 = __fsub_rn(1.0f, a.hp.beta1);
+            s_sc.omb2 = __fsub_rn(1.0f, a.hp.beta2);
+            s_sc.eps = a.hp.eps;
         }
     } else if (STAGED && staged_copy) {
         // staged: meanwhile the other warps update the tile speculatively with c = 1 (the
         // step's other scalars need no norm) from the shared-memory copies of master, m
-        // and v, which stay as they are.  The new master, m and v go straight to global
-        // memory, so their writing overlaps the wait for the norm; the gathered parameters
-        // go to shared memory.  c = 1 multiplies g exactly, so if the step's clip
-        // coefficient turns out to be 1 these are the step's bits; if not they are made
-        // again with the real c, and if the step does not apply they are undone, both from
-        // the shared-memory copies
-        asm volatile("bar.sync 3, %0;" ::"n"(S::kThreads) : "memory");
+        // and v, which stay as they are.  The new master, m, v and gathered parameters go
+        // straight to global memory, so their writing overlaps the wait for the norm.
+        // c = 1 multiplies g exactly, so if the step's clip coefficient turns out to be 1
+        // these are the step's bits; if not they are made again with the real c, and if
+        // the step does not apply they are undone, both from the shared-memory copies (the
+        // gathered parameters as the step found them are kept for that too: each thread
+        // loads the 4-element groups it will update while the gradients are summed)
+        constexpr int kSpec = S::kThreads - kFusedThreads;
+        constexpr int kOutGroups = (int)((kT / 4 + kSpec - 1) / kSpec);
         const int t = threadIdx.x - kFusedThreads;
+        static_assert(4 * kOutGroups * kSpec >= (int)kT, "every group of a tile has a slot");
+        const uint64_t v_end = v_hi < (a.psi & ~3ull) ? v_hi : (a.psi & ~3ull);  // may be < v_lo
+        uint16_t* const so = reinterpret_cast<uint16_t*>(sv + kGcFloats);
+        {
+            uint2 o0[kOutGroups];
+#pragma unroll
+            for (int q = 0; q < kOutGroups; ++q) {
+                const uint64_t i = v_lo + 4ull * (t + q * kSpec);
+                if (i < v_end)
+                    o0[q] = __ldcs(reinterpret_cast<const uint2*>(a.out + i));
+            }
+#pragma unroll
+            for (int q = 0; q < kOutGroups; ++q) {
+                const uint64_t i = v_lo + 4ull * (t + q * kSpec);
+                if (i < v_end && ZERO_OWNED(i - base, 4, 0, kGcFloats, &st->error))
+                    *reinterpret_cast<uint2*>(so + (i - base)) = o0[q];
+            }
+        }
+        asm volatile("bar.sync 3, %0;" ::"n"(S::kThreads) : "memory");
         if (t == 0) {
             s_spec = wait_parity_bounded(bar, 0);
             if (!s_spec)
@@ -437,9 +567,7 @@ k_step_fused(const __grid_constant__ FusedArgs a)
             sc.omb1 = __fsub_rn(1.0f, a.hp.beta1);
             sc.omb2 = __fsub_rn(1.0f, a.hp.beta2);
             sc.eps = a.hp.eps;
-            const uint64_t v_end = v_hi < (a.psi & ~3ull) ? v_hi : (a.psi & ~3ull);  // may be < v_lo
-            uint16_t* const so = reinterpret_cast<uint16_t*>(sv + kGcFloats);
-            for (uint64_t i = v_lo + 4ull * t; i < v_end; i += 4ull * (S::kThreads - kFusedThreads)) {
+            for (uint64_t i = v_lo + 4ull * t; i < v_end; i += 4ull * kSpec) {
                 const uint64_t k = i - base;
                 const float4 g4 = *reinterpret_cast<const float4*>(gc + k);
                 float4 p4 = *reinterpret_cast<const float4*>(sp + k);
@@ -453,12 +581,11 @@ k_step_fused(const __grid_constant__ FusedArgs a)
                     o.x = pack2<false>(adamw_one(g4.x, p4.x, m4.x, v4.x, sc), adamw_one(g4.y, p4.y, m4.y, v4.y, sc));
                     o.y = pack2<false>(adamw_one(g4.z, p4.z, m4.z, v4.z, sc), adamw_one(g4.w, p4.w, m4.w, v4.w, sc));
                 }
-                if (ZERO_OWNED(k, 4, 0, kGcFloats, &st->error))
-                    *reinterpret_cast<uint2*>(so + k) = o;
                 if (ZERO_OWNED(i, 4, lo, hi, &st->error)) {
                     __stcs(reinterpret_cast<float4*>(a.master + i), p4);
                     __stcs(reinterpret_cast<float4*>(a.m + i), m4);
                     __stcs(reinterpret_cast<float4*>(a.v + i), v4);
+                    __stcs(reinterpret_cast<uint2*>(a.out + i), o);
                 }
             }
         }
@@ -468,36 +595,22 @@ k_step_fused(const __grid_constant__ FusedArgs a)
     __syncthreads();
 
     // 3. AdamW over the tile, unless the step is skipped or this block gave up waiting.
-    // Staged, after the speculative update (master, m, v already written with c = 1): with
-    // c = 1 only the gathered parameters remain; with another c the tile is updated again
-    // from the shared-memory copies; if the step does not apply here, master, m and v are
-    // put back from them.  Otherwise the update reads master, m, v from global memory.
-    if (threadIdx.x == 0) {
-        const uint32_t go = s_flag == 1 && __ldcg(&st->skip) == 0 && lo < hi;
-        s_sc.c = __ldcg(&st->clip_coef);
-        s_sc.step = __ldcg(&st->step_size);
-        s_sc.rbc2 = __ldcg(&st->rbc2);
-        s_sc.decay = __ldcg(&st->decay);
-        s_sc.b1 = a.hp.beta1;
-        s_sc.b2 = a.hp.beta2;
-        s_sc.omb1 = __fsub_rn(1.0f, a.hp.beta1);
-        s_sc.omb2 = __fsub_rn(1.0f, a.hp.beta2);
-        s_sc.eps = a.hp.eps;
-        // mode: 0 nothing; 1 speculation kept (gathered parameters from shared memory);
-        // 2 update again from the shared-memory copies; 3 update from global memory;
-        // 4 undo the speculation (put master, m, v back)
-        uint32_t mode = 0;
-        const bool copy_failed = STAGED && staged_copy && !s_spec;  // error recorded: write nothing
-        if (STAGED && staged_copy && s_spec)
-            mode = !go ? 4 : s_sc.c == 1.0f ? 1 : 2;
-        else if (go && !copy_failed)
-            mode = 3;
-        s_flag = mode;
-        s_edges = go && !copy_failed;
-    }
-    __syncthreads();
-    const uint32_t mode = s_flag;
-    const bool edges = s_edges != 0;
+    // Staged, after the speculative update (already written with c = 1): with c = 1 only
+    // the edge elements remain; with another c the tile is updated again from the
+    // shared-memory copies; if the step does not apply here, master, m, v and the gathered
+    // parameters are put back from them.  Otherwise the update reads master, m, v from global memory.
+    // Every thread derives the same mode from the shared flags:
+    // 0 nothing; 1 speculation kept (only the tile's edges remain); 2 update again from the
+    // shared-memory copies; 3 update from global memory; 4 undo the speculation (put
+    // master, m, v and the gathered parameters back)
+    const bool go = s_flag == 1 && !(__float_as_uint(s_applied) >> 31) && lo < hi;
+    const bool copy_failed = STAGED && staged_copy && !s_spec;  // error recorded: write nothing
+    uint32_t mode = 0;
+    if (STAGED && staged_copy && s_spec)
+        mode = !go ? 4 : s_applied == 1.0f ? 1 : 2;
+    else if (go && !copy_failed)
+        mode = 3;
+    const bool edges = go && !copy_failed;
     {
         const Scalars& sc = s_sc;
         // [v_lo, v_end): whole 4-element groups below psi; [v_end, v_hi): the group holding
@@ -520,12 +633,9 @@ k_step_fused(const __grid_constant__ FusedArgs a)
                         update_one(a, i + e, gc[i + e - base], sc, lo, hi);
             }
         }
-        if (mode == 1) {
+        // mode 1: the speculation wrote the tile's vector part already
+        if (mode == 4) {
             const uint16_t* const so = reinterpret_cast<const uint16_t*>(sv + kGcFloats);
-            for (uint64_t i = v_lo + 4ull * threadIdx.x; i < v_end; i += 4ull * S::kThreads)
-                if (ZERO_OWNED(i, 4, lo, hi, &st->error))
-                    __stcs(reinterpret_cast<uint2*>(a.out + i), *reinterpret_cast<const uint2*>(so + (i - base)));
-        } else if (mode == 4) {
             for (uint64_t i = v_lo + 4ull * threadIdx.x; i < v_end; i += 4ull * S::kThreads) {
                 const uint64_t k = i - base;
                 if (!ZERO_OWNED(i, 4, lo, hi, &st->error))
@@ -533,6 +643,7 @@ k_step_fused(const __grid_constant__ FusedArgs a)
                 __stcs(reinterpret_cast<float4*>(a.master + i), *reinterpret_cast<const float4*>(sp + k));
                 __stcs(reinterpret_cast<float4*>(a.m + i), *reinterpret_cast<const float4*>(sm + k));
                 __stcs(reinterpret_cast<float4*>(a.v + i), *reinterpret_cast<const float4*>(sv + k));
+                __stcs(reinterpret_cast<uint2*>(a.out + i), *reinterpret_cast<const uint2*>(so + k));
             }
         } else if (mode == 2 || mode == 3) {
             // Q 4-element groups per thread at a time: all their loads before any store

@@ -47,6 +47,12 @@ __device__ __forceinline__ float bias_rbc2(const zero_adamw_hparams_t& hp, uint3
     return (float)sqrt(1.0 - pow_uint((double)hp.beta2, t));
 }
 
+/* The decoupled weight decay factor 1 - lr*wd, in fp64, rounded to fp32 once. */
+__device__ __forceinline__ float decoupled_decay(const zero_adamw_hparams_t& hp)
+{
+    return (float)(1.0 - (double)hp.lr * (double)hp.weight_decay);
+}
+
 /* The scaler's outcome for either value of the step's overflow flag, computed from the
  * state before the step (it needs no norm, so it can be formed ahead of time):
  *   overflow:  the dynamic scale halves (floor 1), the good-step count restarts;
@@ -83,7 +89,7 @@ __device__ __forceinline__ ScalerCand scaler_candidates(const zero_step_state_t&
     }
     c.inv_skip = (float)(1.0 / ((double)n_ranks * (double)c.L_skip));
     c.inv_ok = (float)(1.0 / ((double)n_ranks * (double)c.L_ok));
-    c.decay = (float)(1.0 - (double)hp.lr * (double)hp.weight_decay);
+    c.decay = decoupled_decay(hp);
     return c;
 }
 

@@ -5,6 +5,7 @@
 
 #include <cuda_runtime.h>
 #include <nvtx3/nvToolsExt.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "../../include/zero.h"
@@ -49,6 +50,13 @@ struct AdamwArgs {
     const uint16_t* rep1;
     uint32_t grad_f16;                       // copies are fp16 (else bf16)
 };
+
+static_assert(sizeof(zero_step_state_t) == 128, "the step state is 128 bytes");
+// the single launch's arrival counter and the step's outcome form one 64-bit word
+// (counter in the low half), written at once when the last block releases the others
+static_assert(offsetof(zero_step_state_t, launch_arrivals) % 8 == 0 &&
+                  offsetof(zero_step_state_t, applied_c) == offsetof(zero_step_state_t, launch_arrivals) + 4,
+              "launch_arrivals and applied_c share one aligned 64-bit word");
 
 /* Kernel arguments of the single-launch step for small layouts (fused.cu). */
 struct FusedArgs {
