@@ -132,12 +132,12 @@ __device__ __forceinline__ bool clip_certainly_one(float u, float max_norm)
     return max_norm >= need;
 }
 
-/* L2 prefetch of [p, p + n) floats, rounded inwards to 16-byte boundaries (a hint: the
- * data is read with ordinary loads later). */
-__device__ __forceinline__ void prefetch_l2(const float* p, uint64_t n)
+/* L2 prefetch of the bytes [p, p + n), rounded inwards to 16-byte boundaries (a hint:
+ * the data is read with ordinary loads later). */
+__device__ __forceinline__ void prefetch_l2(const void* p, uint64_t n)
 {
     const uintptr_t a0 = ((uintptr_t)p + 15u) & ~(uintptr_t)15u;
-    const uintptr_t a1 = ((uintptr_t)(p + n)) & ~(uintptr_t)15u;
+    const uintptr_t a1 = ((uintptr_t)p + n) & ~(uintptr_t)15u;
     if (a1 > a0)
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
                      ::"l"(a0), "r"((uint32_t)(a1 - a0)) : "memory");
@@ -242,9 +242,9 @@ k_step_fused(const __grid_constant__ FusedArgs a)
         if (lane == 3)
             s_decay = decoupled_decay(a.hp);
         if (!STAGED && lane == 2 && lo < hi) {
-            prefetch_l2(a.master + lo, hi - lo);
-            prefetch_l2(a.m + lo, hi - lo);
-            prefetch_l2(a.v + lo, hi - lo);
+            prefetch_l2(a.master + lo, (hi - lo) * sizeof(float));
+            prefetch_l2(a.m + lo, (hi - lo) * sizeof(float));
+            prefetch_l2(a.v + lo, (hi - lo) * sizeof(float));
         }
         __syncwarp();
         asm volatile("bar.arrive 5, %0;" ::"n"(S::kScalarsReady) : "memory");
@@ -459,7 +459,8 @@ k_step_fused(const __grid_constant__ FusedArgs a)
                 for (uint32_t rr = 0; rr < N; ++rr)
                     total += rank_sum[rr];
                 const double norm = sqrt(total);
-                const float c = clip_coefficient(norm, overflow, a.hp.max_grad_norm);
+                // released already: a skipped step or a certain c = 1 (no fp64 division)
+                const float c = released ? 1.0f : clip_coefficient(norm, overflow, a.hp.max_grad_norm);
                 const float applied = overflow ? -1.0f : c;
                 if (!released)
                     release(applied);
