@@ -68,7 +68,7 @@ __device__ unsigned long long zero_test_absent_block = ~0ull;
 constexpr int kFusedWarps = 8;                       // stream the gradients (phase 1)
 constexpr int kFusedThreads = kFusedWarps * 32;      // the reduce pass's block size
 constexpr int kFusedLoads = 8;                       // replica loads in flight per thread (N <= 8)
-constexpr int kFusedLoadsWide = 16;                  // the generic kernel (N = 16, 64, ...)
+constexpr int kFusedLoadsWide = 16;                  // N > 8: the N = 16 and the generic kernel
 constexpr uint64_t kT = ZERO_TILE_ELEMS;
 constexpr int kGcFloats = (int)kT + 8;               // the tile's g from its first whole group
 
@@ -766,6 +766,7 @@ int capacity_dt(uint32_t n)
     case 2: return FusedKernel<DT, 2, STAGED>::capacity();
     case 4: return FusedKernel<DT, 4, STAGED>::capacity();
     case 8: return FusedKernel<DT, 8, STAGED>::capacity();
+    case 16: return FusedKernel<DT, 16, STAGED>::capacity();
     default: return FusedKernel<DT, 0, STAGED>::capacity();
     }
 }
@@ -777,6 +778,7 @@ cudaError_t launch_dt(const FusedArgs& a, unsigned grid, cudaStream_t s)
     case 2: return FusedKernel<DT, 2, STAGED>::launch(a, grid, s);
     case 4: return FusedKernel<DT, 4, STAGED>::launch(a, grid, s);
     case 8: return FusedKernel<DT, 8, STAGED>::launch(a, grid, s);
+    case 16: return FusedKernel<DT, 16, STAGED>::launch(a, grid, s);
     default: return FusedKernel<DT, 0, STAGED>::launch(a, grid, s);
     }
 }

@@ -23,10 +23,12 @@
  *  - every thread moves 8 elements per replica with one 128-bit non-coherent load that
  *    skips L1 (ld.global.nc.L1::no_allocate.v4), all N replica loads issued before the
  *    sum, and writes g with streaming 128-bit stores;
- *  - the sum of squares is carried per thread as an unevaluated fp32 pair with error-free
- *    TwoProduct (FMA) and TwoSum steps, which keeps it at ~2^-48 relative accuracy without
- *    per-element fp64 (GB300's fp64 rate is a small fraction of fp32), then folded into
- *    fp64 once per thread and reduced in a fixed shuffle tree per tile;
+ *  - the sum of squares is carried per thread as two unevaluated fp32 pairs (even and odd
+ *    elements) with error-free TwoProduct (FMA) and TwoSum steps, which keeps it at
+ *    ~2^-48 relative accuracy without per-element fp64 (GB300's fp64 rate is a small
+ *    fraction of fp32), then folded into fp64 once per warp and reduced in a fixed tree
+ *    per tile; the rank sums, the unscale and both pairs' steps use Blackwell's paired
+ *    fp32 instructions (two operations of one thread in one instruction, same bits);
  *  - groups with an element outside the pair arithmetic's exact range (below 2^-74 or
  *    at least 2^34 in magnitude, or not finite) are summed in fp64 instead;
  *  - launched with programmatic dependent launch (the kernel waits for the preceding grid
@@ -41,6 +43,11 @@ namespace {
 
 constexpr int kBlock = 256;
 constexpr int kLoadBatch = 8;  // replica loads in flight per thread before summing
+// with 8 copies the kernel is compiled for 5 resident blocks of 256 threads per SM (48
+// registers; left to itself the compiler takes 56, which allows only 4); the other rank
+// counts are left to the compiler (46-48 registers, 5 blocks; 74 and 3 for the generic
+// kernel), where a bound made it spill
+constexpr int kMinBlocksN8 = 5;
 
 /* The tile j of rank r, clipped to the window: [lo, hi), empty for a rank's trailing
  * slot.  Shards are cut at the flat multiples of the tile size, so the 128-bit loads of
@@ -139,7 +146,7 @@ __device__ __forceinline__ void tile_done(const ReduceArgs& a, uint64_t unit, co
 
 /* The reduce: a persistent grid over the window's tiles, one block per tile at a time. */
 template <zero_dtype_t DT, int NR>
-__global__ void __launch_bounds__(kBlock) k_reduce(const __grid_constant__ ReduceArgs a)
+__global__ void __launch_bounds__(kBlock, NR == 8 ? kMinBlocksN8 : 0 /* unbounded */) k_reduce(const __grid_constant__ ReduceArgs a)
 {
     grid_dependency_wait();
     const float inv = a.st->inv_scale;

@@ -57,17 +57,48 @@ __device__ __forceinline__ uint16_t ld_stream_u16(const void* p)
     return v;
 }
 
+/* Two fp32 values in one 64-bit register, and Blackwell's paired fp32 arithmetic on them
+ * (add/sub/mul .rn.f32x2): each half is the correctly rounded result of the scalar
+ * operation, so a pair of scalar computations done this way keeps its bits, in half the
+ * instructions. */
+__device__ __forceinline__ uint64_t f2(float a, float b)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t r, float& a, float& b)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+/* s[e] += x[e] for the 8 values of one 128-bit load of a copy, in fp32 pairs. */
 template <zero_dtype_t DT>
 __device__ __forceinline__ void add8(float (&s)[8], const uint4& v)
 {
-    s[0] = __fadd_rn(s[0], lo16<DT>(v.x));
-    s[1] = __fadd_rn(s[1], hi16<DT>(v.x));
-    s[2] = __fadd_rn(s[2], lo16<DT>(v.y));
-    s[3] = __fadd_rn(s[3], hi16<DT>(v.y));
-    s[4] = __fadd_rn(s[4], lo16<DT>(v.z));
-    s[5] = __fadd_rn(s[5], hi16<DT>(v.z));
-    s[6] = __fadd_rn(s[6], lo16<DT>(v.w));
-    s[7] = __fadd_rn(s[7], hi16<DT>(v.w));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        f2_split(f2_add(f2(s[2 * q], s[2 * q + 1]), f2(lo16<DT>(w[q]), hi16<DT>(w[q]))),
+                 s[2 * q], s[2 * q + 1]);
 }
 
 /* Sum of squares of the fp32 gradient, carried as an unevaluated pair hi + lo of fp32
@@ -80,19 +111,30 @@ __device__ __forceinline__ void add8(float (&s)[8], const uint4& v)
  * Groups holding anything outside that range take the fp64 path below. */
 constexpr float kSqScale = 16777216.0f;  // 2^24
 constexpr double kSqUnscale = 0x1p-48;
+/* Two such pairs per thread, one for the even and one for the odd elements of its groups,
+ * each updated with the scalar steps, side by side in fp32x2 arithmetic (hi2, lo2 hold
+ * the even pair's parts in their low halves, the odd pair's in their high halves);
+ * tile_fold adds the two pairs first. */
 struct SumSq {
-    float hi = 0.0f, lo = 0.0f;
+    uint64_t hi2 = 0, lo2 = 0;  // +0.0f in both halves
     double wide = 0.0;
 
-    __device__ __forceinline__ void add_fast(float x)
+    /* x2: two scaled values, (even, odd).  The products' rounding errors x*x - p are
+     * formed with scalar FMAs (as many instructions as the paired negation and FMA): a
+     * paired FMA whose addend was a paired 0 - p gave wrong errors on GB300 in this
+     * kernel, while every paired operation here matched its scalar twin on its own. */
+    __device__ __forceinline__ void add_pair(uint64_t x2)
     {
-        const float p = __fmul_rn(x, x);
-        const float pe = __fmaf_rn(x, x, -p);
-        const float s = __fadd_rn(hi, p);
-        const float bb = __fsub_rn(s, hi);
-        const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(p, bb));
-        hi = s;
-        lo = __fadd_rn(lo, __fadd_rn(err, pe));
+        const uint64_t p = f2_mul(x2, x2);
+        float x0, x1, p0, p1;
+        f2_split(x2, x0, x1);
+        f2_split(p, p0, p1);
+        const uint64_t pe = f2(__fmaf_rn(x0, x0, -p0), __fmaf_rn(x1, x1, -p1));  // exact
+        const uint64_t s = f2_add(hi2, p);
+        const uint64_t bb = f2_sub(s, hi2);
+        const uint64_t err = f2_add(f2_sub(hi2, f2_sub(s, bb)), f2_sub(p, bb));
+        hi2 = s;
+        lo2 = f2_add(lo2, f2_add(err, pe));
     }
 };
 
@@ -149,9 +191,13 @@ __device__ __forceinline__ void group_values(uint64_t psi, float inv, const floa
 {
     full = b >= lo && b + 8 <= hi;
     float sq[8];
+    const uint64_t inv2 = f2(inv, inv);
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
-        gv[e] = sq[e] = __fmul_rn(s[e], inv);
+    for (int q = 0; q < 4; ++q) {
+        f2_split(f2_mul(f2(s[2 * q], s[2 * q + 1]), inv2), gv[2 * q], gv[2 * q + 1]);
+        sq[2 * q] = gv[2 * q];
+        sq[2 * q + 1] = gv[2 * q + 1];
+    }
     in = 0xffu;
     if (b + 8 > psi || !full) {  // padding, or a group cut by the tile/window edge
 #pragma unroll
@@ -165,9 +211,10 @@ __device__ __forceinline__ void group_values(uint64_t psi, float inv, const floa
         }
     }
     if (squares_in_range(sq)) {  // every counted element finite: no overflow
+        const uint64_t scale2 = f2(kSqScale, kSqScale);
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            acc.add_fast(__fmul_rn(sq[e], kSqScale));
+        for (int q = 0; q < 4; ++q)
+            acc.add_pair(f2_mul(f2(sq[2 * q], sq[2 * q + 1]), scale2));
     } else {
 #pragma unroll
         for (int e = 0; e < 8; ++e)
@@ -189,7 +236,10 @@ __device__ __forceinline__ double tile_fold(const SumSq& acc, double (*warp_part
                                             uint32_t& parity)
 {
     static_assert(kThreads / 32 <= 32 && (kThreads / 32 & (kThreads / 32 - 1)) == 0, "warp tree");
-    float ph = acc.hi, pl = acc.lo;
+    float ph, pl, h1, l1;
+    f2_split(acc.hi2, ph, h1);
+    f2_split(acc.lo2, pl, l1);
+    pair_add(ph, pl, h1, l1);  // the even elements' pair + the odd elements' pair
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float h2 = __shfl_xor_sync(0xffffffffu, ph, o);
