@@ -174,6 +174,11 @@ class OracleRun:
 # gathered parameters); exact zeros use an absolute floor of 1e-30.
 REL = 1e-5
 FLOOR = 1e-30
+# the norm's own bound, far inside the stated one: the GPU sum of squares is error-free in
+# fp32 pairs and fp64 per warp (~2^-48 relative), and the oracle's sequential fp64 sum
+# differs from the exact one by ~1e-12 relative even at 1.5e9 terms; a systematic error of
+# the GPU's sum (a lost or doubled error term: ~1e-8) fails here while still passing 1e-5
+NORM_REL = 1e-9
 
 
 def assert_state_close(got: dict, want: dict, psi: int, exact_expected: bool = True) -> dict:
@@ -207,7 +212,7 @@ def bf16_ordinal(bits: np.ndarray) -> np.ndarray:
     return np.where(b & 0x8000, -(b & 0x7FFF), b)
 
 
-def assert_scalars(s: z.StepState, rep, rel_norm: float = REL) -> None:
+def assert_scalars(s: z.StepState, rep, rel_norm: float = NORM_REL) -> None:
     assert s.overflow == 0
     assert s.skip == rep.skipped and s.t == rep.t
     assert s.loss_scale == rep.loss_scale_next
