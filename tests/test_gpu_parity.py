@@ -152,12 +152,14 @@ def _bf16_bits(x: np.ndarray) -> np.ndarray:
     return (u >> 16).astype(np.uint16)
 
 
-@pytest.mark.parametrize("case", ["huge", "tiny", "mixed"])
+@pytest.mark.parametrize("case", ["huge", "tiny", "mixed", "edge32"])
 def test_sum_of_squares_at_the_range_edges(case):
     """Finite gradients far from 1: the per-tile sum of squares must not overflow or lose
     small terms.  'huge': three tiles of 2^60 (each tile's squares sum to 2^133, past the
     fp32 range; exact in fp64); 'tiny': magnitudes 2^-60 .. 2^-90 on both sides of the
-    pair arithmetic's exact range; 'mixed': both kinds in one tile."""
+    pair arithmetic's exact range; 'mixed': both kinds in one tile; 'edge32': a full tile
+    just below the pair arithmetic's upper bound 2^32 (8192 squares summed in fp32 pairs
+    reach 2^125 after the 2^24 scaling) and one at 2^33, just above it (fp64 path)."""
     psi, n = 5 * 8192 + 77, 4
     wl = W.scaled(W.C2, psi, steps=1)
     gpu = GpuRun(replace(wl, n_ranks=n))
@@ -167,6 +169,9 @@ def test_sum_of_squares_at_the_range_edges(case):
     vals = np.zeros((n, P), np.float32)
     if case in ("huge", "mixed"):
         vals[:, 1000:1000 + 3 * 8192] = np.float32(2.0 ** 60)
+    if case == "edge32":
+        vals[:, 8192:2 * 8192] = np.float32(1.9921875 * 2.0 ** 31)  # bf16-exact, < 2^32
+        vals[:, 3 * 8192:4 * 8192] = np.float32(2.0 ** 33)
     if case in ("tiny", "mixed"):
         e = rng.integers(-90, -59, size=(n, psi))
         sgn = rng.choice([-1.0, 1.0], size=(n, psi))

@@ -176,7 +176,7 @@ k_step_fused(const __grid_constant__ FusedArgs a)
     using S = Shape<STAGED>;
     extern __shared__ __align__(16) float dyn[];  // g of the tile; staged: then master, m, v
     float* const gc = dyn;                        // gc[i - base] holds g[i]
-    __shared__ double warp_part[2][kFusedWarps];
+    __shared__ WarpPart warp_part[2][kFusedWarps];
     __shared__ double rank_sum[ZERO_MAX_KERNEL_RANKS];
     __shared__ float rank_up[kFusedWarps];  // an upward-rounded fp32 bound of each rank's sum
     __shared__ float s_step, s_rbc2, s_decay;

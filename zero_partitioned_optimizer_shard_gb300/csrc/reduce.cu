@@ -30,7 +30,7 @@
  *    per tile; the rank sums, the unscale and both pairs' steps use Blackwell's paired
  *    fp32 instructions (two operations of one thread in one instruction, same bits);
  *  - groups with an element outside the pair arithmetic's exact range (below 2^-74 or
- *    at least 2^34 in magnitude, or not finite) are summed in fp64 instead;
+ *    at least 2^32 in magnitude, or not finite) are summed in fp64 instead;
  *  - launched with programmatic dependent launch (the kernel waits for the preceding grid
  *    first thing), so its launch overlaps the previous kernel's tail.
  */
@@ -137,7 +137,7 @@ __device__ __forceinline__ void tile_ldg(const ReduceArgs& a, float inv, uint64_
  * launch, and the windows of a step meet a tile in stream order, so the sum's order, and
  * its bits, are fixed. */
 __device__ __forceinline__ void tile_done(const ReduceArgs& a, uint64_t unit, const SumSq& acc,
-                                          double (*warp_part)[kBlock / 32], uint32_t& parity)
+                                          WarpPart (*warp_part)[kBlock / 32], uint32_t& parity)
 {
     const double t = tile_fold<kBlock>(acc, warp_part, parity);
     if (threadIdx.x == 0)
@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kBlock, NR == 8 ? kMinBlocksN8 : 0 /* unbounde
 {
     grid_dependency_wait();
     const float inv = a.st->inv_scale;
-    __shared__ double warp_part[2][kBlock / 32];
+    __shared__ WarpPart warp_part[2][kBlock / 32];
     uint32_t parity = 0;
     bool bad = false;
     for (uint64_t u = blockIdx.x; u < a.unit_count; u += gridDim.x) {

@@ -104,8 +104,8 @@ __device__ __forceinline__ void add8(float (&s)[8], const uint4& v)
 /* Sum of squares of the fp32 gradient, carried as an unevaluated pair hi + lo of fp32
  * values.  TwoProduct: x*x = p + pe exactly (FMA); TwoSum: hi + p = s + err exactly.
  * The values are scaled by 2^24 first (exact) and the tile's total by 2^-48 at the end,
- * which moves the range where every step is exact and nothing can overflow (1024 squares
- * per warp before the fp64 fold) to |x| in [2^-74, 2^34), plus zeros: gradients of
+ * which moves the range where every step is exact and nothing can overflow (8192 squares
+ * per tile before the fp64 conversion) to |x| in [2^-74, 2^32), plus zeros: gradients of
  * ~1e-4 often come within 2^-50 of zero, which unscaled would need the fp64 path.
  * Power-of-two scaling changes no rounding, so the result is the unscaled pair sum's.
  * Groups holding anything outside that range take the fp64 path below. */
@@ -139,7 +139,7 @@ struct SumSq {
 };
 
 /* True when all 8 values are finite and every scaled square is exact in the fp32 pair
- * arithmetic: magnitudes in [2^-74, 2^34) or zero.  Integer compares on the magnitude
+ * arithmetic: magnitudes in [2^-74, 2^32) or zero.  Integer compares on the magnitude
  * bits, so NaN (above inf) and inf fail the test too. */
 __device__ __forceinline__ bool squares_in_range(const float (&x)[8])
 {
@@ -150,7 +150,7 @@ __device__ __forceinline__ bool squares_in_range(const float (&x)[8])
         mx = max(mx, u);
         mn = min(mn, u == 0u ? 0x3f800000u : u);
     }
-    return mx < 0x50800000u && mn >= 0x1a800000u;  // 2^34 and 2^-74
+    return mx < 0x4f800000u && mn >= 0x1a800000u;  // 2^32 and 2^-74
 }
 
 /* fp64 sum of squares of the elements of a group selected by mask; a real call, so the
@@ -223,19 +223,28 @@ __device__ __forceinline__ void group_values(uint64_t psi, float inv, const floa
     }
 }
 
+/* One warp's share of a tile's sum of squares: its fp32 pair and its rare fp64 part. */
+struct WarpPart {
+    float h, l;
+    double wide;
+};
+
 /* A tile's sum of squares from every thread's accumulator: a fixed-order pair-arithmetic
- * shuffle tree in fp32, fp64 once per warp, then the kThreads / 32 warp values pairwise,
- * ((w0 + w4) + (w2 + w6)) + ((w1 + w5) + (w3 + w7)) for 8 warps: three dependent fp64
- * additions instead of eight, which matters on GB300's slow fp64 pipe.  The per-warp
- * values alternate between two buffers (`parity`), so a following tile cannot overwrite
- * them before thread 0 has read them.  Called by the block's
- * first kThreads threads only, which meet at named barrier 1 (other warps of a larger block
- * go on unhindered).  The result is valid in thread 0 only. */
+ * shuffle tree in fp32 per warp, then the kThreads / 32 warp pairs pairwise in the same
+ * arithmetic, ((w0 + w4) + (w2 + w6)) + ((w1 + w5) + (w3 + w7)) for 8 warps, and fp64
+ * once per tile: GB300's fp64 pipe is a small fraction of its fp32 rate, and at N = 2 a
+ * conversion per warp kept it a third busy.  The fp64 parts of the rare out-of-range
+ * groups (zero almost always, tested with integer compares) are added in the same tree
+ * shape.  The warp values alternate between two buffers (`parity`), so a following tile
+ * cannot overwrite them before thread 0 has read them.  Called by the block's first
+ * kThreads threads only, which meet at named barrier 1 (other warps of a larger block go
+ * on unhindered).  The result is valid in thread 0 only. */
 template <int kThreads>
-__device__ __forceinline__ double tile_fold(const SumSq& acc, double (*warp_part)[kThreads / 32],
+__device__ __forceinline__ double tile_fold(const SumSq& acc, WarpPart (*warp_part)[kThreads / 32],
                                             uint32_t& parity)
 {
-    static_assert(kThreads / 32 <= 32 && (kThreads / 32 & (kThreads / 32 - 1)) == 0, "warp tree");
+    constexpr int W = kThreads / 32;
+    static_assert(W <= 32 && (W & (W - 1)) == 0, "warp tree");
     float ph, pl, h1, l1;
     f2_split(acc.hi2, ph, h1);
     f2_split(acc.lo2, pl, l1);
@@ -246,30 +255,46 @@ __device__ __forceinline__ double tile_fold(const SumSq& acc, double (*warp_part
         const float l2 = __shfl_xor_sync(0xffffffffu, pl, o);
         pair_add(ph, pl, h2, l2);
     }
-    double wide = acc.wide;
-    if (__any_sync(0xffffffffu, wide != 0.0)) {
+    double wide = acc.wide;  // >= 0: any set bit means nonzero
+    if (__any_sync(0xffffffffu, __double_as_longlong(wide) != 0)) {
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
             wide += __shfl_xor_sync(0xffffffffu, wide, o);
     }
-    double* wp = warp_part[parity];
+    WarpPart* wp = warp_part[parity];
     const int lane = threadIdx.x & 31;
     if (lane == 0)
-        wp[threadIdx.x >> 5] = ((double)ph + (double)pl) * kSqUnscale + wide;
+        wp[threadIdx.x >> 5] = WarpPart{ph, pl, wide};
     asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
     double t = 0.0;
     if (threadIdx.x == 0) {
-        // pairwise: independent additions, three levels deep for 8 warps
-        double x[kThreads / 32];
+        float h[W], l[W];
+        long long any_wide = 0;
 #pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w)
-            x[w] = wp[w];
+        for (int w = 0; w < W; ++w) {
+            h[w] = wp[w].h;
+            l[w] = wp[w].l;
+            any_wide |= __double_as_longlong(wp[w].wide);
+        }
+        // pairwise: independent pair additions, three levels deep for 8 warps
 #pragma unroll
-        for (int h = kThreads / 64; h > 0; h >>= 1)
+        for (int hh = W / 2; hh > 0; hh >>= 1)
 #pragma unroll
-            for (int w = 0; w < h; ++w)
-                x[w] = x[w] + x[w + h];
-        t = x[0];
+            for (int w = 0; w < hh; ++w)
+                pair_add(h[w], l[w], h[w + hh], l[w + hh]);
+        t = ((double)h[0] + (double)l[0]) * kSqUnscale;
+        if (any_wide != 0) {
+            double x[W];
+#pragma unroll
+            for (int w = 0; w < W; ++w)
+                x[w] = wp[w].wide;
+#pragma unroll
+            for (int hh = W / 2; hh > 0; hh >>= 1)
+#pragma unroll
+                for (int w = 0; w < hh; ++w)
+                    x[w] = x[w] + x[w + hh];
+            t += x[0];
+        }
     }
     parity ^= 1u;
     return t;
