@@ -1,7 +1,10 @@
 /* A plain C program against include/zero.h and libzero_shard.so, using the entry points
  * that need no GPU: the partition/ledger, the workspace size, the per-tensor segment map
- * and the status texts.  Built and run by tests/test_c_abi.py; prints one line per check
- * and exits non-zero on the first failure. */
+ * and the status texts; and the step state's layout as the header defines it (one line
+ * per field, which the test compares with the Python binding's).  Built and run by
+ * tests/test_c_abi.py; prints one line per check and exits non-zero on the first
+ * failure. */
+#include <stddef.h>
 #include <stdint.h>
 #include <stdio.h>
 #include <string.h>
@@ -52,6 +55,14 @@ int main(void)
         return fail("empty model rejected");
     if (strlen(zero_strerror(ZERO_EINVAL)) == 0)
         return fail("strerror");
+#define FIELD(f) printf("state %s %zu\n", #f, offsetof(zero_step_state_t, f))
+    FIELD(sumsq); FIELD(norm); FIELD(clip_coef); FIELD(loss_scale); FIELD(inv_scale);
+    FIELD(step_size); FIELD(rbc2); FIELD(decay); FIELD(overflow); FIELD(skip); FIELD(t);
+    FIELD(good_steps); FIELD(growth_interval); FIELD(dynamic); FIELD(n_ranks); FIELD(n_steps);
+    FIELD(n_skipped); FIELD(error); FIELD(arrivals); FIELD(inv_scale_used);
+    FIELD(launch_arrivals); FIELD(applied_c); FIELD(reserved);
+#undef FIELD
+    printf("state_size %zu\n", sizeof(zero_step_state_t));
     printf("ok\n");
     return 0;
 }

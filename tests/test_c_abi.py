@@ -23,6 +23,18 @@ def test_c_program_links_and_runs(tmp_path):
     r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.strip().endswith("ok")
+    # the Python binding's step state has the header's layout, field by field
+    from zero_partitioned_optimizer_shard_gb300 import STATE_BYTES, StepState
+    fields = {}
+    for line in r.stdout.splitlines():
+        if line.startswith("state "):
+            _, name, off = line.split()
+            fields[name] = int(off)
+        elif line.startswith("state_size "):
+            assert int(line.split()[1]) == STATE_BYTES == 128
+    assert [n for n, _ in StepState._fields_] == list(fields)
+    for name, off in fields.items():
+        assert getattr(StepState, name).offset == off, name
 
 
 def _cuda_home():
