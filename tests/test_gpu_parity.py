@@ -424,11 +424,14 @@ def test_generator_twins_agree():
         assert np.array_equal(d.cpu().numpy().view(np.uint8), h.view(np.uint8))
 
 
-def test_zero_step_replays_from_a_cuda_graph():
+@pytest.mark.parametrize("psi,launches", [(200_003, 1), (8 * 8192 * 60 + 3, 3)])
+def test_zero_step_replays_from_a_cuda_graph(psi, launches):
     """zero_step enqueues kernels only (no host sync, no allocation), so a caller can
-    capture it in a CUDA graph; replaying the graph gives the same bits as direct calls."""
-    wl = W.scaled(W.C2, 200_003, steps=3)
+    capture it in a CUDA graph; replaying the graph gives the same bits as direct calls,
+    for the single cooperative launch and for the three launches of a larger layout."""
+    wl = W.scaled(W.C2, psi, steps=3)
     direct = GpuRun(wl)
+    assert z.zero_step_launches(direct.lay, z.ZERO_BF16) == launches
     graphed = GpuRun(wl, guarded=False)
     stream = torch.cuda.Stream()
     graphed.stream = stream
