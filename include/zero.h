@@ -135,9 +135,10 @@ typedef struct zero_step_state {
     uint32_t launch_arrivals; /* internal to zero_step's single launch: its blocks that
                                have finished their reduce (0 between steps; keep it 0
                                when writing a state) */
-    float applied_c;        /* the clip coefficient the last finalised step applied, or -1
-                               when it was skipped; the single launch hands it to its
-                               blocks together with launch_arrivals in one 64-bit store */
+    float applied_c;        /* the clip coefficient the last finalised step applied, -1
+                               when it was skipped, 0 before the first step; the single
+                               launch hands it to its blocks together with
+                               launch_arrivals in one 64-bit store */
     uint32_t reserved[8];
 } zero_step_state_t;        /* 128 bytes */
 
