@@ -104,6 +104,21 @@ def _reduce(lib, lay, dtype=z.ZERO_BF16, reps=None, begin=0, count=None, g=A, pa
     return lib.zero_reduce_shard_unscale(C.byref(lay), dtype, arr, begin, count, g, part, st, None)
 
 
+def test_step_launches_host_decisions(lib):
+    """zero_step_launches answers on the host, without touching a GPU, for every layout
+    the single launch cannot take: invalid inputs, several buckets, more than 128 tile
+    slots per rank."""
+    with pytest.raises(z.ZeroError) as e:
+        z.zero_step_launches(z.zero_partition(1000, 4), 3)
+    assert e.value.status == z.ZERO_EINVAL
+    with pytest.raises(z.ZeroError):
+        z.zero_step_launches(z.zero_partition(1000, 65), z.ZERO_BF16)  # > 64 ranks in kernels
+    llama = z.zero_partition(6_738_415_616, 8, 3, 1, 1 << 27)
+    assert z.zero_step_launches(llama, z.ZERO_BF16) == llama.n_buckets + 2 == 53
+    gpt2 = z.zero_partition(1_557_611_200, 8, 2)
+    assert gpt2.tiles_per_rank > 128 and z.zero_step_launches(gpt2, z.ZERO_F16) == 3
+
+
 def test_reduce_rejections(lib):
     lay = z.zero_partition(1000, 4)
     assert _reduce(lib, lay, dtype=3) == z.ZERO_EINVAL
