@@ -62,6 +62,25 @@ def _chunk_job(args):
 
 
 def run(wl_name: str, procs: int) -> str:
+    """Compute the workload's rows and write its golden file."""
+    from synth import workloads as W
+    wl = W.by_name(wl_name)
+    lines = golden_rows(wl_name, procs)
+    path = golden_path(wl_name)
+    os.makedirs(os.path.dirname(path), exist_ok=True)
+    with open(path, "w", encoding="utf-8") as f:
+        f.write(f"# Oracle per-step results for workload {wl_name}: {wl.name}\n")
+        f.write("# Written by tests/golden/make_golden.py (CPU oracle + seeded generator only).\n")
+        f.write("# Sums of squares: fp64, ascending index within 2^23-element chunks, chunks in "
+                "ascending order per rank, ranks in order.\n")
+        f.write("# step loss_scale_used overflow skipped t_after sumsq(hex) norm(hex) "
+                "clip_coef(hex) loss_scale_next\n")
+        f.write("\n".join(lines) + "\n")
+    return path
+
+
+def golden_rows(wl_name: str, procs: int) -> list:
+    """The workload's golden rows, one text line per step (nothing written)."""
     import oracle
     from synth import workloads as W
     wl = W.by_name(wl_name)
@@ -96,17 +115,7 @@ def run(wl_name: str, procs: int) -> str:
                          f"{norm.hex()} {float(np.float32(c)).hex()} {sc.loss_scale!r}")
             print(f"[{wl_name}] step {step}: L={L} ov={overflow} norm={norm:.9g} c={c:.9g} "
                   f"t={sc.t} ({time.time() - t0:.0f}s)", flush=True)
-    path = golden_path(wl_name)
-    os.makedirs(os.path.dirname(path), exist_ok=True)
-    with open(path, "w", encoding="utf-8") as f:
-        f.write(f"# Oracle per-step results for workload {wl_name}: {wl.name}\n")
-        f.write("# Written by tests/golden/make_golden.py (CPU oracle + seeded generator only).\n")
-        f.write("# Sums of squares: fp64, ascending index within 2^23-element chunks, chunks in "
-                "ascending order per rank, ranks in order.\n")
-        f.write("# step loss_scale_used overflow skipped t_after sumsq(hex) norm(hex) "
-                "clip_coef(hex) loss_scale_next\n")
-        f.write("\n".join(lines) + "\n")
-    return path
+    return lines
 
 
 def golden_path(wl_name: str) -> str:
