@@ -297,6 +297,60 @@ int zero_adamw_cast_gather_host_state(const zero_layout_t* layout,
                                       const zero_step_state_t* st, zero_stream_t stream);
 
 /* -------------------------------------------------------------------------------------
+ * Rank-local entry points: the step with the ranks spread over processes (one process per
+ * GPU), each process holding only its own ranks' part of g and of the optimizer state.
+ * [ZW] sec. 6(2) and [ZO] stage-2 flow: each rank receives every rank's gradient for its
+ * own partition (reduce-scatter), updates only its partition, and the updated parameters
+ * are all-gathered; [MD] sec. 1: the global norm needs one all-reduce before clipping.
+ *
+ * A process holds the contiguous ranks [rank_begin, rank_begin + rank_count) (one rank per
+ * process, or several); their flat range starts at origin = rank_begin*S and is
+ * local_len = rank_count*S long.  Local buffers are indexed by flat index - origin.
+ * origin must be a multiple of 8 (partition with align = 8; ZERO_EALIGN otherwise).
+ * One step, per process, with the exchanges done by the caller (e.g. NCCL):
+ *   1. exchange: for each local range, every rank's gradient copy of it arrives (an
+ *      all-to-all of equal chunks: rank k's copy of flat [origin, origin + local_len));
+ *   2. zero_reduce_shard_unscale_local over the local range (one or more windows);
+ *   3. exchange: all-gather every process's partial slots [rank_begin*tiles_per_rank,
+ *      (rank_begin + rank_count)*tiles_per_rank) into the full partials array, and
+ *      combine the step state's `overflow` word over processes (maximum);
+ *   4. zero_grad_norm on the full partials (every process forms the same norm, clip
+ *      coefficient, scaler update and skip decision, bit for bit);
+ *   5. zero_adamw_cast_gather_local on the local range;
+ *   6. exchange: all-gather the local parameters into the full gathered buffer.
+ * With the ranks' sums taken in ascending rank order in step 2 and the fixed-order sum of
+ * step 4, every output equals the one-GPU step's (zero_step) bit for bit.
+ * ------------------------------------------------------------------------------------- */
+
+/* zero_reduce_shard_unscale on a window inside the local range, g stored locally.
+ *   replicas   HOST array of N DEVICE pointers; replicas[k] points at flat element `begin`
+ *              of rank k's gradient copy (e.g. inside the chunk received from rank k)
+ *   begin      multiple of 8; [begin, begin + count) inside [origin, origin + local_len)
+ *   g_local    DEVICE fp32, local_len elements: g of flat i is stored at g_local[i - origin]
+ *   partials   DEVICE, zero_workspace_bytes(layout) (all ranks' slots); the local ranks'
+ *              slots are accumulated as in zero_reduce_shard_unscale
+ *   st         DEVICE step state of this process (its overflow word is set as there)
+ * ZERO_EINVAL for a bad rank range or a window outside it. */
+int zero_reduce_shard_unscale_local(const zero_layout_t* layout, zero_dtype_t dtype,
+                                    uint32_t rank_begin, uint32_t rank_count,
+                                    const void* const* replicas, uint64_t begin, uint64_t count,
+                                    float* g_local, double* partials, zero_step_state_t* st,
+                                    zero_stream_t stream);
+
+/* zero_adamw_cast_gather on the local range only: element j of every local array is flat
+ * origin + j; elements at flat >= psi are padding (parameters written 0, state untouched).
+ *   g_local, master_local, m_local, v_local   DEVICE fp32, local_len elements each
+ *   params_local   DEVICE 16-bit, local_len elements: this process's part of the gathered
+ *                  buffer (it may point at flat `origin` of the full buffer, so that an
+ *                  in-place all-gather completes it)
+ *   st             DEVICE step state after zero_grad_norm of this step */
+int zero_adamw_cast_gather_local(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,
+                                 uint32_t rank_begin, uint32_t rank_count, const float* g_local,
+                                 float* master_local, float* m_local, float* v_local,
+                                 uint16_t* params_local, const zero_step_state_t* st,
+                                 zero_stream_t stream);
+
+/* -------------------------------------------------------------------------------------
  * zero_step -- one whole step: every bucket's reduce, the norm, AdamW + cast.
  *   replicas   HOST array of n_buckets * N DEVICE pointers, bucket-major:
  *              replicas[b*N + k] holds rank k's gradient for flat
@@ -373,10 +427,15 @@ int zero_step_host(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,
  *   - Every call shares the one array and clears the slots it uses at its start, so two
  *     calls whose work overlaps on the GPU (different streams or threads) race: issue them
  *     one after another on one stream.
- *   - Arguments as in zero_step, without `partials`.  To initialise st with
- *     zero_step_state_init without allocating, pass any 16-byte-aligned device buffer of
- *     at least zero_workspace_bytes(layout) bytes as its `partials` argument, e.g. `g`
- *     whenever the shard size S is at least 2 (every step overwrites g before reading it).
+ *   - Arguments as in zero_step, without `partials`, except that g must not be NULL:
+ *     this call has no re-reading schedule (ZERO_EINVAL for NULL g).  To initialise st
+ *     with zero_step_state_init without allocating, pass any 16-byte-aligned device buffer
+ *     of at least zero_workspace_bytes(layout) bytes as its `partials` argument, e.g. `g`
+ *     whenever 4*psi_padded >= zero_workspace_bytes(layout), which holds for every shard
+ *     size S >= 4 (every step overwrites g before reading it).
+ *   - The address lookup is cached per device for the life of the process; after a
+ *     cudaDeviceReset the library's device code may be loaded at another address, so do
+ *     not call this entry point again in that process.
  * ------------------------------------------------------------------------------------- */
 #define ZERO_STATIC_WORKSPACE_SLOTS (1u << 20)
 int zero_step_static_workspace(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,

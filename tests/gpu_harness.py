@@ -25,7 +25,7 @@ def dtype_code(wl) -> int:
 
 class GpuRun:
     def __init__(self, wl, bucket_elems: int = 0, device: str = "cuda:0", guarded: bool = True,
-                 hp=None, host_state: bool = False, split: bool = False):
+                 hp=None, host_state: bool = False, split: bool = False, align: int = 1):
         """host_state: master/m/v in page-locked host memory (the offloaded optimizer
         state), updated by zero_adamw_cast_gather_host_state.  split: run each step as
         the separate calls (reduce per bucket, norm, AdamW) even where zero_step would
@@ -37,7 +37,7 @@ class GpuRun:
         self.stream = torch.cuda.current_stream(self.dev)
         self.guarded = guarded
         self._raw = []
-        self.lay = z.zero_partition(wl.psi, wl.n_ranks, wl.stage, 1, bucket_elems)
+        self.lay = z.zero_partition(wl.psi, wl.n_ranks, wl.stage, align, bucket_elems)
         P = self.lay.psi_padded
         self.hp = hp if hp is not None else z.hparams(**wl.hp.__dict__)
         self.reps = [self.alloc(P, torch.int16) for _ in range(wl.n_ranks)]
@@ -133,10 +133,10 @@ class GpuRun:
 
 
 class OracleRun:
-    def __init__(self, wl, hp=None):
+    def __init__(self, wl, hp=None, align: int = 1):
         self.wl = wl
         self.orc = oracle.load()
-        self.lay = self.orc.partition(wl.psi, wl.n_ranks, wl.stage)
+        self.lay = self.orc.partition(wl.psi, wl.n_ranks, wl.stage, align)
         P = self.lay.psi_padded
         self.hp = hp if hp is not None else oracle.hparams(**wl.hp.__dict__)
         f = lambda role, kind, sigma: synth.fill_host(synth.OUT_F32, kind, wl.state_key(role), 0, P,

@@ -199,3 +199,56 @@ def test_step_host_rejections(lib):
 def test_strerror(lib):
     for s in (0, -1, -2, -3, -4, -5, -99):
         assert isinstance(lib.zero_strerror(s), bytes) and lib.zero_strerror(s)
+
+
+def test_local_entry_point_rejections(lib):
+    """The rank-local calls check the rank range, the window and the origin's alignment
+    on the host."""
+    lay = z.zero_partition(1000, 4, 2, 8)          # S = 256: origins 0, 256, 512, 768
+    S = lay.shard
+    red = lib.zero_reduce_shard_unscale_local
+    red.argtypes = [C.POINTER(z.Layout), C.c_int, C.c_uint32, C.c_uint32, C.POINTER(C.c_void_p),
+                    C.c_uint64, C.c_uint64, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
+    red.restype = C.c_int
+    reps = (C.c_void_p * 4)(A, A, A, A)
+    r = lambda rb, rc, begin, count, g=A, lay=lay: red(C.byref(lay), z.ZERO_BF16, rb, rc, reps,
+                                                       begin, count, g, A, A, None)
+    assert r(1, 0, S, S) == z.ZERO_EINVAL          # no ranks
+    assert r(4, 1, 0, S) == z.ZERO_EINVAL          # rank past N
+    assert r(3, 2, 3 * S, S) == z.ZERO_EINVAL      # range past N
+    assert r(1, 1, 0, S) == z.ZERO_EINVAL          # window before the range
+    assert r(1, 1, S, S + 8) == z.ZERO_EINVAL      # window past the range
+    assert r(1, 1, S + 4, 8) == z.ZERO_EALIGN      # window start not a multiple of 8
+    assert r(1, 1, S, S, g=A + 4) == z.ZERO_EALIGN
+    odd = z.zero_partition(1000, 4)                # S = 250: rank 1 starts at flat 250
+    assert r(1, 1, 256, 8, lay=odd) == z.ZERO_EALIGN
+    ada = lib.zero_adamw_cast_gather_local
+    ada.argtypes = [C.POINTER(z.Layout), C.POINTER(z.HParams), C.c_uint32, C.c_uint32] + \
+        [C.c_void_p] * 7
+    ada.restype = C.c_int
+    hp = z.hparams()
+    assert ada(C.byref(lay), C.byref(hp), 2, 3, A, A, A, A, A, A, None) == z.ZERO_EINVAL
+    assert ada(C.byref(lay), C.byref(z.hparams(eps=0.0)), 0, 1, A, A, A, A, A, A, None) == z.ZERO_EINVAL
+    assert ada(C.byref(lay), C.byref(hp), 0, 1, A, A, 0, A, A, A, None) == z.ZERO_EINVAL
+    assert ada(C.byref(lay), C.byref(hp), 0, 1, A, A, A, A, A + 2, A, None) == z.ZERO_EALIGN
+    assert ada(C.byref(odd), C.byref(hp), 1, 1, A, A, A, A, A, A, None) == z.ZERO_EALIGN
+
+
+def test_static_workspace_host_contract(lib):
+    """zero_step_static_workspace has no re-reading schedule (g must be given), and g can
+    stand in as zero_step_state_init's partials exactly when 4*psi_padded bytes cover the
+    workspace: for every shard size S >= 4, never for S = 2 or 3."""
+    f = lib.zero_step_static_workspace
+    f.argtypes = [C.POINTER(z.Layout), C.POINTER(z.HParams), C.c_int, C.POINTER(C.c_void_p)] + \
+        [C.c_void_p] * 7
+    f.restype = C.c_int
+    lay = z.zero_partition(1000, 2)
+    reps = (C.c_void_p * 2)(A, A)
+    hp = z.hparams()
+    assert f(C.byref(lay), C.byref(hp), z.ZERO_BF16, reps, None, A, A, A, A, A, None) == z.ZERO_EINVAL
+    for n in (1, 2, 4, 8, 64):
+        for s_ in (1, 2, 3, 4, 5, 8, 8191, 8192, 8193, 100_000):
+            L = z.zero_partition(n * s_, n)
+            assert L.shard == s_
+            covers = 4 * L.psi_padded >= z.zero_workspace_bytes(L)
+            assert covers == (s_ >= 4), (n, s_)

@@ -461,11 +461,13 @@ def test_zero_step_replays_from_a_cuda_graph(psi, launches):
 
 def test_buckets_reduced_while_a_producer_writes_the_next():
     """Gradient buckets produced on one stream and reduced on another through a two-slot
-    ring of constant-size buffers give the same bits as one zero_step on all copies."""
+    ring of constant-size buffers give the same bits as one zero_step on all copies, and
+    the oracle's step within the stated tolerances, after every step."""
     wl = W.scaled(W.C3, 5 * 65536 + 1000, steps=2)
     Wb = 65536
     ref = GpuRun(wl, bucket_elems=Wb)
     pipe = GpuRun(wl, bucket_elems=Wb, guarded=False)
+    orc = OracleRun(wl)
     lay, N, P = pipe.lay, pipe.lay.n_ranks, pipe.lay.psi_padded
     comp = pipe.stream
     prod = torch.cuda.Stream()
@@ -492,6 +494,8 @@ def test_buckets_reduced_while_a_producer_writes_the_next():
         z.zero_grad_norm(lay, pipe.hp, pipe.partials, pipe.st, comp)
         z.zero_adamw_cast_gather(lay, pipe.hp, pipe.g, pipe.master, pipe.m, pipe.v, pipe.out, pipe.st,
                                  comp)
+        assert_scalars(pipe.state(), orc.step(step))
+        assert_state_close(pipe.arrays(), orc.arrays(), wl.psi, exact_expected=False)
     torch.cuda.synchronize()
     a, b = ref.arrays(), pipe.arrays()
     for k in a:

@@ -1,0 +1,157 @@
+"""The ZeRO step with its ranks spread over processes, on the GPU.
+
+Each process holds a contiguous group of the N ranks ("【论文解读】ZeRO" sec. 6(2): rank r
+keeps and updates only partition r) and runs its part of the step through the C ABI:
+zero_reduce_shard_unscale_local over its own flat range, zero_grad_norm after the
+all-gather of every process's tile partials and the maximum of the overflow word (the
+Megatron page, sec. 1: one all-reduce before clipping), zero_adamw_cast_gather_local, and
+the all-gather of the parameters.  The processes share this one GPU; their data plane is
+gloo through host memory (zero_partitioned_optimizer_shard_gb300.ranks.Exchange).  No
+kernel waits on another process: every exchange happens on the host between launches.
+
+Every process's g, master, m and v, the gathered parameters and the whole 128-byte step
+state must equal the one-GPU step on the same layout bit for bit after every step, and
+the oracle within the stated tolerances.  The schedule is the one
+tests/test_multirank_gloo.py runs with the oracle's arithmetic on CPU.
+"""
+import os
+import queue
+import socket
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+import synth
+from synth import workloads as W
+from tests.gpu_harness import GpuRun, OracleRun, assert_scalars, assert_state_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available()
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _proc_main(proc, world, port, wl, bucket, out_q):
+    import torch.distributed as dist
+
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=proc, world_size=world)
+    try:
+        import zero_partitioned_optimizer_shard_gb300 as z
+        from zero_partitioned_optimizer_shard_gb300.ranks import RankStep, layout_for
+
+        torch.cuda.set_device(0)
+        dev = torch.device("cuda", 0)
+        s = torch.cuda.current_stream(dev).cuda_stream
+        lay = layout_for(wl.psi, wl.n_ranks, wl.stage, bucket)
+        dt = z.ZERO_F16 if wl.grad_dtype == "f16" else z.ZERO_BF16
+        rs = RankStep(lay, z.hparams(**wl.hp.__dict__), dt, wl.loss_scale, wl.dynamic,
+                      wl.growth_interval, dev)
+        fills = [(rs.master, synth.ROLE_MASTER, synth.NORMAL, wl.master_sigma)]
+        if wl.random_moments:
+            fills += [(rs.m, synth.ROLE_MOM, synth.NORMAL, wl.mom_sigma),
+                      (rs.v, synth.ROLE_VAR, synth.NORMAL_SQ, wl.mom_sigma)]
+        for t_, role, kind, sig in fills:
+            synth.fill_dev(t_.data_ptr(), synth.OUT_F32, kind, wl.state_key(role), rs.origin,
+                           rs.local_len, wl.psi, sig, 1.0, s)
+        P = lay.psi_padded
+        copies = [torch.empty(P, dtype=torch.int16, device=dev) for _ in range(rs.rank_count)]
+        per_step = []
+        for step in range(1, wl.steps + 1):
+            L = z.zero_step_state_read(rs.st).loss_scale
+            for j, c in enumerate(copies):
+                synth.fill_dev(c.data_ptr(), wl.grad_out, wl.grad_kind,
+                               wl.grad_key(step, rs.rank_begin + j), 0, P, wl.psi, wl.grad_sigma,
+                               L, s)
+            inj = wl.injection(step)
+            if inj and rs.rank_begin <= inj[0] < rs.rank_begin + rs.rank_count:
+                copies[inj[0] - rs.rank_begin][inj[1]] = int(np.uint16(inj[2]).view(np.int16))
+            rs.step(copies)
+            torch.cuda.synchronize(dev)
+            per_step.append((rs.st.cpu().numpy().copy(), rs.params.cpu().numpy().view(np.uint16).copy()))
+        out_q.put((proc, rs.origin, rs.local_len, per_step, rs.g.cpu().numpy().copy(),
+                   rs.master.cpu().numpy().copy(), rs.m.cpu().numpy().copy(),
+                   rs.v.cpu().numpy().copy()))
+    finally:
+        dist.destroy_process_group()
+
+
+C5_SMALL = replace(W.scaled(W.C5, 3 * 8192 * 4 + 1001, steps=5), n_ranks=4, inject_every=2,
+                   inject_rank=3, inject_base=3 * 8192 * 3 + 17)
+
+
+@pytest.mark.parametrize("world,wl,bucket", [
+    # two ranks, one per process; a ragged last shard
+    (2, replace(W.scaled(W.C2, 2 * 5 * 8192 + 1003, steps=3), n_ranks=2), 0),
+    # fp16 with a dynamic loss scale, two ranks per process: rank 3's copy overflows on
+    # every second step (in process 1's range), so both processes must skip that step
+    (2, C5_SMALL, 0),
+    # four processes of two ranks each, 2^16-element reduce windows that cut tiles
+    (4, replace(W.scaled(W.C2, 8 * 3 * 8192 + 4099, steps=3), n_ranks=8), 1 << 16),
+])
+def test_ranks_over_processes_equal_the_one_gpu_step(world, wl, bucket):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_proc_main, args=(p, world, port, wl, bucket, q))
+             for p in range(world)]
+    for p in procs:
+        p.start()
+    got = {}
+    try:
+        for _ in range(world):
+            r = q.get(timeout=600)
+            got[r[0]] = r[1:]
+    except queue.Empty:
+        pytest.fail(f"processes {sorted(set(range(world)) - set(got))} returned nothing")
+    finally:
+        for p in procs:
+            p.join(timeout=120)
+            if p.is_alive():
+                p.terminate()
+    assert all(p.exitcode == 0 for p in procs)
+
+    # the one-GPU step on the same layout (three launches per step), and the oracle
+    ref = GpuRun(wl, bucket, split=True, align=8)
+    orc = OracleRun(wl, align=8)
+    skipped = 0
+    for step in range(1, wl.steps + 1):
+        sr = ref.step(step)
+        rep = orc.step(step)
+        skipped += rep.skipped
+        want_state = ref.st.cpu().numpy()
+        want_params = ref.out.cpu().numpy().view(np.uint16)
+        for p in range(world):
+            st_p, params_p = got[p][2][step - 1]
+            assert np.array_equal(st_p, want_state), f"process {p}, step {step}: step state"
+            assert np.array_equal(params_p, want_params), f"process {p}, step {step}: parameters"
+        assert_scalars(sr, rep)
+    if wl.inject_every:
+        assert skipped >= 2
+    arrays = ref.arrays()
+    full = {k: np.empty_like(arrays[k]) for k in ("g", "master", "m", "v")}
+    for p in range(world):
+        origin, n, _, g, master, m, v = got[p]
+        sl = slice(origin, origin + n)
+        for k, a in (("g", g), ("master", master), ("m", m), ("v", v)):
+            b = arrays[k][sl]
+            same = (a.view(np.uint32) == b.view(np.uint32)) | (np.isnan(a) & np.isnan(b))
+            assert same.all(), f"process {p}: {k} differs from the one-GPU step"
+            full[k][sl] = a
+    full["out"] = got[0][2][-1][1]
+    assert_state_close(full, orc.arrays(), wl.psi, exact_expected=False)
+    ref.check_guards()

@@ -144,3 +144,136 @@ def test_ranks_as_processes_match_single_process(world, psi, clip):
         sl = slice(r * S, (r + 1) * S)
         for a, b in ((ms, master[sl]), (mm, m[sl]), (mv, v[sl]), (mg, g[sl])):
             assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+# ---------------------------------------------------------------------------------------
+# The product's exchange layer (zero_partitioned_optimizer_shard_gb300.ranks) on CPU: each
+# process holds a contiguous group of ranks; the arithmetic of each step is the oracle's,
+# the data movement is the library's Exchange (all-to-all of the 16-bit copies, all-gather
+# of the per-rank sums of squares and of the parameters, maximum of the overflow word).
+# ---------------------------------------------------------------------------------------
+def _group_main(proc, world, port, n_ranks, psi, seed, steps, clip, inject, out_q):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=proc, world_size=world)
+    try:
+        from zero_partitioned_optimizer_shard_gb300.ranks import Exchange, local_ranks
+        ex = Exchange()
+        rb, R = local_ranks(n_ranks, world, proc)
+        orc = oracle.load()
+        lay = orc.partition(psi, n_ranks, 2, 8)
+        S, P = lay.shard, lay.psi_padded
+        lo, L = rb * S, R * S
+        hp = oracle.hparams(max_grad_norm=clip)
+        sc = oracle.scaler(1.0, False)
+        master = _state(synth.ROLE_MASTER, synth.NORMAL, 0.02, lo, L, psi, seed)
+        m = _state(synth.ROLE_MOM, synth.NORMAL, 1e-4, lo, L, psi, seed)
+        v = _state(synth.ROLE_VAR, synth.NORMAL_SQ, 1e-4, lo, L, psi, seed)
+        g = np.zeros(L, np.float32)
+        params = torch.zeros(P, dtype=torch.int16)
+        results = []
+        for step in range(1, steps + 1):
+            copies = []
+            for j in range(R):
+                c = synth.fill_host(synth.OUT_BF16, synth.NORMAL,
+                                    synth.key(seed, synth.ROLE_GRAD, step, rb + j), 0, P, psi, SIGMA)
+                if inject and inject[0] == step and inject[1] == rb + j:
+                    c[inject[2]] = 0x7F80  # bf16 +inf
+                copies.append(torch.from_numpy(c.view(np.int16)))
+            recv = [torch.empty(P, dtype=torch.int16) for _ in range(R)]
+            for j in range(R):
+                ex.all_to_all(recv[j], copies[j])
+            # rank k's copy of this process's range: chunk k // R of local copy k % R
+            win = [recv[k % R][(k // R) * L:(k // R + 1) * L].numpy().view(np.uint16).copy()
+                   for k in range(n_ranks)]
+            sumsq = torch.zeros(n_ranks, dtype=torch.float64)
+            ov = np.zeros(1, np.uint32)
+            orc.reduce_window(lay, oracle.BF16, win, lo, L, orc.inv_scale(n_ranks, 1.0), g,
+                              sumsq.numpy(), ov)
+            ex.all_gather(sumsq, rb, rb + R)
+            flag = torch.tensor([int(ov[0])], dtype=torch.int32)
+            ex.maximum(flag)
+            norm, _ = orc.global_norm(sumsq.numpy())
+            applied = orc.scaler_update(sc, int(flag.item()))
+            c = orc.clip_coef(norm, hp.max_grad_norm) if applied else 1.0
+            if applied:
+                n = max(0, min(L, psi - lo))  # parameters in this range; the rest is padding
+                out = np.zeros(L, np.uint16)
+                orc.adamw_elements(hp, c, sc.t, g[:n], master[:n], m[:n], v[:n], out[:n])
+                params[lo:lo + L] = torch.from_numpy(out.view(np.int16))
+                ex.all_gather(params, lo, lo + L)
+            results.append((norm, c, int(flag.item()), params.numpy().view(np.uint16).copy()))
+        out_q.put((proc, results, master.copy(), m.copy(), v.copy(), g.copy()))
+    finally:
+        dist.destroy_process_group()
+
+
+def _single_process_aligned(n_ranks, psi, seed, steps, clip, inject):
+    orc = oracle.load()
+    lay = orc.partition(psi, n_ranks, 2, 8)
+    P = lay.psi_padded
+    hp = oracle.hparams(max_grad_norm=clip)
+    sc = oracle.scaler(1.0, False)
+    master = _state(synth.ROLE_MASTER, synth.NORMAL, 0.02, 0, P, psi, seed)
+    m = _state(synth.ROLE_MOM, synth.NORMAL, 1e-4, 0, P, psi, seed)
+    v = _state(synth.ROLE_VAR, synth.NORMAL_SQ, 1e-4, 0, P, psi, seed)
+    g = np.zeros(P, np.float32)
+    out = np.zeros(P, np.uint16)
+    res = []
+    for step in range(1, steps + 1):
+        reps = [synth.fill_host(synth.OUT_BF16, synth.NORMAL,
+                                synth.key(seed, synth.ROLE_GRAD, step, k), 0, P, psi, SIGMA)
+                for k in range(n_ranks)]
+        if inject and inject[0] == step:
+            reps[inject[1]][inject[2]] = 0x7F80
+        rep = orc.step(lay, hp, oracle.BF16, reps, g, master, m, v, out, sc)
+        res.append((rep.norm, rep.clip_coef, rep.overflow, out.copy()))
+    return lay, res, master, m, v, g
+
+
+@pytest.mark.parametrize("world,n_ranks,psi,clip,inject", [
+    (2, 2, 10_001, 1e-3, None),
+    (2, 4, 5_000, 1.0, (2, 3, 77)),        # two ranks per process; rank 3 overflows at step 2
+    (4, 8, 20_011, 1e-3, None),            # two ranks per process, four processes
+    (4, 4, 13, 0.0, None),                 # the last ranks hold only padding
+])
+def test_exchange_layer_over_processes_matches_single_process(world, n_ranks, psi, clip, inject):
+    seed, steps = 7, 3
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_group_main,
+                         args=(p, world, port, n_ranks, psi, seed, steps, clip, inject, q))
+             for p in range(world)]
+    for p in procs:
+        p.start()
+    got = {}
+    try:
+        for _ in range(world):
+            proc, results, master, m, v, g = q.get(timeout=300)
+            got[proc] = (results, master, m, v, g)
+    except queue.Empty:
+        pytest.fail(f"processes {sorted(set(range(world)) - set(got))} returned nothing")
+    finally:
+        for p in procs:
+            p.join(timeout=60)
+            if p.is_alive():
+                p.terminate()
+    assert all(p.exitcode == 0 for p in procs)
+    lay, ref, master, m, v, g = _single_process_aligned(n_ranks, psi, seed, steps, clip, inject)
+    L = lay.shard * (n_ranks // world)
+    for p in range(world):
+        results, ms, mm, mv, mg = got[p]
+        for (n_a, c_a, f_a, out_a), (n_b, c_b, f_b, out_b) in zip(results, ref):
+            assert f_a == f_b
+            if not f_b:
+                assert n_a == n_b and c_a == c_b
+            assert np.array_equal(out_a, out_b)
+        sl = slice(p * L, (p + 1) * L)
+        for a, b in ((ms, master[sl]), (mm, m[sl]), (mv, v[sl])):
+            assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+        # g: bit for bit, NaN payloads aside (an overflowing step's g holds inf/NaN)
+        same = (mg.view(np.uint32) == g[sl].view(np.uint32)) | (np.isnan(mg) & np.isnan(g[sl]))
+        assert same.all()
+    if inject:
+        assert any(r[2] for r in ref)  # the injected step really overflowed and was skipped

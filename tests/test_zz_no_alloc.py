@@ -5,7 +5,8 @@ the GPU's memory, or it must not take the synchronisation a cudaMalloc/cudaFree 
 cause mid-step), so this entry point keeps the per-tile sum-of-squares partials in a
 static device array inside the library.  The test calls it through the C ABI twice in a
 row and checks every output against zero_step, the entry point with a caller-provided
-workspace, on identical inputs, within the tolerances the other GPU tests use.  It
+workspace, on identical inputs, within the tolerances the other GPU tests use; around the
+second call it checks that neither torch's allocator nor the device's free memory moved.  It
 passes alone in a fresh process and after the rest of the suite (the array keeps the
 previous call's contents, and each call clears the slots it uses).
 """
@@ -52,8 +53,16 @@ def test_static_workspace_matches_zero_step_twice(wl, bucket):
     for step in (1, 2):
         ref.step(step)
         new.gen_grads(step)
+        torch.cuda.synchronize()
+        before = (torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0])
         z.zero_step_static_workspace(new.lay, new.hp, dt, new.bucket_ptrs(), new.g, new.master,
                                      new.m, new.v, new.out, new.st)
+        torch.cuda.synchronize()
+        after = (torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0])
+        if step > 1:
+            # the first call on the device may load the library's kernels (lazy module
+            # loading); every later call must leave the device's free memory as it was
+            assert after == before, f"device memory changed across the call: {before} -> {after}"
         sr, sn = ref.state(), new.state()
         assert (sn.t, sn.skip, sn.loss_scale, sn.n_steps) == (sr.t, sr.skip, sr.loss_scale, sr.n_steps)
         assert abs(sn.norm - sr.norm) <= NORM_REL * sr.norm

@@ -223,6 +223,31 @@ def zero_adamw_cast_gather_host_state(layout: Layout, hp: HParams, g, master, m,
         _ptr(st), _stream(stream)))
 
 
+def zero_reduce_shard_unscale_local(layout: Layout, dtype: int, rank_begin: int, rank_count: int,
+                                    replicas: Sequence, begin: int, count: int, g_local, partials,
+                                    st, stream=None) -> None:
+    """g_local holds flat [rank_begin*S, (rank_begin+rank_count)*S) from index 0."""
+    f = _lib().zero_reduce_shard_unscale_local
+    f.argtypes = [C.POINTER(Layout), C.c_int, C.c_uint32, C.c_uint32, C.POINTER(_P), C.c_uint64,
+                  C.c_uint64, _P, _P, _P, _P]
+    f.restype = C.c_int
+    _check("zero_reduce_shard_unscale_local", f(
+        C.byref(layout), dtype, rank_begin, rank_count, _ptr_array(replicas), begin, count,
+        _ptr(g_local), _ptr(partials), _ptr(st), _stream(stream)))
+
+
+def zero_adamw_cast_gather_local(layout: Layout, hp: HParams, rank_begin: int, rank_count: int,
+                                 g_local, master_local, m_local, v_local, params_local, st,
+                                 stream=None) -> None:
+    f = _lib().zero_adamw_cast_gather_local
+    f.argtypes = [C.POINTER(Layout), C.POINTER(HParams), C.c_uint32, C.c_uint32, _P, _P, _P, _P,
+                  _P, _P, _P]
+    f.restype = C.c_int
+    _check("zero_adamw_cast_gather_local", f(
+        C.byref(layout), C.byref(hp), rank_begin, rank_count, _ptr(g_local), _ptr(master_local),
+        _ptr(m_local), _ptr(v_local), _ptr(params_local), _ptr(st), _stream(stream)))
+
+
 def zero_step(layout: Layout, hp: HParams, dtype: int, replicas: Sequence, g, partials, master, m,
               v, params, st, stream=None) -> None:
     """replicas: n_buckets * N device buffers (or addresses), bucket-major."""
@@ -272,6 +297,6 @@ __all__ = [
     "ZERO_F16", "ZERO_BF16", "Segment", "zero_partition", "zero_segment_map", "zero_workspace_bytes", "zero_step_state_init",
     "zero_step_state_read", "zero_step_state_write", "zero_reduce_shard_unscale",
     "zero_grad_norm", "zero_adamw_cast_gather", "zero_adamw_cast_gather_host_state", "zero_step",
-    "zero_step_host", "zero_step_launches",
-    "zero_step_static_workspace",
+    "zero_step_host", "zero_step_launches", "zero_reduce_shard_unscale_local",
+    "zero_adamw_cast_gather_local", "zero_step_static_workspace",
 ]

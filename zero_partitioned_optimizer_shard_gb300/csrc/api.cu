@@ -323,6 +323,79 @@ extern "C" int zero_adamw_cast_gather_host_state(const zero_layout_t* layout,
     return adamw(layout, hp, g, dm[0], dm[1], dm[2], params, st, (cudaStream_t)stream, true);
 }
 
+/* Ranks [rank_begin, rank_begin + rank_count) held by one process: their flat range
+ * starts at origin = rank_begin*S and is local_len = rank_count*S long.  ZERO_EALIGN when
+ * origin is not a multiple of 8 (partition with align = 8 for rank-local buffers). */
+namespace zero {
+namespace {
+int local_range(const zero_layout_t* L, uint32_t rank_begin, uint32_t rank_count,
+                uint64_t& origin, uint64_t& local_len)
+{
+    if (rank_count == 0 || rank_begin >= L->n_ranks || rank_count > L->n_ranks - rank_begin)
+        return ZERO_EINVAL;
+    origin = (uint64_t)rank_begin * L->shard;
+    local_len = (uint64_t)rank_count * L->shard;
+    return origin % 8 == 0 ? ZERO_OK : ZERO_EALIGN;
+}
+}  // namespace
+}  // namespace zero
+
+extern "C" int zero_reduce_shard_unscale_local(const zero_layout_t* layout, zero_dtype_t dtype,
+                                               uint32_t rank_begin, uint32_t rank_count,
+                                               const void* const* replicas, uint64_t begin,
+                                               uint64_t count, float* g_local, double* partials,
+                                               zero_step_state_t* st, zero_stream_t stream)
+{
+    const NvtxRange range("zero_reduce_shard_unscale_local");
+    if (!kernel_layout_ok(layout))
+        return ZERO_EINVAL;
+    uint64_t origin = 0, len = 0;
+    int rc = local_range(layout, rank_begin, rank_count, origin, len);
+    if (rc == ZERO_EINVAL)
+        return rc;
+    if (count == 0 || begin < origin || begin >= origin + len || count > origin + len - begin)
+        return ZERO_EINVAL;
+    const int rc_args = check_reduce_args(layout, dtype, replicas, begin, count, g_local, partials, st);
+    if (rc_args != ZERO_OK)
+        return rc_args;
+    if (rc != ZERO_OK)
+        return rc;
+    // the kernel indexes g by the flat index: hand it the address flat 0 would have, an
+    // integer offset that it never dereferences below origin (the window starts there)
+    float* g_flat = reinterpret_cast<float*>(reinterpret_cast<uintptr_t>(g_local) - origin * sizeof(float));
+    return reduce_window(layout, dtype, replicas, begin, count, g_flat, partials, st,
+                         (cudaStream_t)stream);
+}
+
+extern "C" int zero_adamw_cast_gather_local(const zero_layout_t* layout,
+                                            const zero_adamw_hparams_t* hp, uint32_t rank_begin,
+                                            uint32_t rank_count, const float* g_local,
+                                            float* master_local, float* m_local, float* v_local,
+                                            uint16_t* params_local, const zero_step_state_t* st,
+                                            zero_stream_t stream)
+{
+    const NvtxRange range("zero_adamw_cast_gather_local");
+    if (!kernel_layout_ok(layout))
+        return ZERO_EINVAL;
+    uint64_t origin = 0, len = 0;
+    int rc = local_range(layout, rank_begin, rank_count, origin, len);
+    if (rc == ZERO_EINVAL)
+        return rc;
+    const int rc_args = check_adamw_args(layout, hp, g_local, master_local, m_local, v_local,
+                                         params_local, st);
+    if (rc_args != ZERO_OK)
+        return rc_args;
+    if (rc != ZERO_OK)
+        return rc;
+    // the same pass over the local range: its first psi - origin elements (if any) are
+    // parameters, the rest padding
+    zero_layout_t local = *layout;
+    local.psi = layout->psi > origin ? (layout->psi - origin < len ? layout->psi - origin : len) : 0;
+    local.psi_padded = len;
+    return adamw(&local, hp, g_local, master_local, m_local, v_local, params_local, st,
+                 (cudaStream_t)stream);
+}
+
 extern "C" int zero_step(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,
                          zero_dtype_t dtype, const void* const* replicas, float* g, double* partials,
                          float* master, float* m, float* v, uint16_t* params, zero_step_state_t* st,

@@ -1,0 +1,197 @@
+"""The ZeRO step with its ranks spread over processes (one process per GPU).
+
+"【论文解读】ZeRO" sec. 6(2) and the stage-2 flow of "ZeRO技术概述": every rank receives each
+rank's gradient of its own partition (the reduce-scatter), updates only that partition of
+the fp32 optimizer state, and the updated parameters are all-gathered.  The Megatron
+distributed-optimizer page (sec. 1): one all-reduce forms the global gradient norm before
+clipping.  Here each process holds a contiguous group of the N ranks, [rank_begin,
+rank_begin + rank_count), and only their part of g, master, m and v.
+
+Every step of the arithmetic runs in the library's kernels, through the C ABI:
+zero_reduce_shard_unscale_local, zero_grad_norm and zero_adamw_cast_gather_local.  This
+module only moves data between processes with torch.distributed (NCCL on the device
+buffers; gloo through host memory):
+
+  1. gradients   one all-to-all of equal chunks per local gradient copy: process q
+                 receives every rank's copy of its own flat range, in rank order;
+  2. norm        all-gather of every process's tile partials (fp64, a few bytes per 8192
+                 parameters) and a maximum over processes of the step state's overflow
+                 word; each process then forms the same norm, clip coefficient, scaler
+                 update and skip decision;
+  3. parameters  all-gather of each process's 16-bit parameters into the full buffer.
+
+The reduce-scatter is an all-to-all of the raw 16-bit copies followed by the local fp32 sum
+in ascending rank order, rather than NCCL's reduce-scatter: each process sends and receives
+the same (G-1)/G of its copies either way, but the order of the sum is then fixed, so
+every output equals the one-GPU step's (zero_step on the same layout) bit for bit, wherever
+the ranks live.  16-bit buffers travel as bytes (gloo has no 16-bit integer type).
+"""
+from __future__ import annotations
+
+from typing import Sequence
+
+import torch
+import torch.distributed as dist
+
+from . import (STATE_BYTES, StepState, zero_adamw_cast_gather_local, zero_grad_norm,
+               zero_partition, zero_reduce_shard_unscale_local, zero_step_state_init)
+
+# index of the step state's overflow word in an int32 view of the 128-byte state
+OVERFLOW_WORD = StepState.overflow.offset // 4
+
+
+def local_ranks(n_ranks: int, world: int, proc: int) -> tuple[int, int]:
+    """(rank_begin, rank_count): the contiguous ranks process `proc` of `world` holds."""
+    if world < 1 or not 0 <= proc < world or n_ranks % world:
+        raise ValueError(f"{n_ranks} ranks cannot be split evenly over {world} processes")
+    count = n_ranks // world
+    return proc * count, count
+
+
+class Exchange:
+    """The step's collectives over torch.distributed, on tensors of any device.
+
+    With NCCL the collectives run on the device tensors themselves.  With another backend
+    (gloo), device tensors are copied to host memory, exchanged there and copied back;
+    host tensors are exchanged directly.
+    """
+
+    def __init__(self, group=None):
+        self.group = group
+        self.world = dist.get_world_size(group)
+        self.proc = dist.get_rank(group)
+        self.nccl = dist.get_backend(group) == "nccl"
+
+    def _host(self, t: torch.Tensor) -> bool:
+        return t.is_cuda and not self.nccl
+
+    def all_to_all(self, out: torch.Tensor, inp: torch.Tensor) -> None:
+        """Chunk q of `inp` goes to process q; chunk q of `out` comes from process q
+        (world equal chunks each, as bytes)."""
+        o, i = out.view(torch.uint8), inp.view(torch.uint8)
+        if self._host(o):
+            oh = torch.empty(o.numel(), dtype=torch.uint8)
+            dist.all_to_all_single(oh, i.cpu(), group=self.group)
+            o.copy_(oh)
+        else:
+            dist.all_to_all_single(o, i, group=self.group)
+
+    def all_gather(self, full: torch.Tensor, lo: int, hi: int) -> None:
+        """Every process contributes full[lo:hi] (its own part, the same length on each);
+        afterwards `full` holds all parts in process order."""
+        part = full[lo:hi]
+        if full.dtype in (torch.int16, torch.float16, torch.bfloat16):
+            full, part = full.view(torch.uint8), part.view(torch.uint8)
+        if self._host(full):
+            fh = torch.empty(full.numel(), dtype=full.dtype)
+            dist.all_gather_into_tensor(fh, part.cpu(), group=self.group)
+            full.copy_(fh)
+        elif self.nccl:
+            dist.all_gather_into_tensor(full, part, group=self.group)  # in place
+        else:
+            dist.all_gather_into_tensor(full, part.clone(), group=self.group)
+
+    def maximum(self, t: torch.Tensor) -> None:
+        """Element-wise maximum over processes, in place."""
+        if self._host(t):
+            th = t.cpu()
+            dist.all_reduce(th, op=dist.ReduceOp.MAX, group=self.group)
+            t.copy_(th)
+        else:
+            dist.all_reduce(t, op=dist.ReduceOp.MAX, group=self.group)
+
+
+class RankStep:
+    """One process's part of the ZeRO step: its ranks' g, master, m, v (local_len =
+    rank_count * S elements each, flat index - origin), the full gathered parameters, the
+    full tile partials and the step state, all on `device`.  The state arrays start at 0;
+    fill them (e.g. from a checkpoint) before the first step.
+
+    layout      from zero_partition with align = 8 (the local buffers start at flat
+                origin = rank_begin * S, which must be a multiple of 8)
+    dtype       ZERO_F16 or ZERO_BF16: the gradient copies' element type
+    """
+
+    def __init__(self, layout, hp, dtype: int, loss_scale: float = 1.0, dynamic: bool = False,
+                 growth_interval: int = 1000, device=None, group=None):
+        self.lay, self.hp, self.dtype = layout, hp, dtype
+        self.ex = Exchange(group)
+        self.world, self.proc = self.ex.world, self.ex.proc
+        self.rank_begin, self.rank_count = local_ranks(layout.n_ranks, self.world, self.proc)
+        S, P = layout.shard, layout.psi_padded
+        self.origin, self.local_len = self.rank_begin * S, self.rank_count * S
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        self.dev = dev
+        self.g = torch.empty(self.local_len, dtype=torch.float32, device=dev)
+        self.master = torch.zeros(self.local_len, dtype=torch.float32, device=dev)
+        self.m = torch.zeros(self.local_len, dtype=torch.float32, device=dev)
+        self.v = torch.zeros(self.local_len, dtype=torch.float32, device=dev)
+        self.params = torch.zeros(P, dtype=torch.int16, device=dev)
+        self.params_local = self.params[self.origin:self.origin + self.local_len]
+        self.partials = torch.empty(layout.n_tiles, dtype=torch.float64, device=dev)
+        self.st = torch.empty(STATE_BYTES, dtype=torch.uint8, device=dev)
+        # every rank's copy of this process's range arrives in these (one per local copy)
+        self.recv = [torch.empty(P, dtype=torch.int16, device=dev) for _ in range(self.rank_count)] \
+            if self.world > 1 else []
+        zero_step_state_init(layout, loss_scale, dynamic, growth_interval, self.st, self.partials)
+
+    def windows(self) -> list[tuple[int, int]]:
+        """The layout's reduce windows (its bucket grid) clipped to the local range."""
+        W, lo, hi = self.lay.bucket_elems, self.origin, self.origin + self.local_len
+        out = []
+        b = lo // W
+        while b * W < hi:
+            begin, end = max(b * W, lo), min((b + 1) * W, hi)
+            out.append((begin, end - begin))
+            b += 1
+        return out
+
+    def sources(self, copies: Sequence[torch.Tensor]) -> list[int]:
+        """Device address of flat `origin` in rank k's gradient copy, k = 0 .. N-1."""
+        R, L = self.rank_count, self.local_len
+        out = []
+        for k in range(self.lay.n_ranks):
+            q, j = divmod(k, R)
+            if q == self.proc:
+                out.append(copies[j].data_ptr() + 2 * self.origin)
+            else:
+                out.append(self.recv[j].data_ptr() + 2 * q * L)
+        return out
+
+    def step(self, copies: Sequence[torch.Tensor]) -> None:
+        """One optimizer step on the current stream (the one torch.distributed orders its
+        collectives against).  copies: this process's rank_count gradient copies (ranks
+        rank_begin, rank_begin+1, ... in order), psi_padded 16-bit elements each, on the
+        device; their padding elements are ignored."""
+        lay, R = self.lay, self.rank_count
+        if len(copies) != R:
+            raise ValueError(f"expected {R} gradient copies, got {len(copies)}")
+        s = torch.cuda.current_stream(self.dev)
+        # 1. every rank's copy of this process's range
+        for j in range(R if self.world > 1 else 0):
+            self.ex.all_to_all(self.recv[j], copies[j])
+        src = self.sources(copies)
+        for begin, count in self.windows():
+            off = 2 * (begin - self.origin)
+            zero_reduce_shard_unscale_local(lay, self.dtype, self.rank_begin, R,
+                                            [p + off for p in src], begin, count, self.g,
+                                            self.partials, self.st, s)
+        # 2. the global norm's inputs: every process's tile partials and overflow flag
+        if self.world > 1:
+            tpr = lay.tiles_per_rank
+            self.ex.all_gather(self.partials, self.rank_begin * tpr, (self.rank_begin + R) * tpr)
+            self.ex.maximum(self.st.view(torch.int32)[OVERFLOW_WORD:OVERFLOW_WORD + 1])
+        zero_grad_norm(lay, self.hp, self.partials, self.st, s)
+        # 3. this process's shards, then the parameter all-gather
+        zero_adamw_cast_gather_local(lay, self.hp, self.rank_begin, R, self.g, self.master,
+                                     self.m, self.v, self.params_local, self.st, s)
+        if self.world > 1:
+            self.ex.all_gather(self.params, self.origin, self.origin + self.local_len)
+
+
+def layout_for(psi: int, n_ranks: int, stage: int = 2, bucket_elems: int = 0):
+    """zero_partition with the alignment rank-local buffers need (S a multiple of 8)."""
+    return zero_partition(psi, n_ranks, stage, 8, bucket_elems)
+
+
+__all__ = ["Exchange", "RankStep", "local_ranks", "layout_for", "OVERFLOW_WORD"]
