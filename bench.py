@@ -148,18 +148,44 @@ def cpu_oracle_baseline(steps: int = 1, psi_sample: int = 1 << 24, base=None):
     return wl.psi * steps / dt, dt, wl
 
 
+def cpu_baseline_all_cores(base, psi_sample: int, seconds: float = 8.0) -> dict:
+    """The oracle on every host core (oracle.parallel: fixed 2^20-element chunks on a
+    pool of spawned processes, so the result does not depend on the core count), timed
+    for about `seconds` on a psi_sample-parameter sample of the workload's recipe; plus
+    the single-threaded oracle step on a smaller sample for comparison."""
+    from oracle.parallel import ParallelOracle, host_cores
+    from synth import workloads as W
+
+    wl = base if psi_sample == base.psi else W.scaled(base, psi_sample)
+    cores = host_cores()
+    with ParallelOracle(wl, cores) as par:
+        one = par.time_steps(1)
+        steps = max(2, min(200, int(seconds / max(one, 1e-3))))
+        dt = par.time_steps(steps)
+    single_psi = min(1 << 22, base.psi)
+    v1, dt1, _ = cpu_oracle_baseline(2, single_psi, base)
+    return {"value": wl.psi * steps / dt, "unit": "params/s", "cores": cores, "kind": "oracle",
+            "sample": f"{steps} oracle steps of the {_recipe_name(base)} recipe at psi="
+                      f"{wl.psi} (N={wl.n_ranks} {wl.grad_dtype} copies) on {cores} host "
+                      f"processes (2^20-element chunks), {dt:.1f} s",
+            "single_core": {"value": v1, "unit": "params/s", "cores": 1,
+                            "sample": f"2 serial oracle steps at psi={single_psi}, {dt1:.1f} s"}}
+
+
 def run_reference(args):
+    from oracle.parallel import ParallelOracle, host_cores
+    from synth import workloads as W
+
     ws, rank, _ = _dist()
     if rank != 0:
         return 0
     base = _base_workload(args.workload)
-    sample = min(1 << 22, base.psi)
-    for _ in range(args.warmup):
-        cpu_oracle_baseline(1, sample, base)
-    total = 0.0
-    for _ in range(args.steps):
-        _, dt, wl = cpu_oracle_baseline(1, sample, base)
-        total += dt
+    sample = min(1 << 24, base.psi)
+    wl = base if sample == base.psi else W.scaled(base, sample)
+    cores = host_cores()
+    with ParallelOracle(wl, cores) as par:
+        par.time_steps(args.warmup)
+        total = par.time_steps(args.steps)
     value = sample * args.steps / total
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "params/s",
@@ -167,10 +193,10 @@ def run_reference(args):
         "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": _config(base=base),
-        "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
-                         "sample": f"each step: the {_recipe_name(base)} "
-                                   f"recipe at psi={sample} "
-                                   f"(N={base.n_ranks} {base.grad_dtype} copies), one oracle step"},
+        "cpu_baseline": {"value": value, "unit": "params/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: the {_recipe_name(base)} recipe at psi={sample} "
+                                   f"(N={base.n_ranks} {base.grad_dtype} copies), one oracle "
+                                   f"step on {cores} host processes (2^20-element chunks)"},
         "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -224,18 +250,45 @@ def _config(extra=None, psi=None, base=None):
 def run_ours(args):
     import torch
 
+    ws, rank, local = _dist()
+    if ws > 1:
+        return run_ranks(args)
+    torch.cuda.set_device(local)
+    base = _base_workload(args.workload)
+    line = _measure_simulated(args, base, args.psi)
+    torch.cuda.empty_cache()
+    if not args.no_extra_workloads and args.psi is None and args.workload == "gpt2-1.5b":
+        # the other two workloads the target names, timed by the same code on this GPU
+        # (one at a time: the headline's buffers are freed first)
+        line["workloads"] = {}
+        for name, min_steps in (("llama-7b", 0), ("c1", 200)):
+            sub = _measure_simulated(args, _base_workload(name), None, max(args.steps, min_steps))
+            torch.cuda.empty_cache()
+            line["workloads"][name] = {k: sub[k] for k in (
+                "value", "unit", "steps", "ms_per_step", "ms_per_step_spread", "config", "hbm",
+                "roofline", "kernels", "launches_per_step", "gpu_launches", "clocks", "e2e",
+                "final_state")}
+        line["gpu_launches_all_workloads"] = line["gpu_launches"] + sum(
+            w["gpu_launches"] for w in line["workloads"].values())
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_all_cores(base, min(1 << 26, base.psi))
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _measure_simulated(args, base, psi=None, steps=None):
+    """Time the step of one workload, all N ranks simulated on this GPU (zero_step, inputs
+    resident in HBM); returns the JSON line without its cpu_baseline.  Every buffer it
+    allocates is released when it returns."""
+    import torch
+
     import synth
     import zero_partitioned_optimizer_shard_gb300 as z
     from synth import workloads as W
 
-    ws, rank, local = _dist()
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    base = _base_workload(args.workload)
-    wl = base if args.psi in (None, base.psi) else W.scaled(base, args.psi)
+    steps = args.steps if steps is None else steps
+    dev = torch.device("cuda", torch.cuda.current_device())
+    wl = base if psi in (None, base.psi) else W.scaled(base, psi)
     gdt = z.ZERO_F16 if wl.grad_dtype == "f16" else z.ZERO_BF16
     lay = z.zero_partition(wl.psi, wl.n_ranks, wl.stage, 1, wl.bucket_elems)
     P, N = lay.psi_padded, lay.n_ranks
@@ -290,17 +343,15 @@ def run_ours(args):
         step()
     torch.cuda.synchronize(dev)
 
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(dev.index)
     clocks.start()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    if ws > 1:
-        dist.barrier()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
     torch.cuda.synchronize(dev)
     clocks.mark(True)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
-    for i in range(args.steps):
+    for i in range(steps):
         if flush is not None:
             flush.fill_(float(i))  # evicts the step's working set from L2; not timed
             evs[i][0].record(stream)
@@ -313,15 +364,10 @@ def run_ours(args):
     elapsed_ms = t_start.elapsed_time(t_end)
     if flush is not None:  # the flushes between steps are not part of the step
         elapsed_ms = sum(e[0].elapsed_time(e[1]) for e in evs)
-    if ws > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
-        dist.barrier()
     clk = clocks.stop()
 
     # --- per-kernel breakdown: the same launches made one by one, an event after each --
-    n_split = min(args.steps, 20)
+    n_split = min(steps, 20)
     sev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_split)]
     for i in range(n_split):
         if flush is not None:
@@ -333,7 +379,7 @@ def run_ours(args):
     norm_ms = [e[1].elapsed_time(e[2]) for e in sev]
     adamw_ms = [e[2].elapsed_time(e[3]) for e in sev]
     stt = z.zero_step_state_read(st, stream)
-    assert stt.t == args.warmup + args.steps + n_split and stt.skip == 0 and stt.norm == stt.norm
+    assert stt.t == args.warmup + steps + n_split and stt.skip == 0 and stt.norm == stt.norm
     assert stt.error == 0
 
     # --- end to end through zero_step_host: gradients from pinned host memory -----------
@@ -347,13 +393,13 @@ def run_ours(args):
         e2e = _e2e(args, z, torch, dev, wl, hp, reps, g, partials, master, m, v, out, st, stream)
 
     peak, peak_kind = _peaks()
-    ms = elapsed_ms / args.steps
+    ms = elapsed_ms / steps
     if flush is not None:
         per_step = sorted(e[0].elapsed_time(e[1]) for e in evs)
         spread = {"p10": _pct(per_step, 10), "p50": _pct(per_step, 50), "p90": _pct(per_step, 90)}
     else:
         spread = None  # back-to-back steps: no event between them to keep launches overlapped
-    params_per_s = wl.psi * args.steps * ws / (elapsed_ms / 1e3)
+    params_per_s = wl.psi * steps / (elapsed_ms / 1e3)
     bytes_26 = (26 + 2 * N) * P
     moved = _fused_moved(N, lay, True) if launches == 1 else (34 + 2 * N)  # g re-read if split
     adamw_avg = statistics.mean(adamw_ms)
@@ -376,14 +422,12 @@ def run_ours(args):
                 "traffic": _traffic_from_profile(P), "bytes_per_launch": ADAMW_BYTES * P,
                 "avg_launch_ms": adamw_avg}
     line = {
-        "metric": METRIC, "value": params_per_s, "unit": "params/s", "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "metric": METRIC, "value": params_per_s, "unit": "params/s", "n_gpus": 1,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": ms,
         "ms_per_step_spread": spread,
         "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": _config({"parallelism": f"{ws} independent replica(s) of the simulated "
-                                          f"{N}-rank step" if ws > 1 else f"1 GPU, {N} simulated ranks"},
-                          psi=wl.psi, base=base),
+        "config": _config({"parallelism": f"1 GPU, {N} simulated ranks"}, psi=wl.psi, base=base),
         "hbm": {
             "gbs_at_26p2n_bytes": bytes_26 / (ms / 1e3) / 1e9,
             "pct_of_8tbs": 100 * bytes_26 / (ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
@@ -409,24 +453,153 @@ def run_ours(args):
             "k_adamw": {"avg_ms": adamw_avg, "bytes_per_launch": ADAMW_BYTES * P, "gbs": ach},
         },
         "launches_per_step": launches,
-        "gpu_launches": launches * args.steps,
+        "gpu_launches": launches * steps,
         "clocks": clk,
         "e2e": e2e,
         "final_state": {"t": stt.t, "norm": stt.norm, "clip_coef": stt.clip_coef},
     }
-    if rank == 0 and not args.no_cpu_baseline:
-        sample = min(1 << 26, wl.psi)
-        reps_cpu = 6 * (1 << 26) // sample   # about the same CPU work at any workload size
-        v, dt, swl = cpu_oracle_baseline(reps_cpu, sample, base)
-        line["cpu_baseline"] = {"value": v, "unit": "params/s", "cores": 1, "kind": "oracle",
-                                "sample": f"{reps_cpu} oracle steps of the {_recipe_name(base)} "
-                                          f"recipe at psi={swl.psi} (N={swl.n_ranks} "
-                                          f"{swl.grad_dtype} copies), {dt:.1f} s "
-                                          f"single-threaded"}
+    return line
+
+
+def run_ranks(args):
+    """The step with its ranks spread over the processes of a torchrun job, one GPU each:
+    the workload's N ranks in contiguous groups of N/G per process
+    (zero_partitioned_optimizer_shard_gb300.ranks.RankStep), the gradient reduce-scatter,
+    the norm's all-gather and the parameter all-gather over torch.distributed.  The
+    whole job updates the workload's psi parameters per step, so the total work is fixed
+    as G grows (strong scaling).  Rank 0 prints the line; times are the maximum over
+    ranks."""
+    import torch
+    import torch.distributed as dist
+
+    import synth
+    import zero_partitioned_optimizer_shard_gb300 as z
+    from synth import workloads as W
+    from zero_partitioned_optimizer_shard_gb300.ranks import RankStep, layout_for
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local % torch.cuda.device_count())
+    dist.init_process_group(args.dist_backend)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    base = _base_workload(args.workload)
+    wl = base if args.psi in (None, base.psi) else W.scaled(base, args.psi)
+    if wl.n_ranks % ws:
+        raise SystemExit(f"{wl.n_ranks} ranks cannot be spread evenly over {ws} processes")
+    lay = layout_for(wl.psi, wl.n_ranks, wl.stage, wl.bucket_elems)
+    P, N = lay.psi_padded, lay.n_ranks
+    gdt = z.ZERO_F16 if wl.grad_dtype == "f16" else z.ZERO_BF16
+    rs = RankStep(lay, z.hparams(**wl.hp.__dict__), gdt, wl.loss_scale, wl.dynamic,
+                  wl.growth_interval, dev)
+    stream = torch.cuda.current_stream(dev)
+    s = stream.cuda_stream
+    fills = [(rs.master, synth.ROLE_MASTER, synth.NORMAL, wl.master_sigma)]
+    if wl.random_moments:
+        fills += [(rs.m, synth.ROLE_MOM, synth.NORMAL, wl.mom_sigma),
+                  (rs.v, synth.ROLE_VAR, synth.NORMAL_SQ, wl.mom_sigma)]
+    for t_, role, kind, sig in fills:
+        synth.fill_dev(t_.data_ptr(), synth.OUT_F32, kind, wl.state_key(role), rs.origin,
+                       rs.local_len, wl.psi, sig, 1.0, s)
+    copies = [torch.empty(P, dtype=torch.int16, device=dev) for _ in range(rs.rank_count)]
+    for j, c in enumerate(copies):
+        synth.fill_dev(c.data_ptr(), wl.grad_out, wl.grad_kind, wl.grad_key(1, rs.rank_begin + j),
+                       0, P, wl.psi, wl.grad_sigma, wl.loss_scale, s)
+    for _ in range(args.warmup):
+        rs.step(copies)
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    torch.cuda.synchronize(dev)
+    clocks.mark(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        rs.step(copies)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.mark(False)
+    clk = clocks.stop()
+    elapsed = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
+    dist.all_reduce(elapsed, op=dist.ReduceOp.MAX)
+    elapsed_ms = float(elapsed.item())
+
+    # per-part breakdown: more steps with an event after each part (max over ranks)
+    names = ["gradients", "reduce", "norm inputs", "norm", "adamw", "parameters"]
+    n_split = min(args.steps, 10)
+    parts = {n: [] for n in names}
+    for _ in range(n_split):
+        evs = {"start": torch.cuda.Event(enable_timing=True)}
+        evs["start"].record(stream)
+
+        def mark(name):
+            evs[name] = torch.cuda.Event(enable_timing=True)
+            evs[name].record(stream)
+        rs.step(copies, mark)
+        torch.cuda.synchronize(dev)
+        prev = "start"
+        for n in names:
+            parts[n].append(evs[prev].elapsed_time(evs[n]))
+            prev = n
+    avg = torch.tensor([statistics.mean(parts[n]) for n in names], dtype=torch.float64, device=dev)
+    dist.all_reduce(avg, op=dist.ReduceOp.MAX)
+    avg = dict(zip(names, avg.tolist()))
+    stt = z.zero_step_state_read(rs.st)
+    assert stt.error == 0 and stt.skip == 0 and stt.t == args.warmup + args.steps + n_split
+
+    # end to end: every step copies this process's gradient copies in from pinned host
+    # memory and reads the step state back
+    e2e = None
+    if not args.no_e2e:
+        hcopies = [torch.empty(P, dtype=torch.int16, pin_memory=True) for _ in copies]
+        for h, c in zip(hcopies, copies):
+            h.copy_(c)
+        hstate = torch.empty(z.STATE_BYTES, dtype=torch.uint8, pin_memory=True)
+        n_e2e = max(1, args.e2e_steps)
+        dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            for h, c in zip(hcopies, copies):
+                c.copy_(h, non_blocking=True)
+            rs.step(copies)
+            hstate.copy_(rs.st, non_blocking=True)
+            torch.cuda.synchronize(dev)
+        dt = torch.tensor([time.perf_counter() - t0], dtype=torch.float64, device=dev)
+        dist.all_reduce(dt, op=dist.ReduceOp.MAX)
+        e2e = {"value": wl.psi * n_e2e / float(dt.item()), "unit": "params/s",
+               "h2d_bytes_per_step": ws * len(copies) * P * 2,
+               "d2h_bytes_per_step": ws * z.STATE_BYTES, "steps": n_e2e,
+               "ms_per_step": float(dt.item()) / n_e2e * 1e3,
+               "path": "every process: its gradient copies from pinned host memory, RankStep "
+                       "(all-to-all, local reduce, norm exchange, norm, local AdamW, parameter "
+                       "all-gather), step state read back"}
+    peak, peak_kind = _peaks()
+    ms = elapsed_ms / args.steps
+    L = rs.local_len
+    ach = ADAMW_BYTES * L / (avg["adamw"] / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": wl.psi * args.steps / (elapsed_ms / 1e3), "unit": "params/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": _config({"parallelism": f"{ws} GPUs x {rs.rank_count} of the {N} ZeRO ranks "
+                                          f"each ({args.dist_backend}: all-to-all of the 16-bit "
+                                          "gradient copies, all-gather of tile partials and "
+                                          "parameters, max of the overflow flag)"},
+                          psi=wl.psi, base=base),
+        "roofline": {"kernel": "k_adamw on this process's ranks (zero_adamw_cast_gather_local)",
+                     "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+                     "frac": ach / peak, "peak_kind": peak_kind, "traffic": None,
+                     "bytes_per_launch": ADAMW_BYTES * L, "avg_launch_ms": avg["adamw"]},
+        "parts_ms": avg,
+        "launches_per_step": len(rs.windows()) + 2,
+        "gpu_launches": (len(rs.windows()) + 2) * args.steps,
+        "clocks": clk, "e2e": e2e,
+        "final_state": {"t": stt.t, "norm": stt.norm, "clip_coef": stt.clip_coef},
+    }
     if rank == 0:
         print(json.dumps(line), flush=True)
-    if ws > 1:
-        dist.destroy_process_group()
+    dist.barrier()
+    dist.destroy_process_group()
     return 0
 
 
@@ -444,9 +617,10 @@ def _fused_moved(N: int, lay, g_written: bool) -> int:
 
 
 def _traffic_from_profile(psi_padded):
-    """DRAM bytes per k_adamw launch over psi_padded parameters, scaled from the committed
-    ncu capture (traffic is proportional to the parameters), or None when the kernel
-    source has changed since those counters were taken."""
+    """DRAM bytes per k_adamw launch over psi_padded parameters from the committed ncu
+    captures: a line slope * psi + intercept through three sizes (the intercept is the
+    fixed amount of the launch's last writes still in L2 when it ends), or None when the
+    kernel source has changed since those counters were taken."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "k_adamw_traffic.json")
     csrc = os.path.join(ROOT, "zero_partitioned_optimizer_shard_gb300", "csrc")
@@ -460,7 +634,7 @@ def _traffic_from_profile(psi_padded):
         sha = h.hexdigest()
         if not sha.startswith(rec["source_sha256_prefix"]):
             return None
-        return round(rec["traffic_bytes_per_launch_small"] * psi_padded / rec["small_psi"])
+        return round(rec["slope_bytes_per_param"] * psi_padded + rec["intercept_bytes"])
     except Exception:
         return None
 
@@ -863,6 +1037,11 @@ def main():
                          "psi=6,738,415,616, N=8, ZeRO-3, 51 gradient buckets of 2^27 elements; "
                          "c1: psi=1,000,003, N=4, fp16 copies, dynamic loss scale (latency-bound, "
                          "L2 flushed before every step)")
+    ap.add_argument("--no-extra-workloads", action="store_true",
+                    help="time only the headline workload (no llama-7b / c1 sub-lines)")
+    ap.add_argument("--dist-backend", default="nccl", choices=["nccl", "gloo"],
+                    help="under torchrun: the exchange's backend (gloo stages through host "
+                         "memory; for checking the path where only one GPU is present)")
     ap.add_argument("--psi", type=int, default=None,
                     help="profiling only: the same recipe at another size (default: the "
                          "GPT-2-1.5B buffer)")

@@ -158,35 +158,44 @@ class RankStep:
                 out.append(self.recv[j].data_ptr() + 2 * q * L)
         return out
 
-    def step(self, copies: Sequence[torch.Tensor]) -> None:
+    def step(self, copies: Sequence[torch.Tensor], mark=None) -> None:
         """One optimizer step on the current stream (the one torch.distributed orders its
         collectives against).  copies: this process's rank_count gradient copies (ranks
         rank_begin, rank_begin+1, ... in order), psi_padded 16-bit elements each, on the
-        device; their padding elements are ignored."""
+        device; their padding elements are ignored.  mark: optional callable, called with
+        the name of each part as it has been enqueued ("gradients", "reduce", "norm
+        inputs", "norm", "adamw", "parameters"), e.g. to record timing events."""
         lay, R = self.lay, self.rank_count
         if len(copies) != R:
             raise ValueError(f"expected {R} gradient copies, got {len(copies)}")
         s = torch.cuda.current_stream(self.dev)
         # 1. every rank's copy of this process's range
+        mark = mark or (lambda name: None)
         for j in range(R if self.world > 1 else 0):
             self.ex.all_to_all(self.recv[j], copies[j])
+        mark("gradients")
         src = self.sources(copies)
         for begin, count in self.windows():
             off = 2 * (begin - self.origin)
             zero_reduce_shard_unscale_local(lay, self.dtype, self.rank_begin, R,
                                             [p + off for p in src], begin, count, self.g,
                                             self.partials, self.st, s)
+        mark("reduce")
         # 2. the global norm's inputs: every process's tile partials and overflow flag
         if self.world > 1:
             tpr = lay.tiles_per_rank
             self.ex.all_gather(self.partials, self.rank_begin * tpr, (self.rank_begin + R) * tpr)
             self.ex.maximum(self.st.view(torch.int32)[OVERFLOW_WORD:OVERFLOW_WORD + 1])
+        mark("norm inputs")
         zero_grad_norm(lay, self.hp, self.partials, self.st, s)
+        mark("norm")
         # 3. this process's shards, then the parameter all-gather
         zero_adamw_cast_gather_local(lay, self.hp, self.rank_begin, R, self.g, self.master,
                                      self.m, self.v, self.params_local, self.st, s)
+        mark("adamw")
         if self.world > 1:
             self.ex.all_gather(self.params, self.origin, self.origin + self.local_len)
+        mark("parameters")
 
 
 def layout_for(psi: int, n_ranks: int, stage: int = 2, bucket_elems: int = 0):
