@@ -62,3 +62,30 @@ def test_c_program_runs_a_step_against_the_c_oracle(tmp_path):
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.strip().endswith("ok"), r.stdout
 
+
+
+def _build_ranks_program(tmp_path):
+    lib = _build.build()
+    cuda = _cuda_home()
+    exe = str(tmp_path / "c_abi_ranks")
+    subprocess.run(["gcc", "-std=c11", "-O2", "-Wall", "-Werror",
+                    "-I", os.path.join(ROOT, "include"), "-I", os.path.join(cuda, "include"),
+                    os.path.join(ROOT, "tests", "c_abi_ranks.c"), "-o", exe,
+                    "-L", os.path.dirname(lib), "-lzero_shard", f"-Wl,-rpath,{os.path.dirname(lib)}",
+                    "-L", os.path.join(cuda, "lib64"), "-lcudart",
+                    f"-Wl,-rpath,{os.path.join(cuda, 'lib64')}"], check=True)
+    return exe
+
+
+def test_c_program_of_the_rank_local_step_compiles(tmp_path):
+    assert os.path.exists(_build_ranks_program(tmp_path))
+
+
+@pytest.mark.gpu
+def test_c_program_runs_the_rank_local_step_over_two_processes(tmp_path):
+    """tests/c_abi_ranks.c: two processes of two ranks each through the rank-local entry
+    points, exchanging by cudaMemcpy, equal to zero_step bit for bit."""
+    exe = _build_ranks_program(tmp_path)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.strip().endswith("ok"), r.stdout

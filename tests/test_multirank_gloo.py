@@ -277,3 +277,64 @@ def test_exchange_layer_over_processes_matches_single_process(world, n_ranks, ps
         assert same.all()
     if inject:
         assert any(r[2] for r in ref)  # the injected step really overflowed and was skipped
+
+
+# ---------------------------------------------------------------------------------------
+# A process that leaves between steps: the others learn of it on the host.  The exchange
+# layer waits on no flag of its own; its collectives are torch.distributed's, so a peer
+# that is gone ends the next collective with an error (connection closed, or the process
+# group's timeout), never a hang.  No GPU is involved.
+# ---------------------------------------------------------------------------------------
+def _leaver_main(proc, world, port, out_q):
+    import datetime
+    import time
+
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=proc, world_size=world,
+                            timeout=datetime.timedelta(seconds=10))
+    from zero_partitioned_optimizer_shard_gb300.ranks import Exchange
+    ex = Exchange()
+    full = torch.zeros(4 * world, dtype=torch.float64)
+    full[4 * proc:4 * proc + 4] = proc + 1
+    ex.all_gather(full, 4 * proc, 4 * proc + 4)  # step 1: everyone present
+    ok = bool(torch.all(full == torch.arange(world, dtype=torch.float64).repeat_interleave(4) + 1))
+    if proc == world - 1:
+        out_q.put((proc, ok, "left"))
+        out_q.close()
+        out_q.join_thread()  # the message is out before the process goes
+        os._exit(0)  # leaves between steps, with nothing in flight
+    t0 = time.time()
+    try:
+        flag = torch.tensor([0], dtype=torch.int32)
+        ex.maximum(flag)  # step 2: the peer is gone
+        out_q.put((proc, ok, "no error"))
+    except Exception as e:  # noqa: BLE001 - any collective error is the signal
+        out_q.put((proc, ok, f"error after {time.time() - t0:.1f}s: {type(e).__name__}"))
+    out_q.close()
+    out_q.join_thread()
+    os._exit(0)
+
+
+def test_a_process_that_leaves_ends_the_next_exchange_with_an_error():
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_leaver_main, args=(p, world, port, q)) for p in range(world)]
+    for p in procs:
+        p.start()
+    got = {}
+    try:
+        for _ in range(world):
+            proc, ok, what = q.get(timeout=120)
+            got[proc] = (ok, what)
+    finally:
+        for p in procs:
+            p.join(timeout=60)
+            if p.is_alive():
+                p.terminate()
+    assert got[1] == (True, "left")
+    ok, what = got[0]
+    assert ok and what.startswith("error after"), what
+    assert float(what.split()[2].rstrip("s:")) < 30
