@@ -21,7 +21,8 @@
  * are staged by the Blackwell bulk-copy engine: one thread per block issues
  * cp.async.bulk copies of 4096-element chunks of g, master, m and v (64 KiB per chunk)
  * into a three-stage shared-memory ring tracked by mbarriers, so up to 192 KiB per SM are
- * in flight without holding registers.  One 256-thread block per SM (persistent,
+ * in flight without holding registers.  The copies carry an L2 evict-first policy (each
+ * input byte is read once), which keeps L2 for the lines being written.  One 256-thread block per SM (persistent,
  * grid-stride over chunks) computes from shared memory and writes master, m, v and 8
  * bf16 parameters per thread with streaming 128/64-bit stores.  The ragged end (the part
  * after the last whole chunk, and the padding) is done element by element.  Every
@@ -89,12 +90,10 @@ __global__ void __launch_bounds__(kBlock, 1) k_adamw(const __grid_constant__ Ada
         if (base / kChunk == zero_test_withheld_chunk)
             return;  // test builds only: this chunk's barrier never completes
 #endif
+        const uint64_t pol = l2_evict_first_policy();
         for (int q = 0; q < 4; ++q)
-            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
-                         "[%0], [%1], %2, [%3];"
-                         ::"r"(smem_addr(ring + (k * 4 + q) * kChunk)), "l"(src[q] + base),
-                         "r"((uint32_t)(kChunk * sizeof(float))), "r"(bar)
-                         : "memory");
+            bulk_load(smem_addr(ring + (k * 4 + q) * kChunk), src[q] + base,
+                      (uint32_t)(kChunk * sizeof(float)), bar, pol);
     };
     if (threadIdx.x == 0)
         for (uint64_t i = 0; i < mine && i < kStages; ++i)

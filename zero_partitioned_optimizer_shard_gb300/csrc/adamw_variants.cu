@@ -84,11 +84,9 @@ __global__ void __launch_bounds__(kBlock, 1) k_adamw_rereduce(const __grid_const
         const uint32_t bytes[5] = {kChunk * 2, kChunk * 2, kChunk * 4, kChunk * 4, kChunk * 4};
         float* dst[5] = {stage, stage + kChunk / 2, stage + kChunk, stage + 2 * kChunk,
                          stage + 3 * kChunk};
+        const uint64_t pol = l2_evict_first_policy();
         for (int q = 0; q < 5; ++q)
-            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
-                         "[%0], [%1], %2, [%3];"
-                         ::"r"(smem_addr(dst[q])), "l"(src[q]), "r"(bytes[q]), "r"(bar)
-                         : "memory");
+            bulk_load(smem_addr(dst[q]), src[q], bytes[q], bar, pol);
     };
     if (threadIdx.x == 0)
         for (uint64_t i = 0; i < mine && i < kStages; ++i)
