@@ -1,11 +1,14 @@
-"""bench.py's command-line contract, checked without a GPU: the reference arm (the CPU
-oracle) prints exactly one JSON line with the agreed keys, on one process and under
-torchrun with two ranks (rank 0 prints; the other rank exits 0 without work)."""
+"""bench.py's command-line contract.  Without a GPU: the reference arm (the CPU oracle)
+prints exactly one JSON line with the agreed keys, on one process and under torchrun with
+two ranks (rank 0 prints; the other rank exits 0 without work).  On the GPU: the rank
+path under torchrun (two processes sharing the one GPU over gloo) prints its line."""
 import json
 import os
 import socket
 import subprocess
 import sys
+
+import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 KEYS = {"impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
@@ -60,3 +63,28 @@ def test_reference_arm_names_each_workload():
         _check(lines[0], 1)
         c = lines[0]["config"]
         assert c["psi"] == psi and c["n_ranks"] == n
+
+
+@pytest.mark.gpu
+def test_rank_path_under_torchrun_two_processes_on_one_gpu():
+    """bench.py --gpus 2 runs the step with the ranks spread over two processes (here both
+    on the one GPU, exchanging over gloo through host memory): one JSON line from rank 0,
+    strong scaling, the per-part times and a final state after every step applied."""
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                        "--nproc-per-node", "2", "--master-addr", "127.0.0.1", "--master-port",
+                        str(port), "bench.py", "--gpus", "2", "--dist-backend", "gloo",
+                        "--psi", str((1 << 20) + 12345), "--steps", "3", "--warmup", "3",
+                        "--e2e-steps", "1"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = _lines(r.stdout)
+    assert len(lines) == 1
+    line = lines[0]
+    assert line["n_gpus"] == 2 and line["scaling"] == "strong" and line["value"] > 0
+    assert set(line["parts_ms"]) == {"gradients", "reduce", "norm inputs", "norm", "adamw",
+                                     "parameters"}
+    assert line["final_state"]["t"] == 3 + 3 + 3  # warm-up, timed and breakdown steps
+    assert line["e2e"]["value"] > 0 and line["gpu_launches"] == 3 * 3

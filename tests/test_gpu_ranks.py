@@ -104,6 +104,11 @@ C5_SMALL = replace(W.scaled(W.C5, 3 * 8192 * 4 + 1001, steps=5), n_ranks=4, inje
     (4, replace(W.scaled(W.C2, 8 * 3 * 8192 + 4099, steps=3), n_ranks=8), 1 << 16),
     # a larger buffer: 4.2M parameters, two processes of four ranks, 2^20-element windows
     (2, replace(W.scaled(W.C2, (1 << 22) + 13, steps=2), n_ranks=8), 1 << 20),
+    # 13 parameters over 4 ranks of 8 (align 8): process 1 holds only padding
+    (2, replace(W.scaled(W.C2, 13, steps=2), n_ranks=4), 0),
+    # fp16 gathered parameters
+    (2, replace(W.scaled(W.C2, 3 * 8192 * 4 + 77, steps=2), n_ranks=4,
+                hp=W.HP(params_dtype=1)), 0),
 ])
 def test_ranks_over_processes_equal_the_one_gpu_step(world, wl, bucket):
     ctx = mp.get_context("spawn")
