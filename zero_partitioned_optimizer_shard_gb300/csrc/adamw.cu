@@ -21,8 +21,9 @@
  * are staged by the Blackwell bulk-copy engine: one thread per block issues
  * cp.async.bulk copies of 4096-element chunks of g, master, m and v (64 KiB per chunk)
  * into a three-stage shared-memory ring tracked by mbarriers, so up to 192 KiB per SM are
- * in flight without holding registers.  The copies carry an L2 evict-first policy (each
- * input byte is read once), which keeps L2 for the lines being written.  One 256-thread block per SM (persistent,
+ * in flight without holding registers.  On buffers many times larger than L2 the copies
+ * carry an L2 evict-first policy (each input byte is read once), which keeps L2 for the
+ * lines being written.  One 256-thread block per SM (persistent,
  * grid-stride over chunks) computes from shared memory and writes master, m, v and 8
  * bf16 parameters per thread with streaming 128/64-bit stores.  The ragged end (the part
  * after the last whole chunk, and the padding) is done element by element.  Every
@@ -42,7 +43,7 @@ namespace {
 __device__ unsigned long long zero_test_withheld_chunk = ~0ull;
 #endif
 
-template <bool F16>
+template <bool F16, bool EF>
 __global__ void __launch_bounds__(kBlock, 1) k_adamw(const __grid_constant__ AdamwArgs a)
 {
     extern __shared__ __align__(128) float ring[];  // kStages x {g, master, m, v} x kChunk
@@ -90,10 +91,9 @@ __global__ void __launch_bounds__(kBlock, 1) k_adamw(const __grid_constant__ Ada
         if (base / kChunk == zero_test_withheld_chunk)
             return;  // test builds only: this chunk's barrier never completes
 #endif
-        const uint64_t pol = l2_evict_first_policy();
         for (int q = 0; q < 4; ++q)
-            bulk_load(smem_addr(ring + (k * 4 + q) * kChunk), src[q] + base,
-                      (uint32_t)(kChunk * sizeof(float)), bar, pol);
+            bulk_load<EF>(smem_addr(ring + (k * 4 + q) * kChunk), src[q] + base,
+                          (uint32_t)(kChunk * sizeof(float)), bar);
     };
     if (threadIdx.x == 0)
         for (uint64_t i = 0; i < mine && i < kStages; ++i)
@@ -167,7 +167,8 @@ cudaError_t launch_adamw(const AdamwArgs& a, cudaStream_t s)
     int dev = 0;
     cudaGetDevice(&dev);
     if (!configured[dev & 63].load(std::memory_order_relaxed)) {
-        for (auto kern : {k_adamw<false>, k_adamw<true>}) {
+        for (auto kern : {k_adamw<false, false>, k_adamw<true, false>, k_adamw<false, true>,
+                          k_adamw<true, true>}) {
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  (int)kSmemBytes);
             if (e != cudaSuccess)
@@ -175,14 +176,18 @@ cudaError_t launch_adamw(const AdamwArgs& a, cudaStream_t s)
         }
         configured[dev & 63].store(true, std::memory_order_relaxed);
     }
+    const bool ef = adamw_evict_first(a.psi_padded, 30);
     const uint64_t chunks = a.psi / kChunk;
     const uint64_t tail_blocks = (a.psi_padded - chunks * kChunk + kBlock - 1) / kBlock;
     const uint64_t want = chunks > tail_blocks ? chunks : tail_blocks;
     const uint64_t cap = (uint64_t)sm_count();  // one 192 KiB block per SM
     const unsigned grid = (unsigned)(want < cap ? want : cap);
     const dim3 g(grid > 0 ? grid : 1), b(kBlock);
-    return a.out_f16 ? launch_pdl(k_adamw<true>, g, b, kSmemBytes, s, a)
-                     : launch_pdl(k_adamw<false>, g, b, kSmemBytes, s, a);
+    if (ef)
+        return a.out_f16 ? launch_pdl(k_adamw<true, true>, g, b, kSmemBytes, s, a)
+                         : launch_pdl(k_adamw<false, true>, g, b, kSmemBytes, s, a);
+    return a.out_f16 ? launch_pdl(k_adamw<true, false>, g, b, kSmemBytes, s, a)
+                     : launch_pdl(k_adamw<false, false>, g, b, kSmemBytes, s, a);
 }
 
 }  // namespace zero

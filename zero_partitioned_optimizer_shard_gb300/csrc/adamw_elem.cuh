@@ -73,27 +73,32 @@ __device__ __forceinline__ uint32_t wait_parity_bounded(uint32_t bar, uint32_t p
     }
 }
 
-/* An L2 cache policy that marks what it covers as first to evict.  Every byte the AdamW
- * passes bulk-copy in is read exactly once, so their loads carry it: L2 then keeps the
- * lines being written (master, m, v and the parameters leave through L2) in preference
- * to inputs already consumed.  Measured on the GPT-2-1.5B buffer: k_adamw 6.87 -> 6.68 ms
- * (1.00 -> 1.03 of the copy peak), and the next step's reduce 4.54 -> 4.38 ms. */
-__device__ __forceinline__ uint64_t l2_evict_first_policy()
-{
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-
 /* One bulk copy global -> shared (`bytes` a multiple of 16, both addresses 16-byte
- * aligned), completing on the mbarrier at shared address `bar`, under L2 policy `pol`. */
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
-                                          uint64_t pol)
+ * aligned), completing on the mbarrier at shared address `bar`.  With EvictFirst the copy
+ * carries an L2 policy that marks what it brings in as first to evict: every byte the
+ * AdamW passes read is read exactly once, so on buffers many times larger than L2 it then
+ * keeps the lines being written (master, m, v and the parameters leave through L2) in
+ * preference to inputs already consumed.  Measured on the GPT-2-1.5B buffer: k_adamw
+ * 6.87 -> 6.68 ms (1.00 -> 1.03 of the copy peak), and the next step's reduce 4.54 ->
+ * 4.38 ms; on buffers of 2^22-2^25 parameters the same policy cost 1-3%, so the launchers
+ * pick the kernel by size (adamw_evict_first).  A compile-time choice: a run-time flag
+ * tested in the copy-issuing path cost ~2 us per step by itself. */
+template <bool EvictFirst>
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
 {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
-                 "[%0], [%1], %2, [%3], %4;"
-                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(pol)
-                 : "memory");
+    if constexpr (EvictFirst) {
+        uint64_t pol;
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+                     "[%0], [%1], %2, [%3], %4;"
+                     ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+                     : "memory");
+    } else {
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+                     "[%0], [%1], %2, [%3];"
+                     ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+                     : "memory");
+    }
 }
 
 constexpr int kChunk = 4096;  // elements per bulk-copied chunk of each array

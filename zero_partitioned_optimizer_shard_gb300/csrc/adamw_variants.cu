@@ -35,7 +35,7 @@ __device__ __forceinline__ float regather(uint16_t x0, uint16_t x1, float inv)
     return __fmul_rn(__fadd_rn(__fadd_rn(0.0f, grad_value<DT>(x0)), grad_value<DT>(x1)), inv);
 }
 
-template <zero_dtype_t DT, bool F16>
+template <zero_dtype_t DT, bool F16, bool EF>
 __global__ void __launch_bounds__(kBlock, 1) k_adamw_rereduce(const __grid_constant__ AdamwArgs a)
 {
     extern __shared__ __align__(128) float ring[];  // kStages x {x0|x1, master, m, v} x kChunk
@@ -84,9 +84,8 @@ __global__ void __launch_bounds__(kBlock, 1) k_adamw_rereduce(const __grid_const
         const uint32_t bytes[5] = {kChunk * 2, kChunk * 2, kChunk * 4, kChunk * 4, kChunk * 4};
         float* dst[5] = {stage, stage + kChunk / 2, stage + kChunk, stage + 2 * kChunk,
                          stage + 3 * kChunk};
-        const uint64_t pol = l2_evict_first_policy();
         for (int q = 0; q < 5; ++q)
-            bulk_load(smem_addr(dst[q]), src[q], bytes[q], bar, pol);
+            bulk_load<EF>(smem_addr(dst[q]), src[q], bytes[q], bar);
     };
     if (threadIdx.x == 0)
         for (uint64_t i = 0; i < mine && i < kStages; ++i)
@@ -239,14 +238,26 @@ __global__ void __launch_bounds__(kBlock) k_adamw_host_state(const __grid_consta
 
 }  // namespace
 
+template <bool EF>
+cudaError_t launch_rereduce_ef(const AdamwArgs& a, dim3 g, dim3 b, cudaStream_t s)
+{
+    if (a.grad_f16)
+        return a.out_f16 ? launch_pdl(k_adamw_rereduce<ZERO_F16, true, EF>, g, b, kSmemBytes, s, a)
+                         : launch_pdl(k_adamw_rereduce<ZERO_F16, false, EF>, g, b, kSmemBytes, s, a);
+    return a.out_f16 ? launch_pdl(k_adamw_rereduce<ZERO_BF16, true, EF>, g, b, kSmemBytes, s, a)
+                     : launch_pdl(k_adamw_rereduce<ZERO_BF16, false, EF>, g, b, kSmemBytes, s, a);
+}
+
 cudaError_t launch_adamw_rereduce(const AdamwArgs& a, cudaStream_t s)
 {
     static std::atomic<bool> configured[64];  // per device; a race only repeats the set-up
     int dev = 0;
     cudaGetDevice(&dev);
     if (!configured[dev & 63].load(std::memory_order_relaxed)) {
-        for (auto kern : {k_adamw_rereduce<ZERO_BF16, false>, k_adamw_rereduce<ZERO_BF16, true>,
-                          k_adamw_rereduce<ZERO_F16, false>, k_adamw_rereduce<ZERO_F16, true>}) {
+        for (auto kern : {k_adamw_rereduce<ZERO_BF16, false, false>, k_adamw_rereduce<ZERO_BF16, true, false>,
+                          k_adamw_rereduce<ZERO_F16, false, false>, k_adamw_rereduce<ZERO_F16, true, false>,
+                          k_adamw_rereduce<ZERO_BF16, false, true>, k_adamw_rereduce<ZERO_BF16, true, true>,
+                          k_adamw_rereduce<ZERO_F16, false, true>, k_adamw_rereduce<ZERO_F16, true, true>}) {
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  (int)kSmemBytes);
             if (e != cudaSuccess)
@@ -259,11 +270,8 @@ cudaError_t launch_adamw_rereduce(const AdamwArgs& a, cudaStream_t s)
     const uint64_t want = chunks > tail_blocks ? chunks : tail_blocks;
     const uint64_t cap = (uint64_t)sm_count();
     const dim3 g((unsigned)(want < cap ? (want > 0 ? want : 1) : cap)), b(kBlock);
-    if (a.grad_f16)
-        return a.out_f16 ? launch_pdl(k_adamw_rereduce<ZERO_F16, true>, g, b, kSmemBytes, s, a)
-                         : launch_pdl(k_adamw_rereduce<ZERO_F16, false>, g, b, kSmemBytes, s, a);
-    return a.out_f16 ? launch_pdl(k_adamw_rereduce<ZERO_BF16, true>, g, b, kSmemBytes, s, a)
-                     : launch_pdl(k_adamw_rereduce<ZERO_BF16, false>, g, b, kSmemBytes, s, a);
+    return adamw_evict_first(a.psi_padded, 30) ? launch_rereduce_ef<true>(a, g, b, s)
+                                               : launch_rereduce_ef<false>(a, g, b, s);
 }
 
 cudaError_t launch_adamw_host_state(const AdamwArgs& a, cudaStream_t s)

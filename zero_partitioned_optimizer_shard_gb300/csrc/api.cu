@@ -6,6 +6,7 @@
  */
 #include "zero_internal.h"
 
+#include <atomic>
 #include <mutex>
 #include <stddef.h>
 #include <string.h>
@@ -137,6 +138,7 @@ int adamw(const zero_layout_t* L, const zero_adamw_hparams_t* hp, const float* g
           bool host_state = false)
 {
     AdamwArgs a;
+    memset(&a, 0, sizeof a);
     a.g = g;
     a.master = master;
     a.m = m;
@@ -218,6 +220,21 @@ int sm_count()
         count[dev & 63] = n > 0 ? n : 1;
     }
     return count[dev & 63];
+}
+
+bool adamw_evict_first(uint64_t n, uint64_t bytes_per_elem)
+{
+    static std::atomic<long long> l2[64];  // per device; a race only repeats the query
+    int dev = 0;
+    cudaGetDevice(&dev);
+    long long bytes = l2[dev & 63].load(std::memory_order_relaxed);
+    if (bytes == 0) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev);
+        bytes = v > 0 ? v : 1;
+        l2[dev & 63].store(bytes, std::memory_order_relaxed);
+    }
+    return n * bytes_per_elem >= 16ull * (uint64_t)bytes;
 }
 
 }  // namespace zero
