@@ -57,7 +57,8 @@ class ClockSampler:
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "clocks.mem,temperature.gpu")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -103,12 +104,16 @@ class ClockSampler:
         sm = [float(r[1]) for r in rows if len(r) > 8 and r[1].replace(".", "").isdigit()]
         mx = [float(r[2]) for r in rows if len(r) > 8 and r[2].replace(".", "").isdigit()]
         pw = [float(r[3]) for r in rows if len(r) > 8 and r[3].replace(".", "").isdigit()]
+        mem = [float(r[9]) for r in rows if len(r) > 10 and r[9].replace(".", "").isdigit()]
+        temp = [float(r[10]) for r in rows if len(r) > 10 and r[10].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows if len(r) > 8 for i in range(4)
                           if r[5 + i].lower().startswith("active")})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None,
                 "power_w_max": max(pw) if pw else None,
+                "mem_mhz": statistics.median(mem) if mem else None,
+                "temp_c_max": max(temp) if temp else None,
                 "samples": len(rows), "reasons": reasons}
 
 
