@@ -86,9 +86,8 @@ class Exchange:
             fh = torch.empty(full.numel(), dtype=full.dtype)
             dist.all_gather_into_tensor(fh, part.cpu(), group=self.group)
             full.copy_(fh)
-        elif self.nccl:
-            dist.all_gather_into_tensor(full, part, group=self.group)  # in place
         else:
+            # the input is a copy of this process's part, never a view into the output
             dist.all_gather_into_tensor(full, part.clone(), group=self.group)
 
     def maximum(self, t: torch.Tensor) -> None:
