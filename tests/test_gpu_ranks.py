@@ -162,3 +162,33 @@ def test_ranks_over_processes_equal_the_one_gpu_step(world, wl, bucket):
     full["out"] = got[0][2][-1][1]
     assert_state_close(full, orc.arrays(), wl.psi, exact_expected=False)
     ref.check_guards()
+
+
+def test_rank_step_refuses_wrong_gradient_copies():
+    """RankStep hands the library raw addresses, so it checks the copies first: a copy of
+    the wrong length or element size is refused before anything is enqueued."""
+    import datetime
+    import torch.distributed as dist
+
+    import zero_partitioned_optimizer_shard_gb300 as z
+    from zero_partitioned_optimizer_shard_gb300.ranks import RankStep, layout_for
+
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(_free_port())
+    dist.init_process_group("gloo", rank=0, world_size=1, timeout=datetime.timedelta(seconds=30))
+    try:
+        lay = layout_for(100_000, 4)
+        dev = torch.device("cuda", 0)
+        rs = RankStep(lay, z.hparams(), z.ZERO_BF16, device=dev)
+        P = lay.psi_padded
+        good = [torch.zeros(P, dtype=torch.int16, device=dev) for _ in range(4)]
+        for bad in ([torch.zeros(P - 8, dtype=torch.int16, device=dev)] + good[1:],
+                    [torch.zeros(P, dtype=torch.float32, device=dev)] + good[1:],
+                    good[:3]):
+            with pytest.raises(ValueError):
+                rs.step(bad)
+        rs.step(good)  # all-zero gradients: a valid step
+        s = z.zero_step_state_read(rs.st)
+        assert s.t == 1 and s.norm == 0.0 and s.error == 0
+    finally:
+        dist.destroy_process_group()

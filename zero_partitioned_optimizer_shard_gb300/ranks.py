@@ -167,6 +167,11 @@ class RankStep:
         lay, R = self.lay, self.rank_count
         if len(copies) != R:
             raise ValueError(f"expected {R} gradient copies, got {len(copies)}")
+        for c in copies:  # the kernels read them through raw addresses: check before
+            if (not c.is_cuda or c.device != self.dev or c.element_size() != 2
+                    or c.numel() != lay.psi_padded or not c.is_contiguous()):
+                raise ValueError("each gradient copy must be a contiguous 16-bit tensor of "
+                                 f"psi_padded = {lay.psi_padded} elements on {self.dev}")
         s = torch.cuda.current_stream(self.dev)
         # 1. every rank's copy of this process's range
         mark = mark or (lambda name: None)
