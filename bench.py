@@ -504,7 +504,10 @@ def run_ranks(args):
     wl = base if args.psi in (None, base.psi) else W.scaled(base, args.psi)
     if wl.n_ranks % ws:
         raise SystemExit(f"{wl.n_ranks} ranks cannot be spread evenly over {ws} processes")
-    lay = layout_for(wl.psi, wl.n_ranks, wl.stage, wl.bucket_elems)
+    # the gradient exchange goes bucket by bucket (the next bucket's all-to-all overlapping
+    # this bucket's reduce, constant-size receive buffers): the workload's buckets, or
+    # 2^27-element ones for a workload defined without
+    lay = layout_for(wl.psi, wl.n_ranks, wl.stage, wl.bucket_elems or (1 << 27))
     P, N = lay.psi_padded, lay.n_ranks
     gdt = z.ZERO_F16 if wl.grad_dtype == "f16" else z.ZERO_BF16
     rs = RankStep(lay, z.hparams(**wl.hp.__dict__), gdt, wl.loss_scale, wl.dynamic,
@@ -543,7 +546,7 @@ def run_ranks(args):
     elapsed_ms = float(elapsed.item())
 
     # per-part breakdown: more steps with an event after each part (max over ranks)
-    names = ["gradients", "reduce", "norm inputs", "norm", "adamw", "parameters"]
+    names = ["gradients", "norm inputs", "norm", "adamw", "parameters"]
     n_split = min(args.steps, 10)
     parts = {n: [] for n in names}
     for _ in range(n_split):
@@ -589,8 +592,8 @@ def run_ranks(args):
                "d2h_bytes_per_step": ws * z.STATE_BYTES, "steps": n_e2e,
                "ms_per_step": float(dt.item()) / n_e2e * 1e3,
                "path": "every process: its gradient copies from pinned host memory, RankStep "
-                       "(all-to-all, local reduce, norm exchange, norm, local AdamW, parameter "
-                       "all-gather), step state read back"}
+                       "(per-bucket all-to-all overlapped with the local reduce, norm exchange, "
+                       "norm, local AdamW, parameter all-gather), step state read back"}
     peak, peak_kind = _peaks()
     ms = elapsed_ms / args.steps
     L = rs.local_len
@@ -601,9 +604,10 @@ def run_ranks(args):
         "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": _config({"parallelism": f"{ws} GPUs x {rs.rank_count} of the {N} ZeRO ranks "
-                                          f"each ({args.dist_backend}: all-to-all of the 16-bit "
-                                          "gradient copies, all-gather of tile partials and "
-                                          "parameters, max of the overflow flag)"},
+                                          f"each ({args.dist_backend}: per-bucket all-to-all of "
+                                          "the 16-bit gradient copies, all-gather of tile "
+                                          "partials and parameters, max of the overflow flag)",
+                           "exchange_bucket_elems": lay.bucket_elems},
                           psi=wl.psi, base=base),
         "roofline": {"kernel": "k_adamw on this process's ranks (zero_adamw_cast_gather_local)",
                      "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",

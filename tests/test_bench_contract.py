@@ -84,7 +84,6 @@ def test_rank_path_under_torchrun_two_processes_on_one_gpu():
     assert len(lines) == 1
     line = lines[0]
     assert line["n_gpus"] == 2 and line["scaling"] == "strong" and line["value"] > 0
-    assert set(line["parts_ms"]) == {"gradients", "reduce", "norm inputs", "norm", "adamw",
-                                     "parameters"}
+    assert set(line["parts_ms"]) == {"gradients", "norm inputs", "norm", "adamw", "parameters"}
     assert line["final_state"]["t"] == 3 + 3 + 3  # warm-up, timed and breakdown steps
     assert line["e2e"]["value"] > 0 and line["gpu_launches"] == 3 * 3

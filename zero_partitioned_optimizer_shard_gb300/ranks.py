@@ -12,8 +12,14 @@ zero_reduce_shard_unscale_local, zero_grad_norm and zero_adamw_cast_gather_local
 module only moves data between processes with torch.distributed (NCCL on the device
 buffers; gloo through host memory):
 
-  1. gradients   one all-to-all of equal chunks per local gradient copy: process q
-                 receives every rank's copy of its own flat range, in rank order;
+  1. gradients   bucket by bucket (the layout's bucket grid, "【论文解读】ZeRO" sec. 4(2):
+                 gradients are reduced in buckets at the partition boundaries), one
+                 all-to-all per local gradient copy: the bucket's flat slice of a copy
+                 already lies in destination order, since every process's range is
+                 contiguous, so it is sent as it is with one split per process, and each
+                 process receives every rank's copy of its part of the bucket into a
+                 constant-size buffer (sec. 5(2), constant-size buffers); the exchange of
+                 the next bucket is issued before this bucket's reduce;
   2. norm        all-gather of every process's tile partials (fp64, a few bytes per 8192
                  parameters) and a maximum over processes of the step state's overflow
                  word; each process then forms the same norm, clip coefficient, scaler
@@ -48,12 +54,32 @@ def local_ranks(n_ranks: int, world: int, proc: int) -> tuple[int, int]:
     return proc * count, count
 
 
+class _Done:
+    def wait(self) -> None:
+        pass
+
+
+class _Pending:
+    """An exchange in flight: wait() completes it (and, for host-staged tensors, copies the
+    result into the device tensor)."""
+
+    def __init__(self, work, out=None, host=None):
+        self.work, self.out, self.host = work, out, host
+
+    def wait(self) -> None:
+        if self.work is not None:
+            self.work.wait()
+        if self.host is not None:
+            self.out.copy_(self.host)
+
+
 class Exchange:
     """The step's collectives over torch.distributed, on tensors of any device.
 
-    With NCCL the collectives run on the device tensors themselves.  With another backend
-    (gloo), device tensors are copied to host memory, exchanged there and copied back;
-    host tensors are exchanged directly.
+    With NCCL the collectives run on the device tensors themselves, ordered after the
+    work already enqueued on the current stream, and wait() makes the current stream wait
+    for them.  With another backend (gloo), device tensors are copied to host memory,
+    exchanged there and copied back; host tensors are exchanged directly.
     """
 
     def __init__(self, group=None):
@@ -65,16 +91,28 @@ class Exchange:
     def _host(self, t: torch.Tensor) -> bool:
         return t.is_cuda and not self.nccl
 
-    def all_to_all(self, out: torch.Tensor, inp: torch.Tensor) -> None:
-        """Chunk q of `inp` goes to process q; chunk q of `out` comes from process q
-        (world equal chunks each, as bytes)."""
+    def all_to_all(self, out: torch.Tensor, inp: torch.Tensor, out_splits=None, in_splits=None,
+                   async_op: bool = False):
+        """Part q of `inp` goes to process q; part q of `out` comes from process q.  Parts
+        are equal unless split sizes (in elements of the tensors' type) are given.  Returns
+        a handle whose wait() completes the exchange (already complete unless async_op)."""
         o, i = out.view(torch.uint8), inp.view(torch.uint8)
+        k = out.element_size()
+        os_ = None if out_splits is None else [k * x for x in out_splits]
+        is_ = None if in_splits is None else [k * x for x in in_splits]
         if self._host(o):
             oh = torch.empty(o.numel(), dtype=torch.uint8)
-            dist.all_to_all_single(oh, i.cpu(), group=self.group)
-            o.copy_(oh)
+            work = dist.all_to_all_single(oh, i.cpu(), output_split_sizes=os_, input_split_sizes=is_,
+                                          group=self.group, async_op=async_op)
+            pend = _Pending(work, o, oh)
         else:
-            dist.all_to_all_single(o, i, group=self.group)
+            work = dist.all_to_all_single(o, i, output_split_sizes=os_, input_split_sizes=is_,
+                                          group=self.group, async_op=async_op)
+            pend = _Pending(work)
+        if not async_op:
+            pend.wait()
+            return _Done()
+        return pend
 
     def all_gather(self, full: torch.Tensor, lo: int, hi: int) -> None:
         """Every process contributes full[lo:hi] (its own part, the same length on each);
@@ -107,7 +145,8 @@ class RankStep:
     fill them (e.g. from a checkpoint) before the first step.
 
     layout      from zero_partition with align = 8 (the local buffers start at flat
-                origin = rank_begin * S, which must be a multiple of 8)
+                origin = rank_begin * S, which must be a multiple of 8); its bucket size
+                sets the gradient exchange's granularity and the receive buffers' size
     dtype       ZERO_F16 or ZERO_BF16: the gradient copies' element type
     """
 
@@ -129,32 +168,57 @@ class RankStep:
         self.params_local = self.params[self.origin:self.origin + self.local_len]
         self.partials = torch.empty(layout.n_tiles, dtype=torch.float64, device=dev)
         self.st = torch.empty(STATE_BYTES, dtype=torch.uint8, device=dev)
-        # every rank's copy of this process's range arrives in these (one per local copy)
-        self.recv = [torch.empty(P, dtype=torch.int16, device=dev) for _ in range(self.rank_count)] \
+        self.buckets = self._buckets()
+        # every rank's copy of this process's part of a bucket arrives here: one buffer per
+        # local copy and slot (two slots: the next bucket's exchange overlaps this bucket's
+        # reduce), world * (this process's largest part of a bucket) elements each
+        self.slots = 2 if len(self.buckets) > 1 else 1
+        part = max(sizes[self.proc] for _, _, sizes in self.buckets)
+        self.recv = [[torch.empty(self.world * part, dtype=torch.int16, device=dev)
+                      for _ in range(self.rank_count)] for _ in range(self.slots)] \
             if self.world > 1 else []
         zero_step_state_init(layout, loss_scale, dynamic, growth_interval, self.st, self.partials)
 
-    def windows(self) -> list[tuple[int, int]]:
-        """The layout's reduce windows (its bucket grid) clipped to the local range."""
-        W, lo, hi = self.lay.bucket_elems, self.origin, self.origin + self.local_len
+    def _buckets(self) -> list[tuple[int, int, list[int]]]:
+        """(lo, hi, sizes) per bucket of the layout's grid: sizes[q] is the part of
+        [lo, hi) inside process q's range (the ranges are contiguous and in order, so the
+        parts follow each other)."""
+        W, P, L = self.lay.bucket_elems, self.lay.psi_padded, self.local_len
         out = []
-        b = lo // W
-        while b * W < hi:
-            begin, end = max(b * W, lo), min((b + 1) * W, hi)
-            out.append((begin, end - begin))
-            b += 1
+        for b in range(self.lay.n_buckets):
+            lo, hi = b * W, min((b + 1) * W, P)
+            sizes = [max(0, min(hi, (q + 1) * L) - max(lo, q * L)) for q in range(self.world)]
+            out.append((lo, hi, sizes))
         return out
 
-    def sources(self, copies: Sequence[torch.Tensor]) -> list[int]:
-        """Device address of flat `origin` in rank k's gradient copy, k = 0 .. N-1."""
-        R, L = self.rank_count, self.local_len
+    def windows(self) -> list[tuple[int, int]]:
+        """The layout's reduce windows (its bucket grid) clipped to the local range."""
+        lo_r = self.origin
+        return [(max(lo, lo_r), sizes[self.proc]) for lo, _, sizes in self.buckets
+                if sizes[self.proc] > 0]
+
+    def _issue(self, b: int, copies: Sequence[torch.Tensor]) -> list:
+        lo, hi, sizes = self.buckets[b]
+        n = sizes[self.proc]
+        recv = self.recv[b % self.slots]
+        return [self.ex.all_to_all(recv[j][:self.world * n], copies[j][lo:hi],
+                                   out_splits=[n] * self.world, in_splits=sizes, async_op=True)
+                for j in range(self.rank_count)]
+
+    def _sources(self, b: int, copies: Sequence[torch.Tensor]) -> list[int]:
+        """Device address, for rank k = 0 .. N-1, of the first element of this process's
+        part of bucket b in rank k's copy."""
+        lo, _, sizes = self.buckets[b]
+        R, n = self.rank_count, sizes[self.proc]
+        begin = max(lo, self.origin)
+        recv = self.recv[b % self.slots] if self.world > 1 else None
         out = []
         for k in range(self.lay.n_ranks):
             q, j = divmod(k, R)
             if q == self.proc:
-                out.append(copies[j].data_ptr() + 2 * self.origin)
+                out.append(copies[j].data_ptr() + 2 * begin)
             else:
-                out.append(self.recv[j].data_ptr() + 2 * q * L)
+                out.append(recv[j].data_ptr() + 2 * q * n)
         return out
 
     def step(self, copies: Sequence[torch.Tensor], mark=None) -> None:
@@ -162,8 +226,9 @@ class RankStep:
         collectives against).  copies: this process's rank_count gradient copies (ranks
         rank_begin, rank_begin+1, ... in order), psi_padded 16-bit elements each, on the
         device; their padding elements are ignored.  mark: optional callable, called with
-        the name of each part as it has been enqueued ("gradients", "reduce", "norm
-        inputs", "norm", "adamw", "parameters"), e.g. to record timing events."""
+        the name of each part as it has been enqueued ("gradients", "norm inputs",
+        "norm", "adamw", "parameters"; "gradients" is the exchange and the reduce of every
+        bucket, which overlap), e.g. to record timing events."""
         lay, R = self.lay, self.rank_count
         if len(copies) != R:
             raise ValueError(f"expected {R} gradient copies, got {len(copies)}")
@@ -173,18 +238,27 @@ class RankStep:
                 raise ValueError("each gradient copy must be a contiguous 16-bit tensor of "
                                  f"psi_padded = {lay.psi_padded} elements on {self.dev}")
         s = torch.cuda.current_stream(self.dev)
-        # 1. every rank's copy of this process's range
         mark = mark or (lambda name: None)
-        for j in range(R if self.world > 1 else 0):
-            self.ex.all_to_all(self.recv[j], copies[j])
+        # 1. bucket by bucket: every rank's copy of this process's part arrives, then the
+        #    reduce; bucket b+2's exchange reuses b's slot once b's reduce is enqueued (the
+        #    exchange is ordered after the work already on the stream)
+        nb = len(self.buckets)
+        pending = {}
+        if self.world > 1:
+            for b in range(min(self.slots, nb)):
+                pending[b] = self._issue(b, copies)
+        for b in range(nb):
+            for h in pending.pop(b, []):
+                h.wait()
+            lo, _, sizes = self.buckets[b]
+            n = sizes[self.proc]
+            if n > 0:
+                zero_reduce_shard_unscale_local(lay, self.dtype, self.rank_begin, R,
+                                                self._sources(b, copies), max(lo, self.origin),
+                                                n, self.g, self.partials, self.st, s)
+            if self.world > 1 and b + self.slots < nb:
+                pending[b + self.slots] = self._issue(b + self.slots, copies)
         mark("gradients")
-        src = self.sources(copies)
-        for begin, count in self.windows():
-            off = 2 * (begin - self.origin)
-            zero_reduce_shard_unscale_local(lay, self.dtype, self.rank_begin, R,
-                                            [p + off for p in src], begin, count, self.g,
-                                            self.partials, self.st, s)
-        mark("reduce")
         # 2. the global norm's inputs: every process's tile partials and overflow flag
         if self.world > 1:
             tpr = lay.tiles_per_rank
