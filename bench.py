@@ -504,14 +504,13 @@ def run_ranks(args):
     wl = base if args.psi in (None, base.psi) else W.scaled(base, args.psi)
     if wl.n_ranks % ws:
         raise SystemExit(f"{wl.n_ranks} ranks cannot be spread evenly over {ws} processes")
-    # the gradient exchange goes bucket by bucket (the next bucket's all-to-all overlapping
-    # this bucket's reduce, constant-size receive buffers): the workload's buckets, or
-    # 2^27-element ones for a workload defined without
-    lay = layout_for(wl.psi, wl.n_ranks, wl.stage, wl.bucket_elems or (1 << 27))
+    # the gradient exchange goes in 2^24-element windows of every process's range (the next
+    # windows' exchanges overlapping this window's reduce, constant-size receive buffers)
+    lay = layout_for(wl.psi, wl.n_ranks, wl.stage, wl.bucket_elems)
     P, N = lay.psi_padded, lay.n_ranks
     gdt = z.ZERO_F16 if wl.grad_dtype == "f16" else z.ZERO_BF16
     rs = RankStep(lay, z.hparams(**wl.hp.__dict__), gdt, wl.loss_scale, wl.dynamic,
-                  wl.growth_interval, dev)
+                  wl.growth_interval, dev, exchange_elems=1 << 24)
     stream = torch.cuda.current_stream(dev)
     s = stream.cuda_stream
     fills = [(rs.master, synth.ROLE_MASTER, synth.NORMAL, wl.master_sigma)]
@@ -592,8 +591,8 @@ def run_ranks(args):
                "d2h_bytes_per_step": ws * z.STATE_BYTES, "steps": n_e2e,
                "ms_per_step": float(dt.item()) / n_e2e * 1e3,
                "path": "every process: its gradient copies from pinned host memory, RankStep "
-                       "(per-bucket all-to-all overlapped with the local reduce, norm exchange, "
-                       "norm, local AdamW, parameter all-gather), step state read back"}
+                       "(gradient windows exchanged while the previous ones are reduced, norm "
+                       "exchange, norm, local AdamW, parameter all-gather), step state read back"}
     peak, peak_kind = _peaks()
     ms = elapsed_ms / args.steps
     L = rs.local_len
@@ -604,10 +603,10 @@ def run_ranks(args):
         "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": _config({"parallelism": f"{ws} GPUs x {rs.rank_count} of the {N} ZeRO ranks "
-                                          f"each ({args.dist_backend}: per-bucket all-to-all of "
-                                          "the 16-bit gradient copies, all-gather of tile "
+                                          f"each ({args.dist_backend}: the 16-bit gradient "
+                                          "copies exchanged window by window, all-gather of tile "
                                           "partials and parameters, max of the overflow flag)",
-                           "exchange_bucket_elems": lay.bucket_elems},
+                           "exchange_window_elems": 1 << 24},
                           psi=wl.psi, base=base),
         "roofline": {"kernel": "k_adamw on this process's ranks (zero_adamw_cast_gather_local)",
                      "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",

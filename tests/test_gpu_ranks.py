@@ -60,7 +60,7 @@ def _proc_main(proc, world, port, wl, bucket, out_q):
         lay = layout_for(wl.psi, wl.n_ranks, wl.stage, bucket)
         dt = z.ZERO_F16 if wl.grad_dtype == "f16" else z.ZERO_BF16
         rs = RankStep(lay, z.hparams(**wl.hp.__dict__), dt, wl.loss_scale, wl.dynamic,
-                      wl.growth_interval, dev)
+                      wl.growth_interval, dev, exchange_elems=bucket)
         fills = [(rs.master, synth.ROLE_MASTER, synth.NORMAL, wl.master_sigma)]
         if wl.random_moments:
             fills += [(rs.m, synth.ROLE_MOM, synth.NORMAL, wl.mom_sigma),
@@ -100,10 +100,14 @@ C5_SMALL = replace(W.scaled(W.C5, 3 * 8192 * 4 + 1001, steps=5), n_ranks=4, inje
     # fp16 with a dynamic loss scale, two ranks per process: rank 3's copy overflows on
     # every second step (in process 1's range), so both processes must skip that step
     (2, C5_SMALL, 0),
-    # four processes of two ranks each, 2^16-element reduce windows that cut tiles
+    # four processes of two ranks each: 2^16-element buckets on the one GPU, 2^16-element
+    # exchange windows across the processes (4 windows each)
     (4, replace(W.scaled(W.C2, 8 * 3 * 8192 + 4099, steps=3), n_ranks=8), 1 << 16),
     # a larger buffer: 4.2M parameters, two processes of four ranks, 2^20-element windows
     (2, replace(W.scaled(W.C2, (1 << 22) + 13, steps=2), n_ranks=8), 1 << 20),
+    # windows of 8192 elements: the processes hold different numbers of windows (their
+    # ranges start at different places of the grid), some exchanges are one-sided
+    (2, replace(W.scaled(W.C2, 48_761, steps=2), n_ranks=2), 8192),
     # 13 parameters over 4 ranks of 8 (align 8): process 1 holds only padding
     (2, replace(W.scaled(W.C2, 13, steps=2), n_ranks=4), 0),
     # fp16 gathered parameters

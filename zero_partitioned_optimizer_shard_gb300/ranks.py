@@ -12,14 +12,16 @@ zero_reduce_shard_unscale_local, zero_grad_norm and zero_adamw_cast_gather_local
 module only moves data between processes with torch.distributed (NCCL on the device
 buffers; gloo through host memory):
 
-  1. gradients   bucket by bucket (the layout's bucket grid, "【论文解读】ZeRO" sec. 4(2):
-                 gradients are reduced in buckets at the partition boundaries), one
-                 all-to-all per local gradient copy: the bucket's flat slice of a copy
-                 already lies in destination order, since every process's range is
-                 contiguous, so it is sent as it is with one split per process, and each
-                 process receives every rank's copy of its part of the bucket into a
-                 constant-size buffer (sec. 5(2), constant-size buffers); the exchange of
-                 the next bucket is issued before this bucket's reduce;
+  1. gradients   window by window ("【论文解读】ZeRO" sec. 4(2): gradients are reduced in
+                 buckets at the partition boundaries): every process's range is cut on one
+                 flat grid of w elements, and at exchange k each process receives its k-th
+                 window from every other process (point-to-point sends of the flat slice
+                 of each local gradient copy), so every process sends and receives alike;
+                 the windows land in two constant-size receive slots (sec. 5(2),
+                 constant-size buffers), and the exchanges of the next windows are in
+                 flight while this one is reduced.  w is a multiple of the 8192-element
+                 tile grid, so no tile of the sums of squares is split between windows and
+                 the result does not depend on w;
   2. norm        all-gather of every process's tile partials (fp64, a few bytes per 8192
                  parameters) and a maximum over processes of the step state's overflow
                  word; each process then forms the same norm, clip coefficient, scaler
@@ -60,17 +62,18 @@ class _Done:
 
 
 class _Pending:
-    """An exchange in flight: wait() completes it (and, for host-staged tensors, copies the
-    result into the device tensor)."""
+    """Exchanges in flight: wait() completes them (and, for host-staged tensors, copies
+    the results into the device tensors)."""
 
-    def __init__(self, work, out=None, host=None):
-        self.work, self.out, self.host = work, out, host
+    def __init__(self, works, copies=()):
+        self.works, self.copies = list(works), list(copies)
 
     def wait(self) -> None:
-        if self.work is not None:
-            self.work.wait()
-        if self.host is not None:
-            self.out.copy_(self.host)
+        for w in self.works:
+            if w is not None:
+                w.wait()
+        for dst, src in self.copies:
+            dst.copy_(src)
 
 
 class Exchange:
@@ -104,15 +107,34 @@ class Exchange:
             oh = torch.empty(o.numel(), dtype=torch.uint8)
             work = dist.all_to_all_single(oh, i.cpu(), output_split_sizes=os_, input_split_sizes=is_,
                                           group=self.group, async_op=async_op)
-            pend = _Pending(work, o, oh)
+            pend = _Pending([work], [(o, oh)])
         else:
             work = dist.all_to_all_single(o, i, output_split_sizes=os_, input_split_sizes=is_,
                                           group=self.group, async_op=async_op)
-            pend = _Pending(work)
+            pend = _Pending([work])
         if not async_op:
             pend.wait()
             return _Done()
         return pend
+
+    def send_recv(self, sends, recvs):
+        """Point-to-point: sends and recvs are lists of (peer, tensor); messages between
+        two processes are matched in the order they are listed.  Asynchronous: returns a
+        handle whose wait() completes them all."""
+        ops, copies = [], []
+        for peer, t in sends:
+            b = t.view(torch.uint8)
+            ops.append(dist.P2POp(dist.isend, b.cpu() if self._host(b) else b, peer, self.group))
+        for peer, t in recvs:
+            b = t.view(torch.uint8)
+            if self._host(b):
+                h = torch.empty(b.numel(), dtype=torch.uint8)
+                copies.append((b, h))
+                b = h
+            ops.append(dist.P2POp(dist.irecv, b, peer, self.group))
+        if not ops:
+            return _Done()
+        return _Pending(dist.batch_isend_irecv(ops), copies)
 
     def all_gather(self, full: torch.Tensor, lo: int, hi: int) -> None:
         """Every process contributes full[lo:hi] (its own part, the same length on each);
@@ -144,14 +166,19 @@ class RankStep:
     full tile partials and the step state, all on `device`.  The state arrays start at 0;
     fill them (e.g. from a checkpoint) before the first step.
 
-    layout      from zero_partition with align = 8 (the local buffers start at flat
-                origin = rank_begin * S, which must be a multiple of 8); its bucket size
-                sets the gradient exchange's granularity and the receive buffers' size
-    dtype       ZERO_F16 or ZERO_BF16: the gradient copies' element type
+    layout          from zero_partition with align = 8 (the local buffers start at flat
+                    origin = rank_begin * S, which must be a multiple of 8)
+    dtype           ZERO_F16 or ZERO_BF16: the gradient copies' element type
+    exchange_elems  w: the gradient exchange's window, a multiple of 8192 (the tile grid);
+                    0 = each process's whole range at once.  The receive buffers hold
+                    2 * world * w elements per local copy (world * range when w = 0).
+                    The result does not depend on w.
     """
 
     def __init__(self, layout, hp, dtype: int, loss_scale: float = 1.0, dynamic: bool = False,
-                 growth_interval: int = 1000, device=None, group=None):
+                 growth_interval: int = 1000, device=None, group=None, exchange_elems: int = 0):
+        if exchange_elems < 0 or exchange_elems % 8192:
+            raise ValueError("exchange_elems must be a multiple of 8192 (or 0)")
         self.lay, self.hp, self.dtype = layout, hp, dtype
         self.ex = Exchange(group)
         self.world, self.proc = self.ex.world, self.ex.proc
@@ -168,57 +195,71 @@ class RankStep:
         self.params_local = self.params[self.origin:self.origin + self.local_len]
         self.partials = torch.empty(layout.n_tiles, dtype=torch.float64, device=dev)
         self.st = torch.empty(STATE_BYTES, dtype=torch.uint8, device=dev)
-        self.buckets = self._buckets()
-        # every rank's copy of this process's part of a bucket arrives here: one buffer per
-        # local copy and slot (two slots: the next bucket's exchange overlaps this bucket's
-        # reduce), world * (this process's largest part of a bucket) elements each
-        self.slots = 2 if len(self.buckets) > 1 else 1
-        part = max(sizes[self.proc] for _, _, sizes in self.buckets)
-        self.recv = [[torch.empty(self.world * part, dtype=torch.int16, device=dev)
+        self.windows_of = self._windows(exchange_elems)
+        self.n_exchanges = max(len(w) for w in self.windows_of)
+        # every rank's copy of one window of this process's range arrives here: per local
+        # copy and slot (two slots: the next windows' exchanges overlap this window's
+        # reduce), world * w elements, process q's part at q * w
+        self.slots = 2 if self.n_exchanges > 1 else 1
+        w_max = max((n for ws in self.windows_of for _, n in ws), default=0)
+        self.part = w_max
+        self.recv = [[torch.empty(self.world * w_max, dtype=torch.int16, device=dev)
                       for _ in range(self.rank_count)] for _ in range(self.slots)] \
             if self.world > 1 else []
         zero_step_state_init(layout, loss_scale, dynamic, growth_interval, self.st, self.partials)
 
-    def _buckets(self) -> list[tuple[int, int, list[int]]]:
-        """(lo, hi, sizes) per bucket of the layout's grid: sizes[q] is the part of
-        [lo, hi) inside process q's range (the ranges are contiguous and in order, so the
-        parts follow each other)."""
-        W, P, L = self.lay.bucket_elems, self.lay.psi_padded, self.local_len
+    def _windows(self, w: int) -> list[list[tuple[int, int]]]:
+        """For every process q, its range [q*L, (q+1)*L) cut at the flat multiples of w:
+        a list of (begin, count).  w = 0: the whole range in one window."""
+        L = self.local_len
         out = []
-        for b in range(self.lay.n_buckets):
-            lo, hi = b * W, min((b + 1) * W, P)
-            sizes = [max(0, min(hi, (q + 1) * L) - max(lo, q * L)) for q in range(self.world)]
-            out.append((lo, hi, sizes))
+        for q in range(self.world):
+            lo, hi = q * L, (q + 1) * L
+            if w == 0:
+                out.append([(lo, L)])
+                continue
+            ws, b = [], lo
+            while b < hi:
+                e = min((b // w + 1) * w, hi)
+                ws.append((b, e - b))
+                b = e
+            out.append(ws)
         return out
 
     def windows(self) -> list[tuple[int, int]]:
-        """The layout's reduce windows (its bucket grid) clipped to the local range."""
-        lo_r = self.origin
-        return [(max(lo, lo_r), sizes[self.proc]) for lo, _, sizes in self.buckets
-                if sizes[self.proc] > 0]
+        """This process's reduce windows (begin, count), in order."""
+        return self.windows_of[self.proc]
 
-    def _issue(self, b: int, copies: Sequence[torch.Tensor]) -> list:
-        lo, hi, sizes = self.buckets[b]
-        n = sizes[self.proc]
-        recv = self.recv[b % self.slots]
-        return [self.ex.all_to_all(recv[j][:self.world * n], copies[j][lo:hi],
-                                   out_splits=[n] * self.world, in_splits=sizes, async_op=True)
-                for j in range(self.rank_count)]
+    def _issue(self, k: int, copies: Sequence[torch.Tensor]):
+        """Exchange k: send every other process its k-th window of each local copy, and
+        receive this process's k-th window of every other process's copies."""
+        me, R = self.proc, self.rank_count
+        recv = self.recv[k % self.slots]
+        sends, recvs = [], []
+        for q in range(self.world):
+            if q == me:
+                continue
+            if k < len(self.windows_of[q]):
+                b, n = self.windows_of[q][k]
+                sends += [(q, copies[j][b:b + n]) for j in range(R)]
+            if k < len(self.windows_of[me]):
+                _, n = self.windows_of[me][k]
+                recvs += [(q, recv[j][q * self.part:q * self.part + n]) for j in range(R)]
+        return self.ex.send_recv(sends, recvs)
 
-    def _sources(self, b: int, copies: Sequence[torch.Tensor]) -> list[int]:
-        """Device address, for rank k = 0 .. N-1, of the first element of this process's
-        part of bucket b in rank k's copy."""
-        lo, _, sizes = self.buckets[b]
-        R, n = self.rank_count, sizes[self.proc]
-        begin = max(lo, self.origin)
-        recv = self.recv[b % self.slots] if self.world > 1 else None
+    def _sources(self, k: int, copies: Sequence[torch.Tensor]) -> list[int]:
+        """Device address, for rank i = 0 .. N-1, of the first element of this process's
+        window k in rank i's copy."""
+        b, _ = self.windows_of[self.proc][k]
+        R = self.rank_count
+        recv = self.recv[k % self.slots] if self.world > 1 else None
         out = []
-        for k in range(self.lay.n_ranks):
-            q, j = divmod(k, R)
+        for i in range(self.lay.n_ranks):
+            q, j = divmod(i, R)
             if q == self.proc:
-                out.append(copies[j].data_ptr() + 2 * begin)
+                out.append(copies[j].data_ptr() + 2 * b)
             else:
-                out.append(recv[j].data_ptr() + 2 * q * n)
+                out.append(recv[j].data_ptr() + 2 * q * self.part)
         return out
 
     def step(self, copies: Sequence[torch.Tensor], mark=None) -> None:
@@ -228,7 +269,7 @@ class RankStep:
         device; their padding elements are ignored.  mark: optional callable, called with
         the name of each part as it has been enqueued ("gradients", "norm inputs",
         "norm", "adamw", "parameters"; "gradients" is the exchange and the reduce of every
-        bucket, which overlap), e.g. to record timing events."""
+        window, which overlap), e.g. to record timing events."""
         lay, R = self.lay, self.rank_count
         if len(copies) != R:
             raise ValueError(f"expected {R} gradient copies, got {len(copies)}")
@@ -239,25 +280,25 @@ class RankStep:
                                  f"psi_padded = {lay.psi_padded} elements on {self.dev}")
         s = torch.cuda.current_stream(self.dev)
         mark = mark or (lambda name: None)
-        # 1. bucket by bucket: every rank's copy of this process's part arrives, then the
-        #    reduce; bucket b+2's exchange reuses b's slot once b's reduce is enqueued (the
-        #    exchange is ordered after the work already on the stream)
-        nb = len(self.buckets)
+        # 1. window by window: every rank's copy of this process's window arrives, then the
+        #    reduce; exchange k+2 reuses k's slot once k's reduce is enqueued (a collective
+        #    is ordered after the work already on the stream)
+        K = self.n_exchanges
+        mine = self.windows_of[self.proc]
         pending = {}
         if self.world > 1:
-            for b in range(min(self.slots, nb)):
-                pending[b] = self._issue(b, copies)
-        for b in range(nb):
-            for h in pending.pop(b, []):
-                h.wait()
-            lo, _, sizes = self.buckets[b]
-            n = sizes[self.proc]
-            if n > 0:
+            for k in range(min(self.slots, K)):
+                pending[k] = self._issue(k, copies)
+        for k in range(K):
+            if k in pending:
+                pending.pop(k).wait()
+            if k < len(mine):
+                begin, n = mine[k]
                 zero_reduce_shard_unscale_local(lay, self.dtype, self.rank_begin, R,
-                                                self._sources(b, copies), max(lo, self.origin),
-                                                n, self.g, self.partials, self.st, s)
-            if self.world > 1 and b + self.slots < nb:
-                pending[b + self.slots] = self._issue(b + self.slots, copies)
+                                                self._sources(k, copies), begin, n, self.g,
+                                                self.partials, self.st, s)
+            if self.world > 1 and k + self.slots < K:
+                pending[k + self.slots] = self._issue(k + self.slots, copies)
         mark("gradients")
         # 2. the global norm's inputs: every process's tile partials and overflow flag
         if self.world > 1:
