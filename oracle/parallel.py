@@ -118,29 +118,38 @@ class ParallelOracle:
         spec = {"rep": (np.uint16, N * P), "g": (np.float32, P), "master": (np.float32, P),
                 "m": (np.float32, P), "v": (np.float32, P), "out": (np.uint16, P)}
         self._shm = {}
-        names = {}
-        for key, (dtype, count) in spec.items():
-            shm = shared_memory.SharedMemory(create=True, size=max(1, count * np.dtype(dtype).itemsize))
-            self._shm[key] = shm
-            names[key] = (shm.name, dtype, count)
-        self.arrs = {k: np.ndarray((c,), dtype=d, buffer=self._shm[k].buf)
-                     for k, (d, c) in spec.items()}
-        self.arrs["out"][:] = 0
-        root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-        lay_args = (wl.psi, wl.n_ranks, wl.stage, 1, 0)
-        hp_args = tuple(getattr(self.hp, f) for f, _ in self.hp._fields_)
-        self.pool = mp.get_context("spawn").Pool(
-            self.procs, initializer=_init, initargs=(root, names, P, N, lay_args, hp_args, self.dtype))
-        grads = [(wl.grad_out, wl.grad_kind, wl.grad_key(1, k), wl.grad_sigma, wl.loss_scale)
-                 for k in range(N)]
-        states = [("master", synth.NORMAL, wl.state_key(synth.ROLE_MASTER), wl.master_sigma)]
-        if wl.random_moments:
-            states += [("m", synth.NORMAL, wl.state_key(synth.ROLE_MOM), wl.mom_sigma),
-                       ("v", synth.NORMAL_SQ, wl.state_key(synth.ROLE_VAR), wl.mom_sigma)]
-        else:
-            states += [("m", None, None, 0.0), ("v", None, None, 0.0)]
-        self.pool.map(_fill_job, [(b, min(CHUNK, P - b), grads, states) for b in range(0, P, CHUNK)],
-                      chunksize=1)
+        self.arrs = None
+        self.pool = None
+        try:
+            names = {}
+            for key, (dtype, count) in spec.items():
+                shm = shared_memory.SharedMemory(create=True,
+                                                 size=max(1, count * np.dtype(dtype).itemsize))
+                self._shm[key] = shm
+                names[key] = (shm.name, dtype, count)
+            self.arrs = {k: np.ndarray((c,), dtype=d, buffer=self._shm[k].buf)
+                         for k, (d, c) in spec.items()}
+            self.arrs["out"][:] = 0
+            root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+            lay_args = (wl.psi, wl.n_ranks, wl.stage, 1, 0)
+            hp_args = tuple(getattr(self.hp, f) for f, _ in self.hp._fields_)
+            self.pool = mp.get_context("spawn").Pool(
+                self.procs, initializer=_init,
+                initargs=(root, names, P, N, lay_args, hp_args, self.dtype))
+            grads = [(wl.grad_out, wl.grad_kind, wl.grad_key(1, k), wl.grad_sigma, wl.loss_scale)
+                     for k in range(N)]
+            states = [("master", synth.NORMAL, wl.state_key(synth.ROLE_MASTER), wl.master_sigma)]
+            if wl.random_moments:
+                states += [("m", synth.NORMAL, wl.state_key(synth.ROLE_MOM), wl.mom_sigma),
+                           ("v", synth.NORMAL_SQ, wl.state_key(synth.ROLE_VAR), wl.mom_sigma)]
+            else:
+                states += [("m", None, None, 0.0), ("v", None, None, 0.0)]
+            self.pool.map(_fill_job,
+                          [(b, min(CHUNK, P - b), grads, states) for b in range(0, P, CHUNK)],
+                          chunksize=1)
+        except BaseException:
+            self.close()  # no shared segment outlives a failed set-up
+            raise
 
     def _chunks(self, lo, hi):
         return [(b, min(CHUNK, hi - b)) for b in range(lo, hi, CHUNK)]
@@ -177,12 +186,15 @@ class ParallelOracle:
         return time.perf_counter() - t0
 
     def close(self) -> None:
-        self.pool.close()
-        self.pool.join()
+        if self.pool is not None:
+            self.pool.close()
+            self.pool.join()
+            self.pool = None
         self.arrs = None
         for shm in self._shm.values():
             shm.close()
             shm.unlink()
+        self._shm = {}
 
     def __enter__(self):
         return self
