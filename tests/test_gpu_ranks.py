@@ -196,3 +196,114 @@ def test_rank_step_refuses_wrong_gradient_copies():
         assert s.t == 1 and s.norm == 0.0 and s.error == 0
     finally:
         dist.destroy_process_group()
+
+
+def _full_main(proc, world, port, name, steps, starts, out_q):
+    """The full-size workload's step on this process's ranks; returns, per step, the step
+    state and the values at the sampled windows that fall in this process's range."""
+    import torch.distributed as dist
+
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=proc, world_size=world)
+    try:
+        import zero_partitioned_optimizer_shard_gb300 as z
+        from zero_partitioned_optimizer_shard_gb300.ranks import RankStep, layout_for
+
+        wl = W.by_name(name)
+        torch.cuda.set_device(0)
+        dev = torch.device("cuda", 0)
+        s = torch.cuda.current_stream(dev).cuda_stream
+        lay = layout_for(wl.psi, wl.n_ranks, wl.stage, wl.bucket_elems)
+        rs = RankStep(lay, z.hparams(**wl.hp.__dict__),
+                      z.ZERO_F16 if wl.grad_dtype == "f16" else z.ZERO_BF16, wl.loss_scale,
+                      wl.dynamic, wl.growth_interval, dev, exchange_elems=1 << 24)
+        for t_, role, kind, sig in ((rs.master, synth.ROLE_MASTER, synth.NORMAL, wl.master_sigma),
+                                    (rs.m, synth.ROLE_MOM, synth.NORMAL, wl.mom_sigma),
+                                    (rs.v, synth.ROLE_VAR, synth.NORMAL_SQ, wl.mom_sigma)):
+            synth.fill_dev(t_.data_ptr(), synth.OUT_F32, kind, wl.state_key(role), rs.origin,
+                           rs.local_len, wl.psi, sig, 1.0, s)
+        mine = [b for b in starts if rs.origin <= b and b + 64 <= rs.origin + rs.local_len]
+        flat = torch.tensor(np.concatenate([np.arange(b, b + 64) for b in mine]), device=dev)
+        local = flat - rs.origin
+        P = lay.psi_padded
+        copies = [torch.empty(P, dtype=torch.int16, device=dev) for _ in range(rs.rank_count)]
+        res = []
+        for step in range(1, steps + 1):
+            for j, c in enumerate(copies):
+                synth.fill_dev(c.data_ptr(), wl.grad_out, wl.grad_kind,
+                               wl.grad_key(step, rs.rank_begin + j), 0, P, wl.psi, wl.grad_sigma,
+                               1.0, s)
+            rs.step(copies)
+            st = z.zero_step_state_read(rs.st)
+            vals = {k: getattr(rs, k).index_select(0, local).cpu().numpy()
+                    for k in ("g", "master", "m", "v")}
+            vals["out"] = rs.params.index_select(0, flat).cpu().numpy().view(np.uint16)
+            res.append(((st.t, st.skip, st.norm, st.clip_coef, st.error), mine, vals))
+        out_q.put((proc, res))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_ranks_over_processes_full_size_gpt2():
+    """The GPT-2-1.5B workload (psi = 1,557,611,200, N = 8) over two processes of four
+    ranks, exchanging in 2^24-element windows: each step's norm, clip coefficient and t
+    against the oracle's golden scalars, and the elements on sampled windows (every
+    shard's start, middle and end, random places) against the oracle run on them."""
+    from tests.golden import make_golden as golden
+    from tests.gpu_harness import NORM_REL
+    from tests.test_gpu_fullsize import SampledOracle, _windows, WIN
+
+    name, world, steps = "C2", 2, 2
+    if not os.path.exists(golden.golden_path(name)):
+        pytest.skip("golden file for C2 not generated")
+    if torch.cuda.mem_get_info()[0] < 70e9:
+        pytest.skip("needs ~60 GB of free HBM")
+    wl = W.by_name(name)
+    rows = golden.load(name)
+    import oracle
+    lay = oracle.load().partition(wl.psi, wl.n_ranks, wl.stage)
+    starts = _windows(lay, wl)
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_full_main, args=(p, world, port, name, steps, starts, q))
+             for p in range(world)]
+    for p in procs:
+        p.start()
+    got = {}
+    try:
+        for _ in range(world):
+            r = q.get(timeout=1200)
+            got[r[0]] = r[1]
+    except queue.Empty:
+        pytest.fail(f"processes {sorted(set(range(world)) - set(got))} returned nothing")
+    finally:
+        for p in procs:
+            p.join(timeout=120)
+            if p.is_alive():
+                p.terminate()
+    assert all(p.exitcode == 0 for p in procs)
+    so = SampledOracle(wl, starts)
+    for step in range(1, steps + 1):
+        row = rows[step - 1]
+        so.step(step, row)
+        want = {k: dict(zip(starts, getattr(so, k))) for k in ("g", "master", "m", "v", "out")}
+        for p in range(world):
+            (t, skip, norm, c, err), mine, vals = got[p][step - 1]
+            assert err == 0 and (t, skip) == (row["t"], row["skipped"])
+            assert abs(norm - row["norm"]) <= NORM_REL * row["norm"], (p, step, norm, row["norm"])
+            assert abs(c - row["clip_coef"]) <= 2 ** -23 * row["clip_coef"], (p, step)
+            for k in ("g", "master", "m", "v"):
+                a = vals[k].reshape(len(mine), WIN).astype(np.float64)
+                b = np.stack([want[k][s_] for s_ in mine]).astype(np.float64)
+                if k == "g":
+                    assert np.array_equal(vals[k].reshape(len(mine), WIN).view(np.uint32),
+                                          np.stack([want[k][s_] for s_ in mine]).view(np.uint32))
+                else:
+                    assert np.all(np.abs(a - b) <= 1e-5 * np.abs(b) + 1e-30), (p, step, k)
+            from tests.gpu_harness import bf16_ordinal
+            o = vals["out"].reshape(len(mine), WIN)
+            wo = np.stack([want["out"][s_] for s_ in mine])
+            assert np.abs(bf16_ordinal(o) - bf16_ordinal(wo)).max() <= 1, (p, step)
+    assert sum(len(got[p][0][1]) for p in range(world)) >= len(starts) - 2
