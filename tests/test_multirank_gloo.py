@@ -338,3 +338,136 @@ def test_a_process_that_leaves_ends_the_next_exchange_with_an_error():
     ok, what = got[0]
     assert ok and what.startswith("error after"), what
     assert float(what.split()[2].rstrip("s:")) < 30
+
+
+# ---------------------------------------------------------------------------------------
+# The windowed gradient exchange RankStep makes (ranks.exchange_windows, exchange_plan,
+# Exchange.send_recv: point-to-point, two receive slots, the next windows in flight while
+# one is reduced), run on CPU tensors with the oracle's arithmetic in place of the kernels.
+# ---------------------------------------------------------------------------------------
+def _windowed_main(proc, world, port, n_ranks, psi, seed, steps, w, out_q):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=proc, world_size=world)
+    try:
+        from zero_partitioned_optimizer_shard_gb300.ranks import (Exchange, exchange_plan,
+                                                                   exchange_windows, local_ranks)
+        ex = Exchange()
+        rb, R = local_ranks(n_ranks, world, proc)
+        orc = oracle.load()
+        lay = orc.partition(psi, n_ranks, 2, 8)
+        S, P = lay.shard, lay.psi_padded
+        lo, L = rb * S, R * S
+        wins = exchange_windows(L, world, w)
+        part = max(c for ws in wins for _, c in ws)
+        K = max(len(ws) for ws in wins)
+        slots = 2 if K > 1 else 1
+        recv = [[torch.zeros(world * part, dtype=torch.int16) for _ in range(R)] for _ in range(slots)]
+        hp = oracle.hparams(max_grad_norm=1e-3)
+        sc = oracle.scaler(1.0, False)
+        master = _state(synth.ROLE_MASTER, synth.NORMAL, 0.02, lo, L, psi, seed)
+        m = _state(synth.ROLE_MOM, synth.NORMAL, 1e-4, lo, L, psi, seed)
+        v = _state(synth.ROLE_VAR, synth.NORMAL_SQ, 1e-4, lo, L, psi, seed)
+        g = np.zeros(L, np.float32)
+        params = torch.zeros(P, dtype=torch.int16)
+        results = []
+        for step in range(1, steps + 1):
+            copies = [torch.from_numpy(synth.fill_host(
+                synth.OUT_BF16, synth.NORMAL, synth.key(seed, synth.ROLE_GRAD, step, rb + j),
+                0, P, psi, SIGMA).view(np.int16)) for j in range(R)]
+
+            def issue(k):
+                rv = recv[k % slots]
+                sends, recvs = exchange_plan(wins, proc, k, R, part)
+                return ex.send_recv([(q, copies[j][b:b + n]) for q, j, b, n in sends],
+                                    [(q, rv[j][o:o + n]) for q, j, o, n in recvs])
+
+            sumsq = np.zeros(n_ranks, np.float64)
+            ov = np.zeros(1, np.uint32)
+            pending = {k: issue(k) for k in range(min(slots, K))}
+            for k in range(K):
+                if k in pending:
+                    pending.pop(k).wait()
+                if k < len(wins[proc]):
+                    b, n = wins[proc][k]
+                    rv = recv[k % slots]
+                    reps = []
+                    for i in range(n_ranks):  # rank i's copy of this window, in rank order
+                        q, j = divmod(i, R)
+                        src = copies[j][b:b + n] if q == proc else rv[j][q * part:q * part + n]
+                        reps.append(src.numpy().view(np.uint16).copy())
+                    orc.reduce_window(lay, oracle.BF16, reps, b, n, orc.inv_scale(n_ranks, 1.0),
+                                      g[b - lo:], sumsq, ov)
+                if k + slots < K:
+                    pending[k + slots] = issue(k + slots)
+            ex.all_gather(torch.from_numpy(sumsq), rb, rb + R)  # the norm's inputs
+            flag = torch.tensor([int(ov[0])], dtype=torch.int32)
+            ex.maximum(flag)
+            norm, _ = orc.global_norm(sumsq)
+            applied = orc.scaler_update(sc, int(flag.item()))
+            c = orc.clip_coef(norm, hp.max_grad_norm) if applied else 1.0
+            if applied:
+                n = max(0, min(L, psi - lo))
+                out = np.zeros(L, np.uint16)
+                orc.adamw_elements(hp, c, sc.t, g[:n], master[:n], m[:n], v[:n], out[:n])
+                params[lo:lo + L] = torch.from_numpy(out.view(np.int16))
+                ex.all_gather(params, lo, lo + L)
+            results.append((norm, c, params.numpy().view(np.uint16).copy()))
+        out_q.put((proc, results, master.copy(), m.copy(), v.copy(), g.copy()))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world,n_ranks,psi,w", [
+    (2, 2, 48_761, 8192),      # 3 and 4 windows on the two processes
+    (2, 4, 100_003, 8192),     # two ranks per process
+    (4, 8, 200_003, 16384),
+    (2, 2, 30_001, 0),         # one window per range
+])
+def test_windowed_exchange_matches_single_process(world, n_ranks, psi, w):
+    seed, steps = 5, 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_windowed_main,
+                         args=(p, world, port, n_ranks, psi, seed, steps, w, q))
+             for p in range(world)]
+    for p in procs:
+        p.start()
+    got = {}
+    try:
+        for _ in range(world):
+            proc, results, master, m, v, g = q.get(timeout=300)
+            got[proc] = (results, master, m, v, g)
+    except queue.Empty:
+        pytest.fail(f"processes {sorted(set(range(world)) - set(got))} returned nothing")
+    finally:
+        for p in procs:
+            p.join(timeout=60)
+            if p.is_alive():
+                p.terminate()
+    assert all(p.exitcode == 0 for p in procs)
+    orc = oracle.load()
+    lay = orc.partition(psi, n_ranks, 2, 8)
+    P = lay.psi_padded
+    hp = oracle.hparams(max_grad_norm=1e-3)
+    sc = oracle.scaler(1.0, False)
+    master = _state(synth.ROLE_MASTER, synth.NORMAL, 0.02, 0, P, psi, seed)
+    m = _state(synth.ROLE_MOM, synth.NORMAL, 1e-4, 0, P, psi, seed)
+    v = _state(synth.ROLE_VAR, synth.NORMAL_SQ, 1e-4, 0, P, psi, seed)
+    g, out = np.zeros(P, np.float32), np.zeros(P, np.uint16)
+    L = lay.shard * (n_ranks // world)
+    for step in range(1, steps + 1):
+        reps = [synth.fill_host(synth.OUT_BF16, synth.NORMAL,
+                                synth.key(seed, synth.ROLE_GRAD, step, k), 0, P, psi, SIGMA)
+                for k in range(n_ranks)]
+        rep = orc.step(lay, hp, oracle.BF16, reps, g, master, m, v, out, sc)
+        for p in range(world):
+            n_a, c_a, out_a = got[p][0][step - 1]
+            assert n_a == rep.norm and c_a == rep.clip_coef
+            assert np.array_equal(out_a, out)
+    for p in range(world):
+        _, ms, mm, mv, mg = got[p]
+        sl = slice(p * L, (p + 1) * L)
+        for a, b in ((ms, master[sl]), (mm, m[sl]), (mv, v[sl]), (mg, g[sl])):
+            assert np.array_equal(a.view(np.uint32), b.view(np.uint32))

@@ -56,6 +56,43 @@ def local_ranks(n_ranks: int, world: int, proc: int) -> tuple[int, int]:
     return proc * count, count
 
 
+def exchange_windows(local_len: int, world: int, w: int) -> list[list[tuple[int, int]]]:
+    """For every process q, its flat range [q * local_len, (q + 1) * local_len) cut at the
+    flat multiples of w: a list of (begin, count) in order.  w = 0: one window per range."""
+    out = []
+    for q in range(world):
+        lo, hi = q * local_len, (q + 1) * local_len
+        if w == 0:
+            out.append([(lo, local_len)])
+            continue
+        ws, b = [], lo
+        while b < hi:
+            e = min((b // w + 1) * w, hi)
+            ws.append((b, e - b))
+            b = e
+        out.append(ws)
+    return out
+
+
+def exchange_plan(windows, me: int, k: int, copies: int, part: int):
+    """Exchange k for process `me`: sends (peer, local copy j, flat begin, count) of the
+    peer's k-th window out of each local gradient copy, and receives (peer, local copy j,
+    offset in the receive slot, count) of its own k-th window from every peer, at
+    peer * part in copy j's slot.  Between two processes the messages are listed in the
+    same order on both sides (by copy), which is how point-to-point messages match."""
+    sends, recvs = [], []
+    for q in range(len(windows)):
+        if q == me:
+            continue
+        if k < len(windows[q]):
+            b, n = windows[q][k]
+            sends += [(q, j, b, n) for j in range(copies)]
+        if k < len(windows[me]):
+            _, n = windows[me][k]
+            recvs += [(q, j, q * part, n) for j in range(copies)]
+    return sends, recvs
+
+
 class _Done:
     def wait(self) -> None:
         pass
@@ -195,7 +232,7 @@ class RankStep:
         self.params_local = self.params[self.origin:self.origin + self.local_len]
         self.partials = torch.empty(layout.n_tiles, dtype=torch.float64, device=dev)
         self.st = torch.empty(STATE_BYTES, dtype=torch.uint8, device=dev)
-        self.windows_of = self._windows(exchange_elems)
+        self.windows_of = exchange_windows(self.local_len, self.world, exchange_elems)
         self.n_exchanges = max(len(w) for w in self.windows_of)
         # every rank's copy of one window of this process's range arrives here: per local
         # copy and slot (two slots: the next windows' exchanges overlap this window's
@@ -208,24 +245,6 @@ class RankStep:
             if self.world > 1 else []
         zero_step_state_init(layout, loss_scale, dynamic, growth_interval, self.st, self.partials)
 
-    def _windows(self, w: int) -> list[list[tuple[int, int]]]:
-        """For every process q, its range [q*L, (q+1)*L) cut at the flat multiples of w:
-        a list of (begin, count).  w = 0: the whole range in one window."""
-        L = self.local_len
-        out = []
-        for q in range(self.world):
-            lo, hi = q * L, (q + 1) * L
-            if w == 0:
-                out.append([(lo, L)])
-                continue
-            ws, b = [], lo
-            while b < hi:
-                e = min((b // w + 1) * w, hi)
-                ws.append((b, e - b))
-                b = e
-            out.append(ws)
-        return out
-
     def windows(self) -> list[tuple[int, int]]:
         """This process's reduce windows (begin, count), in order."""
         return self.windows_of[self.proc]
@@ -233,19 +252,10 @@ class RankStep:
     def _issue(self, k: int, copies: Sequence[torch.Tensor]):
         """Exchange k: send every other process its k-th window of each local copy, and
         receive this process's k-th window of every other process's copies."""
-        me, R = self.proc, self.rank_count
         recv = self.recv[k % self.slots]
-        sends, recvs = [], []
-        for q in range(self.world):
-            if q == me:
-                continue
-            if k < len(self.windows_of[q]):
-                b, n = self.windows_of[q][k]
-                sends += [(q, copies[j][b:b + n]) for j in range(R)]
-            if k < len(self.windows_of[me]):
-                _, n = self.windows_of[me][k]
-                recvs += [(q, recv[j][q * self.part:q * self.part + n]) for j in range(R)]
-        return self.ex.send_recv(sends, recvs)
+        sends, recvs = exchange_plan(self.windows_of, self.proc, k, self.rank_count, self.part)
+        return self.ex.send_recv([(q, copies[j][b:b + n]) for q, j, b, n in sends],
+                                 [(q, recv[j][o:o + n]) for q, j, o, n in recvs])
 
     def _sources(self, k: int, copies: Sequence[torch.Tensor]) -> list[int]:
         """Device address, for rank i = 0 .. N-1, of the first element of this process's
@@ -322,4 +332,5 @@ def layout_for(psi: int, n_ranks: int, stage: int = 2, bucket_elems: int = 0):
     return zero_partition(psi, n_ranks, stage, 8, bucket_elems)
 
 
-__all__ = ["Exchange", "RankStep", "local_ranks", "layout_for", "OVERFLOW_WORD"]
+__all__ = ["Exchange", "RankStep", "local_ranks", "layout_for", "exchange_windows",
+           "exchange_plan", "OVERFLOW_WORD"]
