@@ -2,7 +2,7 @@
  * zero.h -- C ABI of the GB300 (sm_103a) ZeRO-DP partitioned mixed-precision AdamW step.
  *
  * One optimizer step of ZeRO-DP data parallelism with all N data-parallel ranks held as
- * buffers on one GPU:
+ * buffers on one GPU (or, through the rank-local entry points, spread over processes):
  *   1. partition      Psi flat parameters into N equal, padded shards (rank r owns
  *                     flat [r*S, (r+1)*S)), with the per-rank model-state ledger
  *   2. reduce-scatter average the N ranks' fp16/bf16 gradient copies into fp32, remove
@@ -308,9 +308,12 @@ int zero_adamw_cast_gather_host_state(const zero_layout_t* layout,
  * local_len = rank_count*S long.  Local buffers are indexed by flat index - origin.
  * origin must be a multiple of 8 (partition with align = 8; ZERO_EALIGN otherwise).
  * One step, per process, with the exchanges done by the caller (e.g. NCCL):
- *   1. exchange: for each local range, every rank's gradient copy of it arrives (an
- *      all-to-all of equal chunks: rank k's copy of flat [origin, origin + local_len));
- *   2. zero_reduce_shard_unscale_local over the local range (one or more windows);
+ *   1. exchange: every rank's gradient copy of the local range arrives (rank k's copy of
+ *      flat [origin, origin + local_len)), whole or window by window (an all-to-all, or
+ *      point-to-point sends of each window);
+ *   2. zero_reduce_shard_unscale_local over the local range (one or more windows; the
+ *      result does not depend on the windows when their boundaries lie on the flat
+ *      multiples of ZERO_TILE_ELEMS);
  *   3. exchange: all-gather every process's partial slots [rank_begin*tiles_per_rank,
  *      (rank_begin + rank_count)*tiles_per_rank) into the full partials array, and
  *      combine the step state's `overflow` word over processes (maximum);
