@@ -401,6 +401,8 @@ int zero_step_launches(const zero_layout_t* layout, zero_dtype_t dtype);
  *   host_state_out  optional HOST pointer (pinned): the step state is copied there at
  *                   the end of the step on `stream` (the caller synchronises)
  *   copy_stream     must differ from stream
+ * A small layout in one bucket (one that zero_step runs as a single launch) runs as that
+ * single launch here too, once its copies have arrived.
  * Returns ZERO_ENOMEM if staging is too small.
  * ------------------------------------------------------------------------------------- */
 int zero_step_host(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,

@@ -351,17 +351,20 @@ def test_stages_share_arithmetic():
             assert np.array_equal(o[k].view(np.uint8), outs[0][k].view(np.uint8))
 
 
-@pytest.mark.parametrize("recipe,steps", [("C2", 2), ("C5", 8)])
-def test_step_host_equals_device_path(recipe, steps):
+@pytest.mark.parametrize("recipe,steps,bucket", [("C2", 2, 65536), ("C5", 8, 65536), ("C1", 3, 0)])
+def test_step_host_equals_device_path(recipe, steps, bucket):
     """zero_step_host (gradients in pinned host memory, bucketed H2D ring) gives the same
     bits as zero_step on device-resident gradients; with the fp16 dynamic-scale recipe
-    the injected inf at step 7 is skipped the same way."""
+    the injected inf at step 7 is skipped the same way.  With one bucket of a small layout
+    (the odd-size fp16 recipe) both take the single-launch step once the copies are in."""
     wl = W.scaled(getattr(W, recipe), 3 * 65536 + 40, steps=steps)
     dt = z.ZERO_F16 if wl.grad_dtype == "f16" else z.ZERO_BF16
-    dev = GpuRun(wl, bucket_elems=65536)
-    host = GpuRun(wl, bucket_elems=65536)
+    dev = GpuRun(wl, bucket_elems=bucket)
+    host = GpuRun(wl, bucket_elems=bucket)
     P = host.lay.psi_padded
-    staging = torch.empty(2 * wl.n_ranks * 65536, dtype=torch.int16, device="cuda")
+    if bucket == 0:
+        assert z.zero_step_launches(host.lay, dt) == 1
+    staging = torch.empty(2 * wl.n_ranks * host.lay.bucket_elems, dtype=torch.int16, device="cuda")
     copy_stream = torch.cuda.Stream()
     hstate = torch.empty(z.STATE_BYTES, dtype=torch.uint8).pin_memory()
     skipped = 0

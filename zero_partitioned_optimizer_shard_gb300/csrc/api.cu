@@ -180,6 +180,46 @@ int adamw_rereduce(const zero_layout_t* L, const zero_adamw_hparams_t* hp, zero_
     return cuda_status(launch_adamw_rereduce(a, stream));
 }
 
+/* The whole step as ONE cooperative launch when the layout takes it (fused.cu: same bits
+ * as the three launches).  *done tells whether it was enqueued; it is not when the layout
+ * takes the three launches, or when the cooperative launch is refused because fewer
+ * blocks fit on the GPU than the occupancy query promised (another context holds part of
+ * it): then nothing was enqueued.  replicas: the N copies, each from flat 0. */
+int fused_step(const zero_layout_t* L, const zero_adamw_hparams_t* hp, zero_dtype_t dtype,
+               const void* const* replicas, float* g, double* partials, float* master, float* m,
+               float* v, uint16_t* params, zero_step_state_t* st, cudaStream_t s, bool* done)
+{
+    *done = false;
+    const int shape = fused_shape(L, dtype);
+    if (shape <= 0)
+        return ZERO_OK;
+    FusedArgs f;
+    memset(&f, 0, sizeof f);
+    for (uint64_t k = 0; k < L->n_ranks; ++k)
+        f.rep[k] = replicas[k];
+    f.g = g;
+    f.partials = partials;
+    f.master = master;
+    f.m = m;
+    f.v = v;
+    f.out = params;
+    f.st = st;
+    f.psi = L->psi;
+    f.psi_padded = L->psi_padded;
+    f.shard = L->shard;
+    f.tiles_per_rank = L->tiles_per_rank;
+    f.n_ranks = L->n_ranks;
+    f.out_f16 = hp->params_dtype == ZERO_F16 ? 1u : 0u;
+    f.hp = *hp;
+    const cudaError_t e = launch_step_fused(f, dtype, L->n_tiles, shape, s);
+    if (e == cudaErrorCooperativeLaunchTooLarge) {
+        cudaGetLastError();  // nothing was enqueued: the caller takes the three launches
+        return ZERO_OK;
+    }
+    *done = e == cudaSuccess;
+    return cuda_status(e);
+}
+
 /* The device address of `bytes` of page-locked host memory at p (cudaHostAlloc or
  * cudaHostRegister, which UVA maps into the device's address space), or null when any
  * part of it is not such memory: pageable, device or unknown pointers are refused. */
@@ -439,34 +479,10 @@ extern "C" int zero_step(const zero_layout_t* layout, const zero_adamw_hparams_t
     if (!aligned16(partials))
         return ZERO_EALIGN;
     const cudaStream_t s = (cudaStream_t)stream;
-    const int shape = fused_shape(layout, dtype);
-    if (shape > 0) {
-        // small layout: the whole step in one launch, with the same bits (fused.cu)
-        FusedArgs f;
-        memset(&f, 0, sizeof f);
-        for (uint64_t k = 0; k < N; ++k)
-            f.rep[k] = replicas[k];
-        f.g = g;
-        f.partials = partials;
-        f.master = master;
-        f.m = m;
-        f.v = v;
-        f.out = params;
-        f.st = st;
-        f.psi = layout->psi;
-        f.psi_padded = P;
-        f.shard = layout->shard;
-        f.tiles_per_rank = layout->tiles_per_rank;
-        f.n_ranks = layout->n_ranks;
-        f.out_f16 = hp->params_dtype == ZERO_F16 ? 1u : 0u;
-        f.hp = *hp;
-        const cudaError_t e = launch_step_fused(f, dtype, layout->n_tiles, shape, s);
-        if (e != cudaErrorCooperativeLaunchTooLarge)
-            return cuda_status(e);
-        // fewer blocks can be resident than the occupancy query promised (another context
-        // holds part of the GPU): nothing was enqueued, so take the three launches instead
-        cudaGetLastError();
-    }
+    bool done = false;
+    rc = fused_step(layout, hp, dtype, replicas, g, partials, master, m, v, params, st, s, &done);
+    if (done || rc != ZERO_OK)
+        return rc;
     for (uint64_t b = 0; b < layout->n_buckets; ++b) {
         const uint64_t begin = b * W, count = begin + W < P ? W : P - begin;
         rc = reduce_window(layout, dtype, replicas + b * N, begin, count, g, partials, st, s);
@@ -536,6 +552,7 @@ extern "C" int zero_step_host(const zero_layout_t* layout, const zero_adamw_hpar
         e = cudaStreamWaitEvent(cs, start, 0);
     uint16_t* ring = (uint16_t*)staging;
     const void* reps[ZERO_MAX_KERNEL_RANKS];
+    bool fused = false;
     for (uint64_t b = 0; b < layout->n_buckets && e == cudaSuccess && rc == ZERO_OK; ++b) {
         const int slot = (int)(b & 1);
         const uint64_t begin = b * W, count = begin + W < P ? W : P - begin;
@@ -551,14 +568,18 @@ extern "C" int zero_step_host(const zero_layout_t* layout, const zero_adamw_hpar
             e = cudaEventRecord(filled[slot], cs);
         if (e == cudaSuccess)
             e = cudaStreamWaitEvent(s, filled[slot], 0);
-        if (e == cudaSuccess)
+        // one bucket of a small layout: the whole step as one launch, once it has arrived
+        if (e == cudaSuccess && layout->n_buckets == 1)
+            rc = fused_step(layout, hp, dtype, reps, g, partials, master, m, v, params, st, s,
+                            &fused);
+        if (e == cudaSuccess && rc == ZERO_OK && !fused)
             rc = reduce_window(layout, dtype, reps, begin, count, g, partials, st, s);
         if (e == cudaSuccess && rc == ZERO_OK)
             e = cudaEventRecord(consumed[slot], s);
     }
-    if (e == cudaSuccess && rc == ZERO_OK)
+    if (e == cudaSuccess && rc == ZERO_OK && !fused)
         rc = grad_norm(layout, hp, partials, st, s);
-    if (e == cudaSuccess && rc == ZERO_OK)
+    if (e == cudaSuccess && rc == ZERO_OK && !fused)
         rc = adamw(layout, hp, g, master, m, v, params, st, s);
     if (e == cudaSuccess && rc == ZERO_OK && host_state_out)
         e = cudaMemcpyAsync(host_state_out, st, sizeof *st, cudaMemcpyDeviceToHost, s);
