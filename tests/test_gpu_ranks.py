@@ -332,3 +332,75 @@ def test_ranks_over_processes_full_size_fp16_stress():
     oracle scalars step by step on both processes."""
     skipped = _full_size("C5", 2, 14)
     assert skipped >= 2
+
+
+@pytest.mark.parametrize("psi,n,world,window", [
+    (100_003, 4, 2, 0), (100_003, 4, 4, 8192), (48_761, 2, 2, 8192), (13, 4, 2, 0),
+    ((1 << 20) + 77, 8, 4, 1 << 16), (3 * 8192 * 8 + 5, 8, 8, 8192),
+])
+def test_local_entry_points_write_only_their_buffers(psi, n, world, window):
+    """The rank-local calls on guard-zoned buffers, the processes simulated one after the
+    other in this process (the exchanges are plain copies): every local buffer's canary
+    zones stay intact, and g, master, m, v and the gathered parameters equal the one-GPU
+    step's bit for bit over two steps."""
+    import zero_partitioned_optimizer_shard_gb300 as z
+    from zero_partitioned_optimizer_shard_gb300.ranks import exchange_windows
+
+    wl = replace(W.scaled(W.C2, psi, steps=2), n_ranks=n)
+    ref = GpuRun(wl, split=True, align=8)
+    lay, S, P = ref.lay, ref.lay.shard, ref.lay.psi_padded
+    R = n // world
+    L = R * S
+    hp = ref.hp
+    guard = GpuRun(wl, align=8)  # only its guarded allocator and canary check are used
+    procs = []
+    for p in range(world):
+        loc = {k: guard.alloc(L, torch.float32) for k in ("g", "master", "m", "v")}
+        for k in ("master", "m", "v"):
+            loc[k].copy_(getattr(ref, k)[p * L:(p + 1) * L])
+        loc["params"] = guard.alloc(P, torch.int16)
+        loc["params"].zero_()
+        loc["partials"] = guard.alloc(lay.n_tiles, torch.float64)
+        loc["st"] = guard.alloc(z.STATE_BYTES, torch.uint8)
+        loc["recv"] = [guard.alloc(L, torch.int16) for _ in range(n)]
+        z.zero_step_state_init(lay, wl.loss_scale, wl.dynamic, wl.growth_interval, loc["st"],
+                               loc["partials"])
+        procs.append(loc)
+    wins = exchange_windows(L, world, window)
+    for step in (1, 2):
+        ref.step(step)  # also leaves this step's gradient copies in ref.reps
+        for p, loc in enumerate(procs):
+            for k in range(n):  # every rank's copy of this process's range arrives
+                loc["recv"][k].copy_(ref.reps[k][p * L:(p + 1) * L])
+            for b, c in wins[p]:
+                reps = [loc["recv"][k].data_ptr() + 2 * (b - p * L) for k in range(n)]
+                z.zero_reduce_shard_unscale_local(lay, z.ZERO_BF16, p * R, R, reps, b, c,
+                                                  loc["g"], loc["partials"], loc["st"])
+        tpr = lay.tiles_per_rank
+        flags = []
+        for p, loc in enumerate(procs):  # the norm's inputs, exchanged
+            for o, other in enumerate(procs):
+                if o != p:
+                    loc["partials"][o * R * tpr:(o + 1) * R * tpr] = \
+                        other["partials"][o * R * tpr:(o + 1) * R * tpr]
+            flags.append(int(loc["st"].view(torch.int32)[10]))
+        for loc in procs:
+            loc["st"].view(torch.int32)[10] = max(flags)
+            z.zero_grad_norm(lay, hp, loc["partials"], loc["st"])
+        for p, loc in enumerate(procs):
+            z.zero_adamw_cast_gather_local(lay, hp, p * R, R, loc["g"], loc["master"], loc["m"],
+                                           loc["v"], loc["params"][p * L:(p + 1) * L], loc["st"])
+        for p, loc in enumerate(procs):  # the parameter all-gather
+            for o, other in enumerate(procs):
+                if o != p:
+                    loc["params"][o * L:(o + 1) * L] = other["params"][o * L:(o + 1) * L]
+        torch.cuda.synchronize()
+        want = ref.arrays()
+        for p, loc in enumerate(procs):
+            sl = slice(p * L, (p + 1) * L)
+            assert np.array_equal(loc["st"].cpu().numpy(), ref.st.cpu().numpy()), (step, p)
+            for k in ("g", "master", "m", "v"):
+                a = loc[k].cpu().numpy()
+                assert np.array_equal(a.view(np.uint32), want[k][sl].view(np.uint32)), (step, p, k)
+            assert np.array_equal(loc["params"].cpu().numpy().view(np.uint16), want["out"])
+    guard.check_guards()
