@@ -698,10 +698,13 @@ def _e2e(args, z, torch, dev, wl, hp, reps, g, partials, master, m, v, out, st, 
     dt = time.perf_counter() - t0
     return {"value": wl.psi * steps / dt, "unit": "params/s", "h2d_bytes_per_step": need,
             "d2h_bytes_per_step": z.STATE_BYTES, "steps": steps, "ms_per_step": dt / steps * 1e3,
-            "path": "zero_step_host: N pinned host gradient copies -> 2 x 16M-element staging "
-                    "ring (H2D on a copy stream, overlapped with the bucket reduces) -> norm -> "
-                    "AdamW (one launch for all three on a small layout in one bucket); step "
-                    "state copied back to pinned host memory"}
+            "path": ("zero_step_host: N pinned host gradient copies read in place over the "
+                     "CPU-GPU link by the single launch (reduce, norm and AdamW in one kernel); "
+                     "step state copied back to pinned host memory"
+                     if z.zero_step_launches(lay, gdt) == 1 else
+                     "zero_step_host: N pinned host gradient copies -> 2 x 16M-element staging "
+                     "ring (H2D on a copy stream, overlapped with the bucket reduces) -> norm -> "
+                     "AdamW; step state copied back to pinned host memory")}
 
 
 def run_sweep(args):

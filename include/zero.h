@@ -402,7 +402,10 @@ int zero_step_launches(const zero_layout_t* layout, zero_dtype_t dtype);
  *                   the end of the step on `stream` (the caller synchronises)
  *   copy_stream     must differ from stream
  * A small layout in one bucket (one that zero_step runs as a single launch) runs as that
- * single launch here too, once its copies have arrived.
+ * single launch here too.  When every copy lies in page-locked host memory (through its
+ * whole psi_padded range, 16-byte aligned), the launch reads the copies there directly
+ * over the CPU-GPU link, and staging is not touched; otherwise the copies are staged
+ * first.
  * Returns ZERO_ENOMEM if staging is too small.
  * ------------------------------------------------------------------------------------- */
 int zero_step_host(const zero_layout_t* layout, const zero_adamw_hparams_t* hp,

@@ -351,12 +351,15 @@ def test_stages_share_arithmetic():
             assert np.array_equal(o[k].view(np.uint8), outs[0][k].view(np.uint8))
 
 
-@pytest.mark.parametrize("recipe,steps,bucket", [("C2", 2, 65536), ("C5", 8, 65536), ("C1", 3, 0)])
-def test_step_host_equals_device_path(recipe, steps, bucket):
+@pytest.mark.parametrize("recipe,steps,bucket,pinned", [("C2", 2, 65536, True), ("C5", 8, 65536, True),
+                                                        ("C1", 3, 0, True), ("C1", 3, 0, False)])
+def test_step_host_equals_device_path(recipe, steps, bucket, pinned):
     """zero_step_host (gradients in pinned host memory, bucketed H2D ring) gives the same
     bits as zero_step on device-resident gradients; with the fp16 dynamic-scale recipe
     the injected inf at step 7 is skipped the same way.  With one bucket of a small layout
-    (the odd-size fp16 recipe) both take the single-launch step once the copies are in."""
+    (the odd-size fp16 recipe) both take the single-launch step: it reads page-locked
+    copies where they are (the staging buffer is left untouched), and pageable ones after
+    they have been staged."""
     wl = W.scaled(getattr(W, recipe), 3 * 65536 + 40, steps=steps)
     dt = z.ZERO_F16 if wl.grad_dtype == "f16" else z.ZERO_BF16
     dev = GpuRun(wl, bucket_elems=bucket)
@@ -364,14 +367,14 @@ def test_step_host_equals_device_path(recipe, steps, bucket):
     P = host.lay.psi_padded
     if bucket == 0:
         assert z.zero_step_launches(host.lay, dt) == 1
-    staging = torch.empty(2 * wl.n_ranks * host.lay.bucket_elems, dtype=torch.int16, device="cuda")
+    staging = torch.full((2 * wl.n_ranks * host.lay.bucket_elems,), 0x5A5A, dtype=torch.int16, device="cuda")
     copy_stream = torch.cuda.Stream()
     hstate = torch.empty(z.STATE_BYTES, dtype=torch.uint8).pin_memory()
     skipped = 0
     for s in range(1, steps + 1):
         dev.step(s)
         host.gen_grads(s)
-        hreps = [r.cpu().pin_memory() for r in host.reps]
+        hreps = [r.cpu().pin_memory() if pinned else r.cpu() for r in host.reps]
         for r in host.reps:
             r.fill_(0x7F7F)  # the device copies must not be read
         z.zero_step_host(host.lay, host.hp, dt, hreps, staging, staging.numel() * 2,
@@ -384,6 +387,8 @@ def test_step_host_equals_device_path(recipe, steps, bucket):
         assert hs.norm == ds.norm or (hs.skip and ds.skip)
         skipped += hs.skip
     assert hs.t == steps - skipped and skipped >= (1 if recipe == "C5" else 0)
+    untouched = bool((staging == 0x5A5A).all())
+    assert untouched == (bucket == 0 and pinned)  # read in place only on the single launch
     x, y = dev.arrays(), host.arrays()
     for k in x:
         assert np.array_equal(x[k].view(np.uint8), y[k].view(np.uint8)), k

@@ -534,6 +534,28 @@ extern "C" int zero_step_host(const zero_layout_t* layout, const zero_adamw_hpar
         return ZERO_EALIGN;
 
     const cudaStream_t s = (cudaStream_t)stream, cs = (cudaStream_t)copy_stream;
+    // a small layout in one bucket whose copies all lie in page-locked host memory: the
+    // single launch reads them where they are, over the CPU-GPU link (its replica reads are
+    // plain global loads), so the transfer overlaps the sums instead of preceding the
+    // launch, and nothing is staged
+    if (layout->n_buckets == 1 && fused_shape(layout, dtype) > 0) {
+        const void* direct[ZERO_MAX_KERNEL_RANKS];
+        bool mapped = true;
+        for (uint64_t k = 0; k < N && mapped; ++k) {
+            direct[k] = pinned_host_device_ptr(host_replicas[k], P * 2);
+            mapped = aligned16(direct[k]);
+        }
+        bool fused = false;
+        if (mapped)
+            rc = fused_step(layout, hp, dtype, direct, g, partials, master, m, v, params, st, s, &fused);
+        if (rc != ZERO_OK)
+            return rc;
+        if (fused)
+            return host_state_out ? cuda_status(cudaMemcpyAsync(host_state_out, st, sizeof *st,
+                                                                cudaMemcpyDeviceToHost, s))
+                                  : ZERO_OK;
+        // not mapped, or the cooperative launch was refused: stage the copies
+    }
     cudaEvent_t start, filled[2], consumed[2];
     cudaError_t e = cudaEventCreateWithFlags(&start, cudaEventDisableTiming);
     int made = e == cudaSuccess ? 1 : 0;
