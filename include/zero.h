@@ -396,7 +396,8 @@ int zero_step_launches(const zero_layout_t* layout, zero_dtype_t dtype);
  * time, through a two-slot device staging ring: the copy of bucket b+1 (on copy_stream,
  * one cudaMemcpyAsync per rank) overlaps the reduce of bucket b (on stream).
  *   host_replicas   HOST array of N HOST pointers (pinned for overlap), each psi_padded
- *                   elements of dtype
+ *                   elements of dtype; read asynchronously, so they must stay unchanged
+ *                   until the step has completed on `stream`
  *   staging         DEVICE buffer of staging_bytes >= 2 * N * W * sizeof(dtype)
  *   host_state_out  optional HOST pointer (pinned): the step state is copied there at
  *                   the end of the step on `stream` (the caller synchronises)
