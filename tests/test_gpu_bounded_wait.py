@@ -11,8 +11,6 @@ status; and the same process then runs a full step through the product library t
 still matches the oracle.
 """
 import ctypes as C
-import os
-import subprocess
 import time
 
 import numpy as np
@@ -22,35 +20,8 @@ import torch
 import zero_partitioned_optimizer_shard_gb300 as z
 from synth import workloads as W
 from tests.gpu_harness import GpuRun, OracleRun, assert_scalars, assert_state_close
-from zero_partitioned_optimizer_shard_gb300 import _build
 
 pytestmark = pytest.mark.gpu
-
-
-@pytest.fixture(scope="module")
-def hooked(tmp_path_factory):
-    import __graft_entry__
-    __graft_entry__.build()
-    assert torch.cuda.is_available()
-    d = tmp_path_factory.mktemp("hooked")
-    objs = []
-    procs = []
-    for src in _build.SOURCES:
-        o = str(d / (os.path.splitext(src)[0] + ".o"))
-        procs.append(subprocess.Popen(["nvcc", *_build.NVCC_FLAGS, "-DZERO_TEST_HOOKS", "-c",
-                                       os.path.join(_build.CSRC, src), "-o", o]))
-        objs.append(o)
-    assert all(p.wait() == 0 for p in procs)
-    lib = str(d / "libzero_shard_hooked.so")
-    arch = _build.ARCH
-    subprocess.run(["nvcc", "-shared", f"-gencode=arch=compute_{arch},code=sm_{arch}", "-o", lib,
-                    *objs, "-lcudart"], check=True)
-    L = C.CDLL(lib)
-    L.zero_test_withhold_adamw_chunk.argtypes = [C.c_ulonglong]
-    L.zero_test_withhold_adamw_chunk.restype = C.c_int
-    L.zero_adamw_cast_gather.argtypes = [C.POINTER(z.Layout), C.POINTER(z.HParams)] + [C.c_void_p] * 7
-    L.zero_adamw_cast_gather.restype = C.c_int
-    return L
 
 
 def test_adamw_wait_runs_out_reports_error_and_gpu_stays_usable(hooked):

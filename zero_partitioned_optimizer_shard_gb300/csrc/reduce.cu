@@ -199,7 +199,34 @@ cudaError_t launch_dt(const ReduceArgs& a, cudaStream_t s)
     }
 }
 
+#ifdef ZERO_TEST_HOOKS
+/* Test builds only (never the product library): the exact-range test of the sum of
+ * squares on n groups of 8 values, one thread per group, so that a test can compare the
+ * device's decisions with the test's integer definition. */
+__global__ void k_test_squares_in_range(const float* x, uint8_t* out, uint64_t n)
+{
+    const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n)
+        return;
+    float v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        v[e] = x[8 * i + e];
+    out[i] = squares_in_range(v) ? 1 : 0;
+}
+#endif
+
 }  // namespace
+
+#ifdef ZERO_TEST_HOOKS
+extern "C" int zero_test_squares_in_range(const float* x, uint8_t* out, unsigned long long n)
+{
+    if (n == 0)
+        return 0;
+    k_test_squares_in_range<<<(unsigned)((n + 255) / 256), 256>>>(x, out, n);
+    return cudaGetLastError() == cudaSuccess && cudaDeviceSynchronize() == cudaSuccess ? 0 : -4;
+}
+#endif
 
 cudaError_t launch_reduce(const ReduceArgs& a, zero_dtype_t dtype, cudaStream_t s)
 {
