@@ -168,6 +168,59 @@ def test_ranks_over_processes_equal_the_one_gpu_step(world, wl, bucket):
     ref.check_guards()
 
 
+def test_exchange_nccl_branch_in_a_one_process_group(monkeypatch):
+    """The exchange layer's NCCL branch (collectives on the device tensors themselves, no
+    host staging) in a group of one process: NCCL runs every call, so the device views,
+    element types and contiguity the branch hands it are exercised, and each call must
+    leave its data as a one-process exchange does.  (NCCL takes one process per GPU, so
+    the exchange between processes itself runs over gloo in the other tests here.)"""
+    import datetime
+    import torch.distributed as dist
+
+    import zero_partitioned_optimizer_shard_gb300 as z
+    from zero_partitioned_optimizer_shard_gb300.ranks import OVERFLOW_WORD, Exchange, RankStep, layout_for
+
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(_free_port())
+    monkeypatch.setenv("NCCL_SOCKET_IFNAME", "lo")  # one process: the loopback is enough
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if not dist.is_nccl_available():
+        pytest.skip("this torch build has no NCCL")
+    dist.init_process_group("nccl", rank=0, world_size=1, timeout=datetime.timedelta(seconds=60))
+    try:
+        ex = Exchange()
+        assert ex.nccl and ex.world == 1 and ex.proc == 0
+        g = torch.Generator(device="cpu").manual_seed(5)
+        params = torch.randint(-32768, 32767, (4 * 1003,), dtype=torch.int16, generator=g).to(dev)
+        want = params.clone()
+        ex.all_gather(params, 0, params.numel())  # 16-bit data travels as bytes
+        assert torch.equal(params, want)
+        partials = torch.rand(77, dtype=torch.float64, generator=g).to(dev)
+        want = partials.clone()
+        ex.all_gather(partials, 0, 77)
+        assert torch.equal(partials, want)
+        st = torch.zeros(z.STATE_BYTES, dtype=torch.uint8, device=dev)
+        st.view(torch.int32)[OVERFLOW_WORD] = 1
+        ex.maximum(st.view(torch.int32)[OVERFLOW_WORD:OVERFLOW_WORD + 1])
+        assert int(st.view(torch.int32)[OVERFLOW_WORD]) == 1 and int(st.sum()) == 1
+        inp = torch.randint(-32768, 32767, (2 * 4096,), dtype=torch.int16, generator=g).to(dev)
+        out = torch.empty_like(inp)
+        ex.all_to_all(out, inp, [inp.numel()], [inp.numel()], async_op=True).wait()
+        assert torch.equal(out, inp)
+        ex.send_recv([], []).wait()  # nothing to exchange
+        # the step itself through the NCCL group: one process holding all four ranks
+        lay = layout_for(100_000, 4)
+        rs = RankStep(lay, z.hparams(), z.ZERO_BF16, device=dev)
+        copies = [torch.zeros(lay.psi_padded, dtype=torch.int16, device=dev) for _ in range(4)]
+        rs.step(copies)
+        torch.cuda.synchronize()
+        s = z.zero_step_state_read(rs.st)
+        assert s.t == 1 and s.norm == 0.0 and s.error == 0
+    finally:
+        dist.destroy_process_group()
+
+
 def test_rank_step_refuses_wrong_gradient_copies():
     """RankStep hands the library raw addresses, so it checks the copies first: a copy of
     the wrong length or element size is refused before anything is enqueued."""
