@@ -415,9 +415,15 @@ def _measure_simulated(args, base, psi=None, steps=None):
     ms = elapsed_ms / steps
     if flush is not None:
         per_step = sorted(e[0].elapsed_time(e[1]) for e in evs)
-        spread = {"p10": _pct(per_step, 10), "p50": _pct(per_step, 50), "p90": _pct(per_step, 90)}
+        spread = {"p10": _pct(per_step, 10), "p50": _pct(per_step, 50), "p90": _pct(per_step, 90),
+                  "from": "the timed steps (an event on each side of every step)"}
     else:
-        spread = None  # back-to-back steps: no event between them to keep launches overlapped
+        # the timed steps run back to back (no event between them, so each launch overlaps
+        # the previous kernel's tail); the spread comes from the breakdown steps, whose
+        # events sit between the calls
+        per_step = sorted(e[0].elapsed_time(e[3]) for e in sev)
+        spread = {"p10": _pct(per_step, 10), "p50": _pct(per_step, 50), "p90": _pct(per_step, 90),
+                  "from": f"the {n_split} breakdown steps (separate calls, events between them)"}
     params_per_s = wl.psi * steps / (elapsed_ms / 1e3)
     bytes_26 = (26 + 2 * N) * P
     moved = _fused_moved(N, lay, True) if launches == 1 else (34 + 2 * N)  # g re-read if split
