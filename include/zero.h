@@ -398,7 +398,10 @@ int zero_step_launches(const zero_layout_t* layout, zero_dtype_t dtype);
  *   host_replicas   HOST array of N HOST pointers (pinned for overlap), each psi_padded
  *                   elements of dtype; read asynchronously, so they must stay unchanged
  *                   until the step has completed on `stream`
- *   staging         DEVICE buffer of staging_bytes >= 2 * N * W * sizeof(dtype)
+ *   staging         DEVICE buffer of staging_bytes >= 2 * N * W8 * sizeof(dtype), W8 = W
+ *                   rounded up to a multiple of 8 (so every staged copy is 16-byte
+ *                   aligned; W itself is a multiple of 8 whenever there are several
+ *                   buckets); not touched when the copies are read in place
  *   host_state_out  optional HOST pointer (pinned): the step state is copied there at
  *                   the end of the step on `stream` (the caller synchronises)
  *   copy_stream     must differ from stream

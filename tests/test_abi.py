@@ -194,6 +194,15 @@ def test_step_host_rejections(lib):
     hreps0 = (C.c_void_p * 4)(A, A, 0, A)
     assert lib.zero_step_host(C.byref(lay), C.byref(hp), z.ZERO_BF16, hreps0, A, need, A, A, A,
                               A, A, A, A, None, 0x10, 0x20) == z.ZERO_EINVAL
+    # one bucket whose length is not a multiple of 8: each staged copy's slot is rounded up
+    # to 8 elements (16-byte aligned copies), so staging needs 2 * N * round8(W) elements
+    odd = z.zero_partition(1_000_003, 4, 2, 1, 0)
+    W = odd.bucket_elems
+    assert odd.n_buckets == 1 and W % 8 == 4
+    no_g = lambda staging_bytes: (C.byref(odd), C.byref(hp), z.ZERO_BF16, hreps, A, staging_bytes,
+                                  0, A, A, A, A, A, A, None, 0x10, 0x20)
+    assert lib.zero_step_host(*no_g(2 * 4 * W * 2)) == z.ZERO_ENOMEM
+    assert lib.zero_step_host(*no_g(2 * 4 * (W + 4) * 2)) == z.ZERO_EINVAL  # size passes; g = NULL
 
 
 def test_strerror(lib):

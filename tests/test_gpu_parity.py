@@ -395,6 +395,52 @@ def test_step_host_equals_device_path(recipe, steps, bucket, pinned):
     assert P == host.lay.psi_padded
 
 
+@pytest.mark.parametrize("n,dtype,one_block", [(16, "bf16", False), (8, "bf16", True), (2, "f16", True)])
+def test_step_host_reads_pinned_copies_in_place(n, dtype, one_block):
+    """The single launch reading page-locked gradient copies in place, beyond the odd-size
+    recipe: the N = 16 specialisation with bf16 copies, and copies that are views into ONE
+    page-locked allocation (each copy's device address is an interior address of that
+    one mapping, at the copy's offset).  Same bits as zero_step on device-resident copies
+    over three steps, clipping active, and the staging buffer is never touched."""
+    wl = replace(W.scaled(W.C2 if dtype == "bf16" else W.C1, (1 << 20) + 3, steps=3), n_ranks=n)
+    dt = z.ZERO_F16 if dtype == "f16" else z.ZERO_BF16
+    hp = z.hparams(max_grad_norm=1e-3)  # clipping active: c < 1 in every step
+    dev = GpuRun(wl, hp=hp)
+    host = GpuRun(wl, hp=hp)
+    assert z.zero_step_launches(host.lay, dt) == 1
+    P = host.lay.psi_padded
+    slot = (host.lay.bucket_elems + 7) // 8 * 8
+    staging = torch.full((2 * n * slot,), 0x5A5A, dtype=torch.int16, device="cuda")
+    copy_stream = torch.cuda.Stream()
+    hstate = torch.empty(z.STATE_BYTES, dtype=torch.uint8).pin_memory()
+    stride = (P + 7) // 8 * 8 + 8  # copies 16-byte aligned, none at the allocation's start
+    pool = torch.empty(n * stride + 8, dtype=torch.int16).pin_memory() if one_block else None
+    for s in range(1, 4):
+        dev.step(s)
+        host.gen_grads(s)
+        if one_block:  # copy k at element offset k * stride + 8
+            hreps = [pool[k * stride + 8:k * stride + 8 + P] for k in range(n)]
+            for h, r in zip(hreps, host.reps):
+                h.copy_(r.cpu())
+        else:
+            hreps = [r.cpu().pin_memory() for r in host.reps]
+        for r in host.reps:
+            r.fill_(0x7F7F)  # the device copies must not be read
+        z.zero_step_host(host.lay, host.hp, dt, hreps, staging, staging.numel() * 2,
+                         host.g, host.partials, host.master, host.m, host.v, host.out, host.st,
+                         hstate, None, copy_stream)
+        torch.cuda.synchronize()
+        hs = z.StepState.from_buffer_copy(hstate.numpy().tobytes())
+        ds = dev.state()
+        assert bytes(hs) == bytes(ds)
+        assert hs.clip_coef < 1.0
+    assert bool((staging == 0x5A5A).all())
+    x, y = dev.arrays(), host.arrays()
+    for k in x:
+        assert np.array_equal(x[k].view(np.uint8), y[k].view(np.uint8)), k
+    host.check_guards()
+
+
 def test_device_rejects_bad_calls_without_side_effects():
     wl = W.scaled(W.C2, 10_000, steps=1)
     gpu = GpuRun(wl)
