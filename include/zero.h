@@ -151,8 +151,8 @@ typedef struct zero_step_state {
  *   n_ranks       1 .. ZERO_MAX_RANKS
  *   stage         0 .. 3 (0 = plain data parallelism, for the ledger only)
  *   align         S is rounded up to a multiple of align (1 .. 2^20)
- *   bucket_elems  window of one reduce launch in zero_step; 0 = one window over the
- *                 whole flat buffer; otherwise a multiple of 8
+ *   bucket_elems  window of one reduce launch in zero_step; 0, or any value of at least
+ *                 N*S, = one window over the whole flat buffer; otherwise a multiple of 8
  *   out           written on success
  * Returns ZERO_OK or ZERO_EINVAL.
  * ------------------------------------------------------------------------------------- */
