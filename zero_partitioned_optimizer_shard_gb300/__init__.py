@@ -94,13 +94,24 @@ def _lib() -> C.CDLL:
                                 _P, _P, _P, _P, _P, _P, _P]
         L.zero_step_host.argtypes = [C.POINTER(Layout), C.POINTER(HParams), C.c_int, C.POINTER(_P),
                                      _P, C.c_uint64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
+        L.zero_reduce_shard_unscale_local.argtypes = [C.POINTER(Layout), C.c_int, C.c_uint32,
+                                                      C.c_uint32, C.POINTER(_P), C.c_uint64,
+                                                      C.c_uint64, _P, _P, _P, _P]
+        L.zero_adamw_cast_gather_local.argtypes = [C.POINTER(Layout), C.POINTER(HParams),
+                                                   C.c_uint32, C.c_uint32, _P, _P, _P, _P, _P,
+                                                   _P, _P]
+        L.zero_step_launches.argtypes = [C.POINTER(Layout), C.c_int]
+        L.zero_step_static_workspace.argtypes = [C.POINTER(Layout), C.POINTER(HParams), C.c_int,
+                                                 C.POINTER(_P), _P, _P, _P, _P, _P, _P, _P]
         L.zero_strerror.argtypes = [C.c_int]
         L.zero_strerror.restype = C.c_char_p
         L.zero_last_cuda_error.argtypes = []
         for name in ("zero_partition", "zero_segment_map", "zero_step_state_init", "zero_step_state_read",
                      "zero_step_state_write", "zero_reduce_shard_unscale", "zero_grad_norm",
                      "zero_adamw_cast_gather", "zero_adamw_cast_gather_host_state", "zero_step",
-                     "zero_step_host", "zero_last_cuda_error"):
+                     "zero_step_host", "zero_last_cuda_error", "zero_reduce_shard_unscale_local",
+                     "zero_adamw_cast_gather_local", "zero_step_launches",
+                     "zero_step_static_workspace"):
             getattr(L, name).restype = C.c_int
         _L = L
     return _L
@@ -228,9 +239,6 @@ def zero_reduce_shard_unscale_local(layout: Layout, dtype: int, rank_begin: int,
                                     st, stream=None) -> None:
     """g_local holds flat [rank_begin*S, (rank_begin+rank_count)*S) from index 0."""
     f = _lib().zero_reduce_shard_unscale_local
-    f.argtypes = [C.POINTER(Layout), C.c_int, C.c_uint32, C.c_uint32, C.POINTER(_P), C.c_uint64,
-                  C.c_uint64, _P, _P, _P, _P]
-    f.restype = C.c_int
     _check("zero_reduce_shard_unscale_local", f(
         C.byref(layout), dtype, rank_begin, rank_count, _ptr_array(replicas), begin, count,
         _ptr(g_local), _ptr(partials), _ptr(st), _stream(stream)))
@@ -240,9 +248,6 @@ def zero_adamw_cast_gather_local(layout: Layout, hp: HParams, rank_begin: int, r
                                  g_local, master_local, m_local, v_local, params_local, st,
                                  stream=None) -> None:
     f = _lib().zero_adamw_cast_gather_local
-    f.argtypes = [C.POINTER(Layout), C.POINTER(HParams), C.c_uint32, C.c_uint32, _P, _P, _P, _P,
-                  _P, _P, _P]
-    f.restype = C.c_int
     _check("zero_adamw_cast_gather_local", f(
         C.byref(layout), C.byref(hp), rank_begin, rank_count, _ptr(g_local), _ptr(master_local),
         _ptr(m_local), _ptr(v_local), _ptr(params_local), _ptr(st), _stream(stream)))
@@ -260,8 +265,6 @@ def zero_step_launches(layout: Layout, dtype: int) -> int:
     """Kernel launches of one zero_step call for this layout: 1 (single-launch step) or
     n_buckets + 2."""
     f = _lib().zero_step_launches
-    f.argtypes = [C.POINTER(Layout), C.c_int]
-    f.restype = C.c_int
     n = f(C.byref(layout), dtype)
     if n < 0:
         _check("zero_step_launches", n)
@@ -284,9 +287,6 @@ def zero_step_static_workspace(layout: Layout, hp: HParams, dtype: int, replicas
     memory.  The per-tile partials live in the library's static device array (8 MiB per
     GPU); calls must not overlap on the GPU.  See include/zero.h."""
     f = _lib().zero_step_static_workspace
-    f.argtypes = [C.POINTER(Layout), C.POINTER(HParams), C.c_int, C.POINTER(_P), _P, _P, _P, _P,
-                  _P, _P, _P]
-    f.restype = C.c_int
     _check("zero_step_static_workspace", f(
         C.byref(layout), C.byref(hp), dtype, _ptr_array(replicas), _ptr(g), _ptr(master), _ptr(m),
         _ptr(v), _ptr(params), _ptr(st), _stream(stream)))
