@@ -16,8 +16,8 @@
  *   [ZO] "3、ZeRO技术概述：ZeRO三个阶段原理与对比", 5688vip.com (DeepSpeed chapter)
  *   [MD] "Megatron distributed optimizer and ZeRO", gitcode.csdn.net/69f2000254b52172bc70cc37
  *
- * Parity pins (tests/test_oracle_*.py) and the one function left unpinned are listed in
- * zero_oracle.c next to each function.
+ * The parity pins of each function (tests/test_oracle_*.py) are listed in zero_oracle.c;
+ * no function is left without one.
  */
 #ifndef ZERO_ORACLE_H
 #define ZERO_ORACLE_H
