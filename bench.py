@@ -9,9 +9,16 @@ set is far larger than the 129 MB L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
---impl reference times the CPU oracle (the build's own baseline) on bounded samples of the
-same workload on the host cores.  Under torchrun (N > 1) every rank runs its own replica
-of the single-GPU step (weak scaling, no collective); rank 0 prints one JSON line.
+The same line carries the Llama-7B buffer (ZeRO-3, 51 gradient buckets) and the
+1,000,003-parameter fp16 workload under `workloads`, each timed by the same code after the
+previous workload's buffers are freed, and an end-to-end figure (`e2e`) through
+zero_step_host with the gradient copies in pinned host memory.  --impl reference times the
+CPU oracle (the build's own baseline) on bounded samples of the same workload on the host
+cores.  Under torchrun (N > 1) the workload's ranks are spread over the N processes, one
+GPU each, and exchange over torch.distributed (ranks.RankStep: the gradient copies window
+by window, the norm's partials and overflow flag, the gathered parameters); the whole job
+updates the workload's parameters once per step (strong scaling), and rank 0 prints one
+JSON line with the maximum time over ranks.
 """
 from __future__ import annotations
 
