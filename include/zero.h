@@ -139,7 +139,11 @@ typedef struct zero_step_state {
                                when it was skipped, 0 before the first step; the single
                                launch hands it to its blocks together with
                                launch_arrivals in one 64-bit store */
-    uint32_t reserved[8];
+    uint64_t adamw_next_chunk; /* internal to the AdamW pass: the next chunk its blocks
+                               take (0 between steps; keep it 0 when writing a state) */
+    uint32_t adamw_done;    /* internal to the AdamW pass: its blocks that have finished;
+                               the last one puts both words back to 0 */
+    uint32_t reserved[5];
 } zero_step_state_t;        /* 128 bytes */
 
 /* -------------------------------------------------------------------------------------

@@ -60,7 +60,8 @@ int main(void)
     FIELD(step_size); FIELD(rbc2); FIELD(decay); FIELD(overflow); FIELD(skip); FIELD(t);
     FIELD(good_steps); FIELD(growth_interval); FIELD(dynamic); FIELD(n_ranks); FIELD(n_steps);
     FIELD(n_skipped); FIELD(error); FIELD(arrivals); FIELD(inv_scale_used);
-    FIELD(launch_arrivals); FIELD(applied_c); FIELD(reserved);
+    FIELD(launch_arrivals); FIELD(applied_c); FIELD(adamw_next_chunk); FIELD(adamw_done);
+    FIELD(reserved);
 #undef FIELD
     printf("state_size %zu\n", sizeof(zero_step_state_t));
     printf("ok\n");

@@ -25,7 +25,7 @@ pytestmark = pytest.mark.gpu
 
 
 def test_adamw_wait_runs_out_reports_error_and_gpu_stays_usable(hooked):
-    # every block owns at least 3 chunks of 4096 elements
+    # 3 chunks of 4096 elements per block on average (the blocks take them from a queue)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     wl = W.scaled(W.C2, sms * 4096 * 3 + 123, steps=1)
     gpu = GpuRun(wl, guarded=False)
@@ -35,7 +35,7 @@ def test_adamw_wait_runs_out_reports_error_and_gpu_stays_usable(hooked):
                                 gpu.st)
     z.zero_grad_norm(gpu.lay, gpu.hp, gpu.partials, gpu.st)
     assert gpu.state().error == 0
-    assert hooked.zero_test_withhold_adamw_chunk(sms + 5) == 0  # block 5's second chunk
+    assert hooked.zero_test_withhold_adamw_chunk(sms + 5) == 0  # whichever block takes it
     t0 = time.time()
     rc = hooked.zero_adamw_cast_gather(C.byref(gpu.lay), C.byref(gpu.hp), gpu.g.data_ptr(),
                                        gpu.master.data_ptr(), gpu.m.data_ptr(), gpu.v.data_ptr(),
@@ -48,6 +48,9 @@ def test_adamw_wait_runs_out_reports_error_and_gpu_stays_usable(hooked):
     s = gpu.state()
     assert s.error == 1, s.error
     assert 1.0 < waited < 60.0, waited
+    # the block that gave up still counted itself done, so the last block put the chunk
+    # queue back to 0 for the next launch
+    assert (s.adamw_next_chunk, s.adamw_done) == (0, 0), (s.adamw_next_chunk, s.adamw_done)
     # the context is still good: a full step through the product library matches the oracle
     wl2 = W.scaled(W.C2, 300_007, steps=1)
     fresh = GpuRun(wl2)

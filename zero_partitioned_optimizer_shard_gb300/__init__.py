@@ -56,7 +56,8 @@ class StepState(C.Structure):
         ("dynamic", C.c_uint32), ("n_ranks", C.c_uint32), ("n_steps", C.c_uint32),
         ("n_skipped", C.c_uint32), ("error", C.c_uint32), ("arrivals", C.c_uint32),
         ("inv_scale_used", C.c_float), ("launch_arrivals", C.c_uint32),
-        ("applied_c", C.c_float), ("reserved", C.c_uint32 * 8),
+        ("applied_c", C.c_float), ("adamw_next_chunk", C.c_uint64), ("adamw_done", C.c_uint32),
+        ("reserved", C.c_uint32 * 5),
     ]
 
 

@@ -43,11 +43,14 @@ namespace {
 __device__ unsigned long long zero_test_withheld_chunk = ~0ull;
 #endif
 
+constexpr uint64_t kNoChunk = ~0ull;  // a stage with no chunk: the queue is empty
+
 template <bool F16, bool EF>
 __global__ void __launch_bounds__(kBlock, 1) k_adamw(const __grid_constant__ AdamwArgs a)
 {
     extern __shared__ __align__(128) float ring[];  // kStages x {g, master, m, v} x kChunk
     __shared__ __align__(8) uint64_t full[kStages];
+    __shared__ uint64_t s_chunk[kStages];  // the chunk each stage holds, or kNoChunk
     grid_dependency_wait();
     const zero_step_state_t* st = a.st;
     if (st->skip)
@@ -70,9 +73,6 @@ __global__ void __launch_bounds__(kBlock, 1) k_adamw(const __grid_constant__ Ada
     const Scalars& s = s_sh;
 
     const uint64_t n_chunks = a.psi / kChunk;  // whole chunks, none holding padding
-    uint64_t mine = 0;                         // chunks of this block: blockIdx.x + i*gridDim.x
-    if (blockIdx.x < n_chunks)
-        mine = (n_chunks - 1 - blockIdx.x) / gridDim.x + 1;
     const float* src[4] = {a.g, a.master, a.m, a.v};
 
     if (threadIdx.x == 0) {
@@ -81,41 +81,61 @@ __global__ void __launch_bounds__(kBlock, 1) k_adamw(const __grid_constant__ Ada
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    auto issue = [&](uint64_t i) {  // chunk i of this block into stage i % kStages
-        const int k = (int)(i % kStages);
-        const uint64_t base = (blockIdx.x + i * gridDim.x) * (uint64_t)kChunk;
+    // Stage k gets chunk c: its index for the block (published by the barrier's arrival),
+    // then the four bulk copies; past the last chunk, an arrival with no copies.
+    auto issue = [&](int k, uint64_t c) {
         const uint32_t bar = smem_addr(&full[k]);
+        if (c >= n_chunks) {
+            s_chunk[k] = kNoChunk;
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+            return;
+        }
+        s_chunk[k] = c;
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
                      ::"r"(bar), "r"((uint32_t)(4 * kChunk * sizeof(float))) : "memory");
 #ifdef ZERO_TEST_HOOKS
-        if (base / kChunk == zero_test_withheld_chunk)
+        if (c == zero_test_withheld_chunk)
             return;  // test builds only: this chunk's barrier never completes
 #endif
         for (int q = 0; q < 4; ++q)
-            bulk_load<EF>(smem_addr(ring + (k * 4 + q) * kChunk), src[q] + base,
+            bulk_load<EF>(smem_addr(ring + (k * 4 + q) * kChunk), src[q] + c * kChunk,
                           (uint32_t)(kChunk * sizeof(float)), bar);
     };
-    if (threadIdx.x == 0)
-        for (uint64_t i = 0; i < mine && i < kStages; ++i)
-            issue(i);
+    // Chunks are handed out in order by one counter in the step state, one at a time to
+    // the block that asks: the chunks in flight stay together at the front of the buffers
+    // however the blocks' speeds differ, and a faster block takes more of them.  (A fixed
+    // assignment, block b taking chunks b, b + gridDim.x, ..., let the blocks drift apart
+    // over long launches: 0.999 of the copy peak on the Llama-7B buffer in one launch,
+    // 1.031 in four.)  Thread 0 takes each chunk one refill ahead of its use, so the
+    // atomic's latency stays off the ring's path.
+    uint64_t ahead = 0;  // thread 0: the next chunk it will issue
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < kStages; ++k)
+            issue(k, atomicAdd(a.next_chunk, 1ull));
+        ahead = atomicAdd(a.next_chunk, 1ull);
+    }
 
-    for (uint64_t i = 0; i < mine; ++i) {
+    bool failed = false;
+    for (uint64_t i = 0;; ++i) {
         const int k = (int)(i % kStages);
         const uint32_t ok = wait_parity_bounded(smem_addr(&full[k]), (uint32_t)((i / kStages) & 1));
-        if (__syncthreads_or(!ok)) {  // the whole block leaves together
+        if (__syncthreads_or(!ok)) {  // the whole block leaves the ring together
             if (threadIdx.x == 0) {
                 atomicOr(a.err, 1u);
-                for (uint64_t j = i; j < mine && j < i + kStages; ++j)
+                for (uint64_t j = i; j < i + kStages; ++j)  // every stage was issued
                     wait_parity_bounded(smem_addr(&full[j % kStages]), (uint32_t)((j / kStages) & 1));
             }
-            __syncthreads();
-            return;
+            failed = true;
+            break;
         }
+        const uint64_t c = s_chunk[k];
+        if (c == kNoChunk)  // the queue ran dry: every later stage is empty too
+            break;
         const float* sg = ring + (k * 4 + 0) * kChunk;
         const float* sp = ring + (k * 4 + 1) * kChunk;
         const float* sm = ring + (k * 4 + 2) * kChunk;
         const float* sv = ring + (k * 4 + 3) * kChunk;
-        const uint64_t base = (blockIdx.x + i * gridDim.x) * (uint64_t)kChunk;
+        const uint64_t base = c * (uint64_t)kChunk;
 #pragma unroll
         for (int e = threadIdx.x * 4; e < kChunk; e += kBlock * 4) {
             const float4 g0 = *reinterpret_cast<const float4*>(sg + e);
@@ -130,15 +150,18 @@ __global__ void __launch_bounds__(kBlock, 1) k_adamw(const __grid_constant__ Ada
             __stcs(reinterpret_cast<float4*>(a.v + base + e), v0);
             __stcs(reinterpret_cast<uint2*>(a.out + base + e), o);
         }
-        __syncthreads();  // stage k fully read: refill it
-        if (threadIdx.x == 0 && i + kStages < mine)
-            issue(i + kStages);
+        __syncthreads();  // stage k fully read (and s_chunk[k] by every thread): refill it
+        if (threadIdx.x == 0) {
+            issue(k, ahead);
+            if (ahead < n_chunks)
+                ahead = atomicAdd(a.next_chunk, 1ull);
+        }
     }
 
     // the ragged end: after the last whole chunk, up to psi_padded (padding gets out = 0)
     const uint64_t stride = (uint64_t)gridDim.x * kBlock;
     const uint64_t tid = (uint64_t)blockIdx.x * kBlock + threadIdx.x;
-    for (uint64_t i = n_chunks * kChunk + tid; i < a.psi_padded; i += stride) {
+    for (uint64_t i = n_chunks * kChunk + tid; !failed && i < a.psi_padded; i += stride) {
         if (i < a.psi) {
             float p = a.master[i], m = a.m[i], v = a.v[i];
             const float r = adamw_one(a.g[i], p, m, v, s);
@@ -148,6 +171,16 @@ __global__ void __launch_bounds__(kBlock, 1) k_adamw(const __grid_constant__ Ada
             a.out[i] = pack1<F16>(r);
         } else {
             a.out[i] = 0;  // padding: gathered value 0, state untouched
+        }
+    }
+    // the queue back to 0 for the next launch, by the last block to finish (every block
+    // has taken its last chunk before it counts itself done)
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(a.done, 1u) == gridDim.x - 1) {
+            __threadfence();
+            atomicExch(a.next_chunk, 0ull);
+            atomicExch(a.done, 0u);
         }
     }
 }
@@ -163,6 +196,9 @@ extern "C" int zero_test_withhold_adamw_chunk(unsigned long long chunk)
 
 cudaError_t launch_adamw(const AdamwArgs& a, cudaStream_t s)
 {
+    // the kernel takes its chunks from the step state's queue and writes through these
+    if (!a.next_chunk || !a.done || !a.err)
+        return cudaErrorInvalidValue;
     static std::atomic<bool> configured[64];  // per device; a race only repeats the set-up
     int dev = 0;
     cudaGetDevice(&dev);

@@ -159,6 +159,7 @@ extern "C" int zero_step_static_workspace(const zero_layout_t* layout,
         return fail_cuda(e);
 
     zero::AdamwArgs u;
+    memset(&u, 0, sizeof u);
     u.g = g;
     u.master = master;
     u.m = m;
@@ -166,6 +167,8 @@ extern "C" int zero_step_static_workspace(const zero_layout_t* layout,
     u.out = params;
     u.st = st;
     u.err = &st->error;
+    u.next_chunk = reinterpret_cast<unsigned long long*>(&st->adamw_next_chunk);
+    u.done = &st->adamw_done;
     u.psi = layout->psi;
     u.psi_padded = P;
     u.beta1 = hp->beta1;

@@ -42,6 +42,8 @@ struct AdamwArgs {
     uint16_t* out;
     const zero_step_state_t* st;
     uint32_t* err;                           // the state's error word (bounded waits)
+    unsigned long long* next_chunk;          // the state's adamw_next_chunk (k_adamw's queue)
+    uint32_t* done;                          // the state's adamw_done
     uint64_t psi, psi_padded;
     float beta1, beta2, eps;
     uint32_t out_f16;                        // gathered parameters as fp16 instead of bf16
@@ -52,6 +54,7 @@ struct AdamwArgs {
 };
 
 static_assert(sizeof(zero_step_state_t) == 128, "the step state is 128 bytes");
+static_assert(offsetof(zero_step_state_t, adamw_next_chunk) % 8 == 0, "the chunk queue is 8-byte aligned");
 // the single launch's arrival counter and the step's outcome form one 64-bit word
 // (counter in the low half), written at once when the last block releases the others
 static_assert(offsetof(zero_step_state_t, launch_arrivals) % 8 == 0 &&
