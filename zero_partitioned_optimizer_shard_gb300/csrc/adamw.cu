@@ -43,8 +43,6 @@ namespace {
 __device__ unsigned long long zero_test_withheld_chunk = ~0ull;
 #endif
 
-constexpr uint64_t kNoChunk = ~0ull;  // a stage with no chunk: the queue is empty
-
 template <bool F16, bool EF>
 __global__ void __launch_bounds__(kBlock, 1) k_adamw(const __grid_constant__ AdamwArgs a)
 {

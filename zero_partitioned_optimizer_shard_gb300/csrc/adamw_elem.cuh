@@ -104,6 +104,7 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 constexpr int kChunk = 4096;  // elements per bulk-copied chunk of each array
 constexpr int kStages = 3;
 constexpr size_t kSmemBytes = (size_t)kStages * 4 * kChunk * sizeof(float);  // 192 KiB
+constexpr uint64_t kNoChunk = ~0ull;  // a ring stage with no chunk: the chunk queue is empty
 
 }  // namespace
 }  // namespace zero

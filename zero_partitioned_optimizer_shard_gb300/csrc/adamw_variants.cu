@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(kBlock, 1) k_adamw_rereduce(const __grid_const
 {
     extern __shared__ __align__(128) float ring[];  // kStages x {x0|x1, master, m, v} x kChunk
     __shared__ __align__(8) uint64_t full[kStages];
+    __shared__ uint64_t s_chunk[kStages];  // the chunk each stage holds, or kNoChunk
     grid_dependency_wait();
     const zero_step_state_t* st = a.st;
     if (st->skip)
@@ -63,9 +64,6 @@ __global__ void __launch_bounds__(kBlock, 1) k_adamw_rereduce(const __grid_const
     const float inv = s_inv;
 
     const uint64_t n_chunks = a.psi / kChunk;
-    uint64_t mine = 0;
-    if (blockIdx.x < n_chunks)
-        mine = (n_chunks - 1 - blockIdx.x) / gridDim.x + 1;
 
     if (threadIdx.x == 0) {
         for (int k = 0; k < kStages; ++k)
@@ -73,10 +71,17 @@ __global__ void __launch_bounds__(kBlock, 1) k_adamw_rereduce(const __grid_const
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    auto issue = [&](uint64_t i) {  // chunk i of this block into stage i % kStages
-        const int k = (int)(i % kStages);
-        const uint64_t base = (blockIdx.x + i * gridDim.x) * (uint64_t)kChunk;
+    // chunks from the step state's queue, as in k_adamw: stage k gets chunk c (its index
+    // published by the barrier's arrival), or, past the last chunk, an arrival alone
+    auto issue = [&](int k, uint64_t c) {
         const uint32_t bar = smem_addr(&full[k]);
+        if (c >= n_chunks) {
+            s_chunk[k] = kNoChunk;
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+            return;
+        }
+        s_chunk[k] = c;
+        const uint64_t base = c * (uint64_t)kChunk;
         float* stage = ring + k * 4 * kChunk;
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
                      ::"r"(bar), "r"((uint32_t)(4 * kChunk * sizeof(float))) : "memory");
@@ -87,29 +92,36 @@ __global__ void __launch_bounds__(kBlock, 1) k_adamw_rereduce(const __grid_const
         for (int q = 0; q < 5; ++q)
             bulk_load<EF>(smem_addr(dst[q]), src[q], bytes[q], bar);
     };
-    if (threadIdx.x == 0)
-        for (uint64_t i = 0; i < mine && i < kStages; ++i)
-            issue(i);
+    uint64_t ahead = 0;  // thread 0: the next chunk it will issue
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < kStages; ++k)
+            issue(k, atomicAdd(a.next_chunk, 1ull));
+        ahead = atomicAdd(a.next_chunk, 1ull);
+    }
 
-    for (uint64_t i = 0; i < mine; ++i) {
+    bool failed = false;
+    for (uint64_t i = 0;; ++i) {
         const int k = (int)(i % kStages);
         const uint32_t ok = wait_parity_bounded(smem_addr(&full[k]), (uint32_t)((i / kStages) & 1));
-        if (__syncthreads_or(!ok)) {  // the whole block leaves together
+        if (__syncthreads_or(!ok)) {  // the whole block leaves the ring together
             if (threadIdx.x == 0) {
                 atomicOr(a.err, 1u);
-                for (uint64_t j = i; j < mine && j < i + kStages; ++j)
+                for (uint64_t j = i; j < i + kStages; ++j)  // every stage was issued
                     wait_parity_bounded(smem_addr(&full[j % kStages]), (uint32_t)((j / kStages) & 1));
             }
-            __syncthreads();
-            return;
+            failed = true;
+            break;
         }
+        const uint64_t c = s_chunk[k];
+        if (c == kNoChunk)  // the queue ran dry: every later stage is empty too
+            break;
         const float* stage = ring + k * 4 * kChunk;
         const uint16_t* s0 = reinterpret_cast<const uint16_t*>(stage);
         const uint16_t* s1 = reinterpret_cast<const uint16_t*>(stage + kChunk / 2);
         const float* sp = stage + kChunk;
         const float* sm = stage + 2 * kChunk;
         const float* sv = stage + 3 * kChunk;
-        const uint64_t base = (blockIdx.x + i * gridDim.x) * (uint64_t)kChunk;
+        const uint64_t base = c * (uint64_t)kChunk;
 #pragma unroll
         for (int e = threadIdx.x * 4; e < kChunk; e += kBlock * 4) {
             const uint2 x0 = *reinterpret_cast<const uint2*>(s0 + e);
@@ -129,14 +141,17 @@ __global__ void __launch_bounds__(kBlock, 1) k_adamw_rereduce(const __grid_const
             __stcs(reinterpret_cast<float4*>(a.v + base + e), v0);
             __stcs(reinterpret_cast<uint2*>(a.out + base + e), o);
         }
-        __syncthreads();  // stage k fully read: refill it
-        if (threadIdx.x == 0 && i + kStages < mine)
-            issue(i + kStages);
+        __syncthreads();  // stage k fully read (and s_chunk[k] by every thread): refill it
+        if (threadIdx.x == 0) {
+            issue(k, ahead);
+            if (ahead < n_chunks)
+                ahead = atomicAdd(a.next_chunk, 1ull);
+        }
     }
 
     const uint64_t stride = (uint64_t)gridDim.x * kBlock;
     const uint64_t tid = (uint64_t)blockIdx.x * kBlock + threadIdx.x;
-    for (uint64_t i = n_chunks * kChunk + tid; i < a.psi_padded; i += stride) {
+    for (uint64_t i = n_chunks * kChunk + tid; !failed && i < a.psi_padded; i += stride) {
         if (i < a.psi) {
             float p = a.master[i], m = a.m[i], v = a.v[i];
             const float r = adamw_one(regather<DT>(a.rep0[i], a.rep1[i], inv), p, m, v, s);
@@ -146,6 +161,15 @@ __global__ void __launch_bounds__(kBlock, 1) k_adamw_rereduce(const __grid_const
             a.out[i] = pack1<F16>(r);
         } else {
             a.out[i] = 0;
+        }
+    }
+    // the queue back to 0 for the next launch, by the last block to finish
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(a.done, 1u) == gridDim.x - 1) {
+            __threadfence();
+            atomicExch(a.next_chunk, 0ull);
+            atomicExch(a.done, 0u);
         }
     }
 }
@@ -250,6 +274,9 @@ cudaError_t launch_rereduce_ef(const AdamwArgs& a, dim3 g, dim3 b, cudaStream_t 
 
 cudaError_t launch_adamw_rereduce(const AdamwArgs& a, cudaStream_t s)
 {
+    // the kernel takes its chunks from the step state's queue and writes through these
+    if (!a.next_chunk || !a.done || !a.err || !a.rep0 || !a.rep1)
+        return cudaErrorInvalidValue;
     static std::atomic<bool> configured[64];  // per device; a race only repeats the set-up
     int dev = 0;
     cudaGetDevice(&dev);

@@ -170,6 +170,8 @@ int adamw_rereduce(const zero_layout_t* L, const zero_adamw_hparams_t* hp, zero_
     a.out = params;
     a.st = st;
     a.err = const_cast<uint32_t*>(&st->error);
+    a.next_chunk = reinterpret_cast<unsigned long long*>(const_cast<uint64_t*>(&st->adamw_next_chunk));
+    a.done = const_cast<uint32_t*>(&st->adamw_done);
     a.psi = L->psi;
     a.psi_padded = L->psi_padded;
     a.beta1 = hp->beta1;
