@@ -651,22 +651,32 @@ def _fused_moved(N: int, lay, g_written: bool) -> int:
     return 26 + 2 * N + (4 if g_written else 0) + (2 if staged else 0)
 
 
+def kernel_code_hash(paths) -> str:
+    """sha256 of C++/CUDA sources with their comments and whitespace runs removed: it
+    changes when the code changes, not when a comment is edited."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
+    return h.hexdigest()
+
+
 def _traffic_from_profile(psi_padded):
     """DRAM bytes per k_adamw launch over psi_padded parameters from the committed ncu
     captures: a line slope * psi + intercept through three sizes (the intercept is the
     fixed amount of the launch's last writes still in L2 when it ends), or None when the
-    kernel source has changed since those counters were taken."""
-    import hashlib
+    kernel's code has changed since those counters were taken."""
     path = os.path.join(ROOT, "profiles", "k_adamw_traffic.json")
     csrc = os.path.join(ROOT, "zero_partitioned_optimizer_shard_gb300", "csrc")
     try:
         with open(path) as f:
             rec = json.load(f)
-        h = hashlib.sha256()
-        for name in ("adamw.cu", "adamw_elem.cuh"):  # k_adamw's whole source
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
-        sha = h.hexdigest()
+        sha = kernel_code_hash([os.path.join(csrc, n) for n in ("adamw.cu", "adamw_elem.cuh")])
         if not sha.startswith(rec["source_sha256_prefix"]):
             return None
         return round(rec["slope_bytes_per_param"] * psi_padded + rec["intercept_bytes"])

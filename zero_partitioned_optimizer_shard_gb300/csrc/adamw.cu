@@ -23,9 +23,9 @@
  * into a three-stage shared-memory ring tracked by mbarriers, so up to 192 KiB per SM are
  * in flight without holding registers.  On buffers many times larger than L2 the copies
  * carry an L2 evict-first policy (each input byte is read once), which keeps L2 for the
- * lines being written.  One 256-thread block per SM (persistent,
- * grid-stride over chunks) computes from shared memory and writes master, m, v and 8
- * bf16 parameters per thread with streaming 128/64-bit stores.  The ragged end (the part
+ * lines being written.  One 256-thread block per SM (persistent, taking its chunks in
+ * order from a queue in the step state) computes from shared memory and writes master,
+ * m, v and 8 bf16 parameters per thread with streaming 128/64-bit stores.  The ragged end (the part
  * after the last whole chunk, and the padding) is done element by element.  Every
  * mbarrier wait is bounded (~2 s); on a timeout the block records an error in the step
  * state, waits (bounded) for its copies in flight and leaves.
