@@ -89,7 +89,10 @@ class GpuRun:
                        self.stream.cuda_stream)
 
     def state(self) -> z.StepState:
-        return z.zero_step_state_read(self.st, self.stream)
+        s = z.zero_step_state_read(self.st, self.stream)
+        # between steps the AdamW passes' chunk queue is back at 0, on every path
+        assert (s.adamw_next_chunk, s.adamw_done) == (0, 0), (s.adamw_next_chunk, s.adamw_done)
+        return s
 
     def gen_grads(self, step: int) -> float:
         """Fill the N gradient copies for `step` at the current loss scale; returns L."""
