@@ -213,7 +213,9 @@ int zero_step_state_init(const zero_layout_t* layout, float loss_scale, uint32_t
 int zero_step_state_read(const zero_step_state_t* st, zero_step_state_t* host_out,
                          zero_stream_t stream);
 
-/* Copy a host state (e.g. from a checkpoint) to the device and wait for it. */
+/* Copy a host state (e.g. from a checkpoint) to the device and wait for it.  The
+ * kernels' internal counters (arrivals, launch_arrivals, adamw_next_chunk, adamw_done)
+ * are written as 0 whatever host_in holds. */
 int zero_step_state_write(zero_step_state_t* st, const zero_step_state_t* host_in,
                           zero_stream_t stream);
 

@@ -307,10 +307,16 @@ def test_determinism_bitwise():
         assert r[0] == results[0][0] and r[1] == results[0][1] and r[2] == results[0][2]
 
 
-def test_checkpoint_resume_bitwise():
-    """5 steps, save state + arrays, restore into fresh buffers, 5 more == 10 straight."""
-    wl = W.scaled(W.C5, 200_000, steps=10)
+@pytest.mark.parametrize("wl", [W.scaled(W.C5, 200_000, steps=10),
+                                replace(W.scaled(W.C2, 8 * 8192 * 200 + 5, steps=10), n_ranks=8)],
+                         ids=["single-launch", "three-launch"])
+def test_checkpoint_resume_bitwise(wl):
+    """5 steps, save state + arrays, restore into fresh buffers, 5 more == 10 straight.  The
+    saved state is written back with garbage in the kernels' internal counters, which
+    zero_step_state_write must clear (the harness checks the chunk queue reads 0)."""
     a = GpuRun(wl)
+    dt = z.ZERO_F16 if wl.grad_dtype == "f16" else z.ZERO_BF16
+    assert (z.zero_step_launches(a.lay, dt) == 1) == (wl.psi < 1_000_000)
     for s in range(1, 11):
         a.step(s)
     b = GpuRun(wl)
@@ -321,7 +327,11 @@ def test_checkpoint_resume_bitwise():
     c = GpuRun(wl)
     for k, t in arrs.items():
         getattr(c, k).copy_(t)
+    saved.arrivals, saved.launch_arrivals = 7, 9
+    saved.adamw_next_chunk, saved.adamw_done = 12345, 3
     z.zero_step_state_write(c.st, saved)
+    back = c.state()
+    assert (back.arrivals, back.launch_arrivals) == (0, 0)
     for s in range(6, 11):
         c.step(s)
     x, y = a.arrays(), c.arrays()

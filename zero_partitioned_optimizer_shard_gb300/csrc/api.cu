@@ -323,9 +323,16 @@ extern "C" int zero_step_state_write(zero_step_state_t* st, const zero_step_stat
         return ZERO_EINVAL;
     if (!aligned16(st))
         return ZERO_EALIGN;
-    cudaError_t e = cudaMemcpyAsync(st, host_in, sizeof *st, cudaMemcpyHostToDevice, (cudaStream_t)stream);
+    // the kernels' internal counters start every step at 0, whatever the copy holds (a
+    // stale chunk counter would make the AdamW pass skip chunks)
+    zero_step_state_t s = *host_in;
+    s.arrivals = 0;
+    s.launch_arrivals = 0;
+    s.adamw_next_chunk = 0;
+    s.adamw_done = 0;
+    cudaError_t e = cudaMemcpyAsync(st, &s, sizeof s, cudaMemcpyHostToDevice, (cudaStream_t)stream);
     if (e == cudaSuccess)
-        e = cudaStreamSynchronize((cudaStream_t)stream);
+        e = cudaStreamSynchronize((cudaStream_t)stream);  // s lives until the copy is done
     return cuda_status(e);
 }
 
